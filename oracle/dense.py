@@ -1,0 +1,138 @@
+"""Dense float64 attention: the plain definition (oracle; test infrastructure only).
+
+The method computes, up to rounding order, exactly the dense softmax attention
+("Exact tiled softmax attention with block-recomputed vector-Jacobian
+products", Inputs: "exact real arithmetic"; "txf-modern-flash-attention",
+Constraints: the same output for every block size).  So the oracle is that
+definition written out, one (batch, head) slice at a time, in float64:
+
+  s_ij = c * <Q_i, K_j>            for j in A_i, and -inf otherwise
+  m_i  = max_j s_ij,   l_i = sum_j exp(s_ij - m_i),   p_ij = exp(s_ij - m_i) / l_i
+  Y    = P V,          L_i = m_i + ln l_i           (the retained statistic)
+
+and the vector-Jacobian product for an upstream G = dY with the statistics held
+fixed (Reverse procedure of the same page; "python-flash-attention-online-
+softmax-block-recompute", The fix, item 2):
+
+  dV = P^T G,   dP = G V^T,   delta_i = sum_j p_ij dP_ij,
+  dS = P o (dP - delta),   dQ = c dS K,   dK = c dS^T Q.
+
+delta is formed from P and dP, NOT as G_i . Y_i, so that the identity
+delta_i = G_i . Y_i (HarshvardhanJ/FlashAttention, backward section) stays a
+real check on it.  Rows of S are always formed whole; rows are only processed
+in groups to bound memory.  No online recurrence appears here.
+"""
+import numpy as np
+
+from .masks import allowed_matrix
+
+ROW_GROUP = 1024
+
+
+def _check_rows(allowed):
+    if not allowed.any(axis=1).all():
+        raise ValueError("every allowed-key set A_i must be nonempty")
+
+
+def head_forward(Q, K, V, c, allowed):
+    """One head. Q [n,d], K [n,d], V [n,v] float64; allowed [n,n] bool -> (Y, L)."""
+    _check_rows(allowed)
+    n = Q.shape[0]
+    Y = np.empty((n, V.shape[1]))
+    L = np.empty(n)
+    for r0 in range(0, n, ROW_GROUP):
+        r1 = min(n, r0 + ROW_GROUP)
+        s = c * (Q[r0:r1] @ K.T)
+        s = np.where(allowed[r0:r1], s, -np.inf)
+        m = s.max(axis=1)
+        e = np.exp(s - m[:, None])
+        l = e.sum(axis=1)
+        Y[r0:r1] = (e / l[:, None]) @ V
+        L[r0:r1] = m + np.log(l)
+    return Y, L
+
+
+def head_probabilities(Q, K, c, allowed):
+    """One head: the full probability matrix P [n,n] (small cases only)."""
+    _check_rows(allowed)
+    s = np.where(allowed, c * (Q @ K.T), -np.inf)
+    m = s.max(axis=1)
+    e = np.exp(s - m[:, None])
+    return e / e.sum(axis=1)[:, None]
+
+
+def head_backward(Q, K, V, G, c, allowed):
+    """One head. Returns (dQ, dK, dV, delta) for the upstream G [n,v]."""
+    _check_rows(allowed)
+    n = Q.shape[0]
+    dQ = np.zeros_like(Q)
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    delta = np.empty(n)
+    for r0 in range(0, n, ROW_GROUP):
+        r1 = min(n, r0 + ROW_GROUP)
+        s = c * (Q[r0:r1] @ K.T)
+        s = np.where(allowed[r0:r1], s, -np.inf)
+        m = s.max(axis=1)
+        e = np.exp(s - m[:, None])
+        P = e / e.sum(axis=1)[:, None]
+        Gr = G[r0:r1]
+        dV += P.T @ Gr
+        dP = Gr @ V.T
+        dl = (P * dP).sum(axis=1)
+        dS = P * (dP - dl[:, None])
+        dQ[r0:r1] = c * (dS @ K)
+        dK += c * (dS.T @ Q[r0:r1])
+        delta[r0:r1] = dl
+    return dQ, dK, dV, delta
+
+
+def _heads(x):
+    """View [..., n, f] as [heads, n, f]."""
+    return x.reshape(-1, x.shape[-2], x.shape[-1])
+
+
+def forward(Q, K, V, c, mask_kind, window=0, bitmask=None, heads=None):
+    """Batched forward over [B,H,n,*] float64 arrays -> (Y [B,H,n,v], L [B,H,n]).
+
+    ``heads`` (optional) is a list of flat (b*H + h) indices; only those heads
+    are computed and the result has a leading axis of len(heads).
+    """
+    n = Q.shape[-2]
+    allowed = allowed_matrix(n, mask_kind, window, bitmask)
+    q, k, vv = _heads(Q), _heads(K), _heads(V)
+    idx = range(q.shape[0]) if heads is None else heads
+    out = [head_forward(q[h], k[h], vv[h], c, allowed) for h in idx]
+    Y = np.stack([o[0] for o in out])
+    L = np.stack([o[1] for o in out])
+    if heads is None:
+        Y = Y.reshape(V.shape[:-2] + Y.shape[-2:])
+        L = L.reshape(Q.shape[:-1])
+    return Y, L
+
+
+def backward(Q, K, V, G, c, mask_kind, window=0, bitmask=None, heads=None):
+    """Batched reverse pass -> (dQ, dK, dV, delta), same layout rules as ``forward``."""
+    n = Q.shape[-2]
+    allowed = allowed_matrix(n, mask_kind, window, bitmask)
+    q, k, vv, g = _heads(Q), _heads(K), _heads(V), _heads(G)
+    idx = range(q.shape[0]) if heads is None else heads
+    out = [head_backward(q[h], k[h], vv[h], g[h], c, allowed) for h in idx]
+    res = [np.stack([o[t] for o in out]) for t in range(4)]
+    if heads is None:
+        res[0] = res[0].reshape(Q.shape)
+        res[1] = res[1].reshape(K.shape)
+        res[2] = res[2].reshape(V.shape)
+        res[3] = res[3].reshape(Q.shape[:-1])
+    return tuple(res)
+
+
+def row_forward(Q, K, V, c, allowed_row, i):
+    """A single output row Y_i and L_i of one head (for sampled full-size checks)."""
+    if not allowed_row.any():
+        raise ValueError("every allowed-key set A_i must be nonempty")
+    s = np.where(allowed_row, c * (K @ Q[i]), -np.inf)
+    m = s.max()
+    e = np.exp(s - m)
+    l = e.sum()
+    return (e @ V) / l, m + np.log(l)

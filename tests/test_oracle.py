@@ -1,0 +1,456 @@
+"""Pins for the float64 oracle (CPU only).
+
+Each pin ties the oracle to something other than itself: hand-worked values
+(re-derived here with exact rationals), the pages' own block procedures at
+every block size, a library routine (torch's float64 scaled-dot-product
+attention and autograd), central finite differences, and invariants that the
+mathematics fixes.  ``test_planted_mistakes_are_caught`` plants typical mistakes
+in a copy of the oracle and checks that the same pins reject every one.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import dense, masks, tiled
+from workloads import pack_bitmask
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_cases.json")
+KINDS = {"none": masks.NONE, "causal": masks.CAUSAL}
+
+
+def _expr(x):
+    """Evaluate a fixture entry: a number or an expression in rationals and ln(k)."""
+    if isinstance(x, (int, float)):
+        return float(x)
+    return float(eval(x, {"__builtins__": {}}, {"ln": math.log}))
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _rel(a, b):
+    """Normwise relative error max|a-b| / max|b|."""
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
+
+
+# --------------------------------------------------------------------------- #
+# Hand-worked cases (re-derived exactly, then compared with the fixture)
+# --------------------------------------------------------------------------- #
+
+def test_hand_cases_rederived_exactly():
+    """The 3x3 Q=0 case has rational outputs: re-derive them with Fractions."""
+    V = [Fraction(1), Fraction(2), Fraction(3)]
+    K = [Fraction(1), Fraction(0), Fraction(-1)]
+    G = [Fraction(1)] * 3
+    Y, dQ = [], []
+    dV = [Fraction(0)] * 3
+    for i in range(3):
+        p = [Fraction(1, i + 1) if j <= i else Fraction(0) for j in range(3)]
+        y = sum(p[j] * V[j] for j in range(3))
+        Y.append(y)
+        gam = [p[j] * (G[i] * V[j] - G[i] * y) for j in range(3)]
+        dQ.append(sum(gam[j] * K[j] for j in range(3)))
+        for j in range(3):
+            dV[j] += p[j] * G[i]
+    case = json.load(open(GOLDEN))["cases"][2]
+    assert [Fraction(s) for s in case["Y"]] == Y
+    assert [Fraction(s) for s in case["dQ"]] == dQ
+    assert [Fraction(s) for s in case["dV"]] == dV
+    # 2x2 full: p_11 = 2/3 (e^{ln 2} = 2 against e^0 = 1), p_21 = 1/2.
+    p = [[Fraction(2, 3), Fraction(1, 3)], [Fraction(1, 2), Fraction(1, 2)]]
+    Vv = [Fraction(1), Fraction(0)]
+    Yf = [sum(p[i][j] * Vv[j] for j in range(2)) for i in range(2)]
+    gam = [[p[i][j] * (Vv[j] - Yf[i]) for j in range(2)] for i in range(2)]
+    case = json.load(open(GOLDEN))["cases"][0]
+    assert [Fraction(s) for s in case["Y"]] == Yf
+    # dK_j = sum_i gamma_ij Q_i with Q = (1, 0)
+    assert [Fraction(s) for s in case["dK"]] == [gam[0][0], gam[0][1]]
+    assert [Fraction(s) for s in case["dV"]] == [p[0][j] + p[1][j] for j in range(2)]
+    # dQ_i = gamma_i1 * ln 2 (K_2 = 0): coefficients 2/9 and 1/4
+    assert gam[0][0] == Fraction(2, 9) and gam[1][0] == Fraction(1, 4)
+
+
+def _hand_failures(head_forward, head_backward):
+    out = []
+    for case in json.load(open(GOLDEN))["cases"]:
+        arr = {k: np.array([[_expr(x) for x in row] for row in case[k]])
+               for k in ("Q", "K", "V", "G")}
+        n = arr["Q"].shape[0]
+        allowed = masks.allowed_matrix(n, KINDS[case["mask"]])
+        Y, L = head_forward(arr["Q"], arr["K"], arr["V"], case["c"], allowed)
+        dQ, dK, dV = head_backward(arr["Q"], arr["K"], arr["V"], arr["G"], case["c"],
+                                   allowed)[:3]
+        got = {"Y": Y[:, 0], "L": L, "dQ": dQ[:, 0], "dK": dK[:, 0], "dV": dV[:, 0]}
+        for key, val in got.items():
+            want = np.array([_expr(x) for x in case[key]])
+            if not np.allclose(val, want, rtol=0, atol=1e-14):
+                out.append(f"hand case '{case['name']}' {key}: {val} != {want}")
+    return out
+
+
+# --------------------------------------------------------------------------- #
+# Pins shared by the real oracle and the planted-mistake copies
+# --------------------------------------------------------------------------- #
+
+def _fd_failures(head_forward, head_backward, self_attention=False):
+    """Central differences of f = <G, Y> against the reverse pass, rel err <= 1e-5."""
+    out = []
+    r = _rng(11)
+    for kind, n, d, v, c in [(masks.NONE, 3, 2, 3, 0.7), (masks.CAUSAL, 4, 3, 2, 1.3)]:
+        allowed = masks.allowed_matrix(n, kind)
+        Q, K, V = r.normal(size=(n, d)), r.normal(size=(n, d)), r.normal(size=(n, v))
+        G = r.normal(size=(n, v))
+        if self_attention:
+            X = r.normal(size=(n, d))
+            G = r.normal(size=(n, d))
+            Q = K = V = X
+        dQ, dK, dV = head_backward(Q, K, V, G, c, allowed)[:3]
+        h = 1e-6
+
+        def f(q, k, vv):
+            return float((G * head_forward(q, k, vv, c, allowed)[0]).sum())
+
+        if self_attention:
+            num = np.zeros_like(X)
+            for idx in np.ndindex(*X.shape):
+                e = np.zeros_like(X)
+                e[idx] = h
+                num[idx] = (f(X + e, X + e, X + e) - f(X - e, X - e, X - e)) / (2 * h)
+            err = _rel(dQ + dK + dV, num)
+            if err > 1e-5:
+                out.append(f"finite differences, shared X: rel err {err:.2e}")
+            continue
+        for name, grad, which in (("dQ", dQ, 0), ("dK", dK, 1), ("dV", dV, 2)):
+            base = [Q, K, V]
+            num = np.zeros_like(base[which])
+            for idx in np.ndindex(*base[which].shape):
+                e = np.zeros_like(base[which])
+                e[idx] = h
+                plus = [x.copy() for x in base]
+                minus = [x.copy() for x in base]
+                plus[which] += e
+                minus[which] -= e
+                num[idx] = (f(*plus) - f(*minus)) / (2 * h)
+            err = _rel(grad, num)
+            if err > 1e-5:
+                out.append(f"finite differences {name} (kind {kind}): rel err {err:.2e}")
+    return out
+
+
+def _torch_failures(head_forward, head_backward):
+    """torch's float64 scaled_dot_product_attention + autograd + logsumexp."""
+    out = []
+    r = _rng(5)
+    for kind, n, d, v, c in [(masks.NONE, 37, 8, 5, 0.31), (masks.CAUSAL, 41, 6, 9, 1.7),
+                             (masks.WINDOW, 29, 4, 4, 0.5), (masks.BITMASK, 33, 7, 3, 0.9)]:
+        bitmask = None
+        if kind == masks.BITMASK:
+            a = r.random((n, n)) < 0.3
+            np.fill_diagonal(a, True)
+            bitmask = pack_bitmask(a)
+        allowed = masks.allowed_matrix(n, kind, window=5, bitmask=bitmask)
+        Q, K, V = r.normal(size=(n, d)), r.normal(size=(n, d)), r.normal(size=(n, v))
+        G = r.normal(size=(n, v))
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (Q, K, V))
+        tm = torch.tensor(allowed)
+        ty = torch.nn.functional.scaled_dot_product_attention(
+            tq[None], tk[None], tv[None], attn_mask=tm, scale=c)[0]
+        (ty * torch.tensor(G)).sum().backward()
+        s = (tq @ tk.T * c).masked_fill(~tm, float("-inf"))
+        tL = torch.logsumexp(s, dim=1)
+        Y, L = head_forward(Q, K, V, c, allowed)
+        dQ, dK, dV = head_backward(Q, K, V, G, c, allowed)[:3]
+        for name, mine, ref in (("Y", Y, ty.detach().numpy()), ("L", L, tL.detach().numpy()),
+                                ("dQ", dQ, tq.grad.numpy()), ("dK", dK, tk.grad.numpy()),
+                                ("dV", dV, tv.grad.numpy())):
+            err = _rel(mine, ref)
+            if err > 1e-12:
+                out.append(f"torch cross-check {name} (kind {kind}): rel err {err:.2e}")
+    return out
+
+
+def _invariant_failures(head_forward, head_backward):
+    out = []
+    r = _rng(7)
+    n, d, v, c = 23, 5, 4, 0.8
+    for kind in (masks.NONE, masks.CAUSAL, masks.WINDOW):
+        allowed = masks.allowed_matrix(n, kind, window=4)
+        Q, K, V = r.normal(size=(n, d)), r.normal(size=(n, d)), r.normal(size=(n, v))
+        G = r.normal(size=(n, v))
+        Y, L = head_forward(Q, K, V, c, allowed)
+        dQ, dK, dV, delta = head_backward(Q, K, V, G, c, allowed)
+        # Y_i is a convex combination of the allowed V_j: inside their column range.
+        for i in range(n):
+            Va = V[allowed[i]]
+            if (Y[i] < Va.min(0) - 1e-12).any() or (Y[i] > Va.max(0) + 1e-12).any():
+                out.append(f"Y row {i} outside the hull of its allowed values")
+                break
+        # delta_i = G_i . Y_i (the D identity of the backward section).
+        if _rel(delta, (G * Y).sum(1)) > 1e-12:
+            out.append("delta != G.Y")
+        # sum_j gamma_ij = 0  =>  sum_j dK_j = 0;  sum_j p_ij = 1  =>  sum_j dV_j = sum_i G_i.
+        if np.abs(dK.sum(0)).max() > 1e-12 * max(1.0, np.abs(dK).max()):
+            out.append("sum_j dK_j != 0")
+        if _rel(dV.sum(0), G.sum(0)) > 1e-12:
+            out.append("sum_j dV_j != sum_i G_i")
+        # Adding a constant row w to every V_j shifts Y by w and leaves dQ, dK alone.
+        w = r.normal(size=v)
+        Y2, L2 = head_forward(Q, K, V + w, c, allowed)
+        dQ2, dK2 = head_backward(Q, K, V + w, G, c, allowed)[:2]
+        if _rel(Y2, Y + w) > 1e-12 or _rel(L2, L) > 1e-14:
+            out.append("V + 1w^T does not shift Y by w")
+        if _rel(dQ2, dQ) > 1e-10 or _rel(dK2, dK) > 1e-10:
+            out.append("V + 1w^T changes dQ or dK")
+        # Scale: (Q a, c / a) gives the same scores.
+        Y3 = head_forward(Q * 2.5, K, V, c / 2.5, allowed)[0]
+        if _rel(Y3, Y) > 1e-12:
+            out.append("scale c not applied to <Q_i, K_j>")
+        # Logsumexp: L_i >= max allowed score and L_i <= max + ln|A_i|.
+        s = np.where(allowed, c * Q @ K.T, -np.inf)
+        smax = s.max(1)
+        if (L < smax - 1e-12).any() or (L > smax + np.log(allowed.sum(1)) + 1e-12).any():
+            out.append("L outside [max s, max s + ln|A_i|]")
+    # Full mask: permuting the keys (with their values) leaves Y unchanged and
+    # permutes dK and dV the same way.
+    allowed = np.ones((n, n), dtype=bool)
+    Q, K, V = r.normal(size=(n, d)), r.normal(size=(n, d)), r.normal(size=(n, v))
+    G = r.normal(size=(n, v))
+    perm = r.permutation(n)
+    Y = head_forward(Q, K, V, c, allowed)[0]
+    Yp = head_forward(Q, K[perm], V[perm], c, allowed)[0]
+    dK, dV = head_backward(Q, K, V, G, c, allowed)[1:3]
+    dKp, dVp = head_backward(Q, K[perm], V[perm], G, c, allowed)[1:3]
+    if _rel(Yp, Y) > 1e-12 or _rel(dKp, dK[perm]) > 1e-10 or _rel(dVp, dV[perm]) > 1e-12:
+        out.append("key permutation equivariance broken")
+    return out
+
+
+def _special_failures(head_forward, head_backward):
+    out = []
+    r = _rng(9)
+    n, d, v, c = 9, 3, 4, 0.6
+    Q, K, V = r.normal(size=(n, d)), r.normal(size=(n, d)), r.normal(size=(n, v))
+    G = r.normal(size=(n, v))
+    # One allowed key per row (a permutation): Y_i = V_pi(i), L_i = s_i,pi(i), dQ = 0.
+    pi = r.permutation(n)
+    allowed = np.zeros((n, n), dtype=bool)
+    allowed[np.arange(n), pi] = True
+    Y, L = head_forward(Q, K, V, c, allowed)
+    dQ = head_backward(Q, K, V, G, c, allowed)[0]
+    if _rel(Y, V[pi]) > 1e-15:
+        out.append("single key: Y_i != V_j")
+    if _rel(L, c * (Q * K[pi]).sum(1)) > 1e-14:
+        out.append("single key: L_i != s_ij")
+    if np.abs(dQ).max() > 1e-15:
+        out.append("single key: dQ != 0")
+    # Q = 0 under the causal mask: uniform p = 1/|A_i|, L_i = ln |A_i|, Y_i = prefix mean.
+    allowed = masks.allowed_matrix(n, masks.CAUSAL)
+    Y, L = head_forward(np.zeros((n, d)), K, V, c, allowed)
+    if _rel(Y, np.cumsum(V, 0) / np.arange(1, n + 1)[:, None]) > 1e-14:
+        out.append("Q=0: Y != prefix mean")
+    if _rel(L, np.log(np.arange(1, n + 1))) > 1e-14:
+        out.append("Q=0: L != ln |A_i|")
+    return out
+
+
+def _tiled_failures(head_forward, head_backward):
+    """The page's block procedures agree with the definition under test."""
+    out = []
+    r = _rng(3)
+    n, d, v, c = 19, 4, 5, 0.9
+    for kind in (masks.NONE, masks.CAUSAL, masks.WINDOW):
+        allowed = masks.allowed_matrix(n, kind, window=6)
+        Q, K, V = r.normal(size=(n, d)), r.normal(size=(n, d)), r.normal(size=(n, v))
+        G = r.normal(size=(n, v))
+        Y, L = head_forward(Q, K, V, c, allowed)
+        Yt, m, l, Lt = tiled.summary_forward(Q, K, V, c, allowed, 4)
+        if _rel(Yt, Y) > 1e-12 or _rel(Lt, L) > 1e-12:
+            out.append(f"summary forward disagrees (kind {kind})")
+        got = head_backward(Q, K, V, G, c, allowed)[:3]
+        want = tiled.recompute_backward(Q, K, V, G, Yt, m, l, c, allowed, 4)[:3]
+        for name, a, b in zip(("dQ", "dK", "dV"), got, want):
+            if _rel(a, b) > 1e-11:
+                out.append(f"recompute backward {name} disagrees (kind {kind})")
+    return out
+
+
+def pin_failures(head_forward, head_backward):
+    return (_hand_failures(head_forward, head_backward)
+            + _fd_failures(head_forward, head_backward)
+            + _fd_failures(head_forward, head_backward, self_attention=True)
+            + _torch_failures(head_forward, head_backward)
+            + _invariant_failures(head_forward, head_backward)
+            + _special_failures(head_forward, head_backward)
+            + _tiled_failures(head_forward, head_backward))
+
+
+def test_oracle_passes_every_pin():
+    assert pin_failures(dense.head_forward, dense.head_backward) == []
+
+
+# --------------------------------------------------------------------------- #
+# Block-size exactness (O1) and the recompute reverse pass (O2)
+# --------------------------------------------------------------------------- #
+
+def _case(n, d, v, kind, seed, window=3, p=0.3):
+    r = _rng(seed)
+    bitmask = None
+    if kind == masks.BITMASK:
+        a = r.random((n, n)) < p
+        np.fill_diagonal(a, True)
+        bitmask = pack_bitmask(a)
+    allowed = masks.allowed_matrix(n, kind, window=window, bitmask=bitmask)
+    return (r.normal(size=(n, d)), r.normal(size=(n, d)), r.normal(size=(n, v)),
+            r.normal(size=(n, v)), allowed)
+
+
+ALL_KINDS = (masks.NONE, masks.CAUSAL, masks.WINDOW, masks.BITMASK)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 7, 16, 33])
+@pytest.mark.parametrize("kind", ALL_KINDS)
+def test_every_block_size_gives_the_dense_result(n, kind):
+    Q, K, V, G, allowed = _case(n, 5, 3, kind, seed=100 + n)
+    c = 0.45
+    Y, L = dense.head_forward(Q, K, V, c, allowed)
+    for b in range(1, n + 1):
+        Ys, m, l, Ls = tiled.summary_forward(Q, K, V, c, allowed, b)
+        Yo, Lo = tiled.online_forward(Q, K, V, c, allowed, b)
+        assert _rel(Ys, Y) <= 1e-12 and _rel(Ls, L) <= 1e-12, b
+        assert _rel(Yo, Y) <= 1e-12 and _rel(Lo, L) <= 1e-12, b
+
+
+@pytest.mark.parametrize("kind", ALL_KINDS)
+def test_block_sizes_at_n256(kind):
+    Q, K, V, G, allowed = _case(256, 16, 12, kind, seed=256, window=40)
+    c = 0.25
+    Y, L = dense.head_forward(Q, K, V, c, allowed)
+    dQ, dK, dV, _ = dense.head_backward(Q, K, V, G, c, allowed)
+    for b in (1, 2, 3, 16, 31, 64, 100, 256):
+        Ys, m, l, Ls = tiled.summary_forward(Q, K, V, c, allowed, b)
+        assert _rel(Ys, Y) <= 1e-12 and _rel(Ls, L) <= 1e-12, b
+        got = tiled.recompute_backward(Q, K, V, G, Ys, m, l, c, allowed, b)
+        for a, ref in zip(got[:3], (dQ, dK, dV)):
+            assert _rel(a, ref) <= 1e-11, b
+
+
+def test_delta_identity_rowwise():
+    """sum_j p_ij dP_ij = G_i . Y_i per row (backward section, D identity)."""
+    for kind in ALL_KINDS:
+        Q, K, V, G, allowed = _case(64, 8, 8, kind, seed=21)
+        Y, _ = dense.head_forward(Q, K, V, 0.3, allowed)
+        delta = dense.head_backward(Q, K, V, G, 0.3, allowed)[3]
+        gy = (G * Y).sum(1)
+        assert np.all(np.abs(delta - gy) <= 1e-12 * np.maximum(1.0, np.abs(gy)))
+
+
+def test_batched_layout_matches_heads():
+    r = _rng(2)
+    Q, K, V, G = (r.normal(size=(2, 3, 10, 4)) for _ in range(4))
+    Y, L = dense.forward(Q, K, V, 0.5, masks.CAUSAL)
+    dQ, dK, dV, delta = dense.backward(Q, K, V, G, 0.5, masks.CAUSAL)
+    allowed = masks.allowed_matrix(10, masks.CAUSAL)
+    y, l = dense.head_forward(Q[1, 2], K[1, 2], V[1, 2], 0.5, allowed)
+    assert np.array_equal(Y[1, 2], y) and np.array_equal(L[1, 2], l)
+    g = dense.head_backward(Q[1, 2], K[1, 2], V[1, 2], G[1, 2], 0.5, allowed)
+    assert np.array_equal(dK[1, 2], g[1]) and np.array_equal(dV[1, 2], g[2])
+    Ys, Ls = dense.forward(Q, K, V, 0.5, masks.CAUSAL, heads=[5])
+    assert np.array_equal(Ys[0], y)
+    yi, li = dense.row_forward(Q[1, 2], K[1, 2], V[1, 2], 0.5, allowed[7], 7)
+    assert _rel(yi, y[7]) < 1e-15 and abs(li - l[7]) < 1e-15
+
+
+def test_empty_allowed_set_is_rejected():
+    allowed = np.ones((3, 3), dtype=bool)
+    allowed[1] = False
+    z = np.zeros((3, 2))
+    with pytest.raises(ValueError):
+        dense.head_forward(z, z, z, 1.0, allowed)
+    with pytest.raises(ValueError):
+        tiled.summary_forward(z, z, z, 1.0, allowed, 2)
+
+
+# --------------------------------------------------------------------------- #
+# Mask readings, checked by plain membership loops
+# --------------------------------------------------------------------------- #
+
+def test_mask_readings():
+    n = 45
+    for i in range(n):
+        for j in range(n):
+            assert masks.allowed_matrix(n, masks.CAUSAL)[i, j] == (j <= i)
+    win = masks.allowed_matrix(n, masks.WINDOW, window=7)
+    for i in range(n):
+        assert set(np.nonzero(win[i])[0]) == set(range(max(0, i - 6), i + 1))
+    r = _rng(4)
+    a = r.random((n, n)) < 0.4
+    words = pack_bitmask(a)
+    assert words.shape == (n, 2) and words.dtype == np.uint32
+    for i in range(n):
+        for j in range(n):
+            bit = (int(words[i, j // 32]) >> (j % 32)) & 1
+            assert bit == int(a[i, j])
+    assert np.array_equal(masks.allowed_matrix(n, masks.BITMASK, bitmask=words), a)
+    # A window wider than n is the causal mask.
+    assert np.array_equal(masks.allowed_matrix(n, masks.WINDOW, window=10 * n),
+                          masks.allowed_matrix(n, masks.CAUSAL))
+
+
+# --------------------------------------------------------------------------- #
+# Planted mistakes: a copy of the oracle with one fault at a time must fail a pin
+# --------------------------------------------------------------------------- #
+
+def _mutant(fault):
+    def fwd(Q, K, V, c, allowed):
+        cc = 1.0 if fault == "no_scale" else c
+        s = cc * (K @ Q.T) if fault == "transposed_scores" else cc * (Q @ K.T)
+        al = allowed.T if fault == "transposed_mask" else allowed
+        s = np.where(al, s, -np.inf)
+        m = s.max(1)
+        e = np.exp(s - m[:, None])
+        l = e.sum(1)
+        Y = (e / l[:, None]) @ V
+        L = np.log(l) if fault == "L_without_max" else m + np.log(l)
+        return Y, L
+
+    def bwd(Q, K, V, G, c, allowed):
+        s = np.where(allowed, c * (Q @ K.T), -np.inf)
+        e = np.exp(s - s.max(1)[:, None])
+        P = e / e.sum(1)[:, None]
+        dV = P @ G if fault == "dV_untransposed" else P.T @ G
+        dP = G @ V.T
+        delta = (P * dP).sum(1)
+        if fault == "no_delta":
+            delta = 0 * delta
+        if fault == "delta_sign":
+            delta = -delta
+        dS = P * (dP - delta[:, None])
+        dQ = c * (dS.T @ K) if fault == "dQ_transposed" else c * (dS @ K)
+        dK = dS.T @ Q if fault == "dK_no_scale" else c * (dS.T @ Q)
+        if fault == "dK_uses_K":
+            dK = c * (dS.T @ K)
+        return dQ, dK, dV, delta
+
+    return fwd, bwd
+
+
+FAULTS = ["no_scale", "transposed_scores", "transposed_mask", "L_without_max",
+          "dV_untransposed", "no_delta", "delta_sign", "dQ_transposed", "dK_no_scale",
+          "dK_uses_K"]
+
+
+def test_unfaulted_copy_passes():
+    assert pin_failures(*_mutant(None)) == []
+
+
+@pytest.mark.parametrize("fault", FAULTS)
+def test_planted_mistakes_are_caught(fault):
+    assert pin_failures(*_mutant(fault)), f"no pin caught {fault}"
