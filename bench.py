@@ -1,0 +1,417 @@
+"""Benchmark: exact masked attention, forward + reverse, on GB300.
+
+One step = attn_fwd + attn_bwd (every step of the path: forward kernel,
+delta, reverse kernel, dQ conversion) over one batch of the workload,
+default B=4, H=32, n=4096, d=v=128, bf16, causal (the training-shaped
+attention problem; inputs 4 x 134 MB, larger than the 129 MB L2, so no flush
+is needed between steps).
+
+Flop convention: forward 4 n^2 d per head (2 n^2 (d+v) when d != v), reverse
+2.5x the forward, both halved under the causal mask; for window and bitmask
+masks the algorithmic 2 |A| (d+v) is used instead (|A| = allowed pairs).
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def flops(w: workloads.Workload, allowed_pairs=None):
+    """(forward, reverse) flop counts of one step of workload ``w``."""
+    heads = w.B * w.H
+    if w.mask in ("none", "causal"):
+        f = 2.0 * w.n * w.n * (w.d + w.v) * heads
+        if w.mask == "causal":
+            f /= 2.0
+    else:
+        pairs = allowed_pairs if allowed_pairs is not None else w.allowed_pairs_per_head()
+        f = 2.0 * pairs * (w.d + w.v) * heads
+    return f, 2.5 * f
+
+
+# --------------------------------------------------------------------------- #
+# Clock sampling during the timed region
+# --------------------------------------------------------------------------- #
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- #
+# The oracle on the host cores (cpu_baseline and the reference arm)
+# --------------------------------------------------------------------------- #
+
+def oracle_sample_step(w, Q, K, V, G, rows):
+    """Oracle forward + reverse over the last ``rows`` query rows of head 0.
+
+    Returns the algorithmic flops of that sample (same convention as the GPU
+    metric: 2 |A| (d+v) forward, 2.5x that reverse)."""
+    from oracle import dense, masks
+    n = w.n
+    r0 = n - rows
+    allowed = masks.allowed_matrix(n, w.mask_kind, w.window, None)[r0:]
+    dense.head_forward(Q[r0:], K, V, w.scale, allowed)
+    dense.head_backward(Q[r0:], K, V, G[r0:], w.scale, allowed)
+    f = 2.0 * float(allowed.sum()) * (w.d + w.v)
+    return 3.5 * f
+
+
+def oracle_inputs(w, x):
+    return tuple(t[0, 0].to(torch.float64).numpy() for t in (x.Q, x.K, x.V, x.dY))
+
+
+def cpu_baseline(w, x, budget_s=12.0, rows=512):
+    Q, K, V, G = oracle_inputs(w, x)
+    done_flops, t0, samples = 0.0, time.perf_counter(), 0
+    while True:
+        done_flops += oracle_sample_step(w, Q, K, V, G, rows)
+        samples += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": done_flops / el / 1e12, "unit": "TFLOP/s", "cores": host_cores(),
+            "kind": "oracle",
+            "sample": f"{samples} x (fwd+bwd of the last {rows} query rows of head 0, float64 "
+                      f"dense NumPy), {el:.1f} s"}
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    x = workloads.make_inputs(w, heads=1)
+    Q, K, V, G = oracle_inputs(w, x)
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample_step(w, Q, K, V, G, rows)
+    t0 = time.perf_counter()
+    total = 0.0
+    for _ in range(args.steps):
+        total += oracle_sample_step(w, Q, K, V, G, rows)
+    el = time.perf_counter() - t0
+    value = total / el / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d, "v": w.v,
+                   "mask": w.mask, "input_dtype": w.dtype,
+                   "step": f"oracle fwd+bwd of the last {rows} query rows of head 0"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(),
+                         "kind": "oracle",
+                         "sample": f"{args.steps} x fwd+bwd of the last {rows} query rows of "
+                                   f"head 0 (float64 dense NumPy)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- #
+# The GPU arm
+# --------------------------------------------------------------------------- #
+
+METRIC = "attention TFLOP/s fwd+bwd (fwd alone in fwd_tflops) at 1 GB300; % of dense BF16 peak"
+
+
+def read_traffic(kernel_tag):
+    """DRAM bytes per launch from the committed ncu summary, if it still matches
+    the current kernel source (null otherwise)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    entries = {}
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        kv = dict(p.split("=", 1) for p in line.split() if "=" in p)
+        entries[kv.get("kernel")] = kv
+    e = entries.get(kernel_tag)
+    if e is None:
+        return None
+    src = os.path.join(ROOT, "exact_tiled_softmax_gb300", "csrc", e.get("source", ""))
+    if not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if sha != e.get("source_sha"):
+        return None
+    return float(e["bytes_per_launch"])
+
+
+def run_gpu(args, w):
+    import exact_tiled_softmax_gb300 as ex
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if args.path != "auto":
+        ex.set_path(args.path)
+
+    x = workloads.make_inputs(w)
+    q, k, v, dy = (t.to(dev) for t in (x.Q, x.K, x.V, x.dY))
+    bm = None if x.bitmask is None else torch.from_numpy(x.bitmask.view(np.int32)).to(dev)
+    shape = ex.Shape(w.B, w.H, w.n, w.d, w.v, 0 if w.dtype == "f32" else 1)
+    ws_f = ex.workspace(ex.fwd_workspace_size(shape, w.mask), dev)
+    ws_b = ex.workspace(ex.bwd_workspace_size(shape, w.mask), dev)
+    y = torch.empty(q.shape[:-1] + (w.v,), dtype=q.dtype, device=dev)
+    L = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ex.fwd(q, k, v, w.scale, w.mask, w.window, bm, y=y, L=L, ws=ws_f, stream=stream)
+        ex.bwd(q, k, v, y, dy, L, w.scale, w.mask, w.window, bm, dq=dq, dk=dk, dv=dv, ws=ws_b,
+               stream=stream)
+
+    def fwd_only():
+        ex.fwd(q, k, v, w.scale, w.mask, w.window, bm, y=y, L=L, ws=ws_f, stream=stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(val):
+        if dist is None:
+            return val
+        t = torch.tensor([val], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    pairs = None
+    if w.mask == "bitmask":
+        from_words = np.unpackbits(x.bitmask.view(np.uint8)).sum()
+        pairs = int(from_words)
+    f_fwd, f_bwd = flops(w, pairs)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+
+    # Timed region: K full steps; the forward and reverse kernels of every step
+    # are also bracketed by events recorded on this stream by the library.
+    K = args.steps
+    ev = {role: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(K)] for role in (ex.KERNEL_FWD, ex.KERNEL_BWD)}
+    for pairs_ in ev.values():
+        for a, b in pairs_:
+            a.record(stream)
+            b.record(stream)
+    barrier()
+    launches0 = ex.launch_count()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clocks:
+        barrier()
+        start.record(stream)
+        for i in range(K):
+            for role in ev:
+                ex.record_kernel_events(role, *ev[role][i])
+            step()
+        stop.record(stream)
+        barrier()
+    launches = ex.launch_count() - launches0
+    ms = max_over_ranks(start.elapsed_time(stop))
+    kern_ms = {role: sum(a.elapsed_time(b) for a, b in ev[role]) / K for role in ev}
+
+    # Forward alone.
+    for _ in range(args.warmup):
+        fwd_only()
+    barrier()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(K):
+        fwd_only()
+    e2.record(stream)
+    barrier()
+    ms_fwd = max_over_ranks(s2.elapsed_time(e2))
+
+    # End to end through the public API: pinned host inputs in, results out.
+    e2e = None
+    if not args.no_e2e:
+        pin = [t.pin_memory() for t in (x.Q, x.K, x.V, x.dY)]
+        outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (y, L, dq, dk, dv)]
+        h2d = sum(t.numel() * t.element_size() for t in pin)
+        d2h = sum(t.numel() * t.element_size() for t in outs)
+
+        def e2e_step():
+            for dst, src in zip((q, k, v, dy), pin):
+                dst.copy_(src, non_blocking=True)
+            step()
+            for dst, src in zip(outs, (y, L, dq, dk, dv)):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        barrier()
+        s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s3.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e3.record(stream)
+        barrier()
+        ms_e2e = max_over_ranks(s3.elapsed_time(e3))
+        e2e = {"value": world * (f_fwd + f_bwd) * K / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": ms_e2e / K}
+
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    tflops = world * (f_fwd + f_bwd) * K / (ms * 1e-3) / 1e12
+    tflops_fwd = world * f_fwd * K / (ms_fwd * 1e-3) / 1e12
+    # Dominant kernel by measured time.
+    dom = max(kern_ms, key=kern_ms.get)
+    dom_flops = f_fwd if dom == ex.KERNEL_FWD else f_bwd
+    dom_name = "fwd" if dom == ex.KERNEL_FWD else "bwd"
+    achieved = dom_flops / (kern_ms[dom] * 1e-3) / 1e12
+    tc = args.path == "auto" and w.dtype == "bf16"
+    roofline = {"kernel": f"{'tc' if tc else 'simt'}_{dom_name}",
+                "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_kind": f"bf16 dense burst, of {peak_kind}",
+                "traffic": read_traffic(f"{'tc' if tc else 'simt'}_{dom_name}"),
+                "kernel_ms": {"fwd": kern_ms[ex.KERNEL_FWD], "bwd": kern_ms[ex.KERNEL_BWD]}}
+    line = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d, "v": w.v,
+                   "mask": w.mask, "window": w.window, "scale": w.scale,
+                   "kernel_path": args.path,
+                   "l2": "inputs larger than L2 (4 x 134 MB bf16 vs 129 MB), no flush",
+                   "flops_per_step": f_fwd + f_bwd},
+        "fwd_tflops": tflops_fwd, "fwd_frac_of_peak": tflops_fwd / peak,
+        "fwd_bwd_frac_of_peak": tflops / peak, "ms_fwd": ms_fwd / K,
+        "gpu_launches": launches,
+        "roofline": roofline,
+        "e2e": e2e,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--variant", default="")
+    ap.add_argument("--path", choices=["auto", "simt"], default="auto")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-rows", type=int, default=256)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = workloads.workload(args.workload, args.variant)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

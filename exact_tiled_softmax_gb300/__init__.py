@@ -1,0 +1,196 @@
+"""exact_tiled_softmax_gb300: exact masked attention on one GB300 (sm_103a).
+
+A thin ctypes binding over ``libexattn.so`` (C ABI in ``include/exattn.h``).
+Every step of the forward and reverse pass runs in the library's CUDA
+kernels; this module only checks tensors, allocates outputs and workspaces
+with torch (device memory and streams are all torch is used for) and passes
+raw pointers.  There is no CPU fallback: if the library is missing, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = ["fwd", "bwd", "fwd_workspace_size", "bwd_workspace_size", "device_status",
+           "set_path", "library_path", "load_library", "ExattnError", "Shape",
+           "record_kernel_events", "launch_count", "workspace",
+           "MASK_NONE", "MASK_CAUSAL", "MASK_WINDOW", "MASK_BITMASK"]
+
+MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_BITMASK = 0, 1, 2, 3
+_MASKS = {"none": MASK_NONE, "causal": MASK_CAUSAL, "window": MASK_WINDOW,
+          "bitmask": MASK_BITMASK}
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+_PATHS = {"auto": 0, "simt": 1}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libexattn.so")
+
+
+class ExattnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = load_library().exattn_status_string(status).decode()
+        super().__init__(f"{where}: status {status} ({msg})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("heads", ctypes.c_int), ("n", ctypes.c_int),
+                ("d", ctypes.c_int), ("v", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+def load_library():
+    """Load libexattn.so (built by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libexattn.so not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    vp, sz, ci, cf = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+    sp = ctypes.POINTER(Shape)
+    lib.exattn_set_path.argtypes = [ci]
+    lib.exattn_set_path.restype = ci
+    lib.exattn_fwd_workspace_size.argtypes = [sp, ci]
+    lib.exattn_fwd_workspace_size.restype = sz
+    lib.exattn_bwd_workspace_size.argtypes = [sp, ci]
+    lib.exattn_bwd_workspace_size.restype = sz
+    lib.attn_fwd.argtypes = [sp, vp, vp, vp, cf, ci, ci, vp, vp, vp, vp, sz, vp]
+    lib.attn_fwd.restype = ci
+    lib.attn_bwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, cf, ci, ci, vp, vp, vp, vp, vp, sz, vp]
+    lib.attn_bwd.restype = ci
+    lib.exattn_device_status.argtypes = [vp, vp]
+    lib.exattn_device_status.restype = ci
+    lib.exattn_status_string.argtypes = [ci]
+    lib.exattn_status_string.restype = ctypes.c_char_p
+    lib.exattn_record_kernel_events.argtypes = [ci, vp, vp]
+    lib.exattn_record_kernel_events.restype = ci
+    lib.exattn_launch_count.argtypes = []
+    lib.exattn_launch_count.restype = ctypes.c_ulonglong
+    _lib = lib
+    return lib
+
+
+def set_path(path: str) -> str:
+    """Process-wide kernel path: "auto" (tensor-core kernels where supported) or "simt"."""
+    prev = load_library().exattn_set_path(_PATHS[path])
+    return {v: k for k, v in _PATHS.items()}[prev]
+
+
+def _mask_kind(mask) -> int:
+    return _MASKS[mask] if isinstance(mask, str) else int(mask)
+
+
+def _shape(q: torch.Tensor, v: torch.Tensor) -> Shape:
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("expected [batch, heads, n, width] tensors")
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    B, H, n, d = q.shape
+    return Shape(B, H, n, d, v.shape[-1], _DTYPES[q.dtype])
+
+
+def fwd_workspace_size(shape: Shape, mask) -> int:
+    return load_library().exattn_fwd_workspace_size(ctypes.byref(shape), _mask_kind(mask))
+
+
+def bwd_workspace_size(shape: Shape, mask) -> int:
+    return load_library().exattn_bwd_workspace_size(ctypes.byref(shape), _mask_kind(mask))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(ts, dtype, device):
+    for t in ts:
+        if t is None:
+            continue
+        if t.device != device or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous and on the same CUDA device")
+        if dtype is not None and t.dtype != dtype:
+            raise ValueError(f"dtype mismatch: {t.dtype} vs {dtype}")
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A 256-byte aligned device byte buffer of at least ``nbytes``."""
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def fwd(q, k, v, scale, mask="none", window=0, bitmask=None, y=None, L=None, ws=None,
+        stream=None):
+    """Forward pass -> (Y, L).  q, k [B,H,n,d], v [B,H,n,v]; bitmask int32/uint32 words."""
+    lib = load_library()
+    shape = _shape(q, v)
+    _check((k, v, y), q.dtype, q.device)
+    kind = _mask_kind(mask)
+    if y is None:
+        y = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    if L is None:
+        L = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    need = lib.exattn_fwd_workspace_size(ctypes.byref(shape), kind)
+    if ws is None:
+        ws = workspace(need, q.device)
+    st = lib.attn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale), kind,
+                      int(window), _ptr(bitmask), _ptr(y), _ptr(L), _ptr(ws), ws.numel(),
+                      _stream(stream))
+    if st != 0:
+        raise ExattnError(st, "attn_fwd")
+    return y, L
+
+
+def bwd(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, dq=None, dk=None,
+        dv=None, ws=None, stream=None):
+    """Reverse pass -> (dQ, dK, dV) for the upstream gradient dy."""
+    lib = load_library()
+    shape = _shape(q, v)
+    _check((k, v, y, dy, dq, dk, dv), q.dtype, q.device)
+    kind = _mask_kind(mask)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = lib.exattn_bwd_workspace_size(ctypes.byref(shape), kind)
+    if ws is None:
+        ws = workspace(need, q.device)
+    st = lib.attn_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(dy),
+                      _ptr(L), float(scale), kind, int(window), _ptr(bitmask), _ptr(dq),
+                      _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream))
+    if st != 0:
+        raise ExattnError(st, "attn_bwd")
+    return dq, dk, dv
+
+
+KERNEL_FWD, KERNEL_DELTA, KERNEL_BWD, KERNEL_DQ_CONVERT = 0, 1, 2, 3
+
+
+def record_kernel_events(which: int, start, stop) -> None:
+    """One-shot: record torch.cuda.Event ``start``/``stop`` around the next launch
+    of kernel ``which`` (KERNEL_FWD, KERNEL_DELTA, KERNEL_BWD, KERNEL_DQ_CONVERT)."""
+    for e in (start, stop):
+        if e.cuda_event == 0:
+            raise ValueError("events must be created (record or query them once) first")
+    if load_library().exattn_record_kernel_events(which, ctypes.c_void_p(start.cuda_event),
+                                                  ctypes.c_void_p(stop.cuda_event)) != 0:
+        raise ValueError(f"unknown kernel {which}")
+
+
+def launch_count() -> int:
+    """Kernels launched by the library since it was loaded."""
+    return int(load_library().exattn_launch_count())
+
+
+def device_status(ws, stream=None) -> int:
+    """Synchronise the stream and read the status word of workspace ``ws``."""
+    return load_library().exattn_device_status(_ptr(ws), _stream(stream))

@@ -1,0 +1,221 @@
+// The C ABI of libexattn (include/exattn.h): argument checks, workspace layout
+// and kernel dispatch.  No memory is allocated here.
+#include <stdint.h>
+#include <stdio.h>
+
+#include <atomic>
+
+#include "../../include/exattn.h"
+#include "internal.h"
+
+namespace {
+
+using namespace exattn;
+
+std::atomic<int> g_path{EXATTN_PATH_AUTO};
+std::atomic<unsigned long long> g_launches{0};
+std::atomic<void*> g_hook_start[kKernRoles];
+std::atomic<void*> g_hook_stop[kKernRoles];
+
+constexpr size_t kStatusBytes = 256;
+constexpr int kMaxWidth = 256;
+constexpr int kMaxN = 1 << 20;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int check_shape(const exattn_shape* s) {
+  if (!s) return EXATTN_INVALID_ARG;
+  if (s->batch < 1 || s->heads < 1 || s->n < 1 || s->d < 1 || s->v < 1)
+    return EXATTN_INVALID_ARG;
+  if (s->dtype != EXATTN_F32 && s->dtype != EXATTN_BF16) return EXATTN_INVALID_ARG;
+  if (s->d > kMaxWidth || s->v > kMaxWidth || s->n > kMaxN) return EXATTN_UNSUPPORTED;
+  if ((long long)s->batch * s->heads > 65535) return EXATTN_UNSUPPORTED;
+  if (s->dtype == EXATTN_BF16 && (s->d % 8 != 0 || s->v % 8 != 0)) return EXATTN_UNSUPPORTED;
+  return EXATTN_OK;
+}
+
+int check_mask(int mask_kind, int window, const uint32_t* bitmask) {
+  if (mask_kind < EXATTN_MASK_NONE || mask_kind > EXATTN_MASK_BITMASK) return EXATTN_INVALID_ARG;
+  if (mask_kind == EXATTN_MASK_WINDOW && window < 1) return EXATTN_INVALID_ARG;
+  if (mask_kind == EXATTN_MASK_BITMASK && bitmask == nullptr) return EXATTN_INVALID_ARG;
+  if (mask_kind == EXATTN_MASK_BITMASK && (reinterpret_cast<uintptr_t>(bitmask) & 3u))
+    return EXATTN_MISALIGNED;
+  return EXATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+Problem make_problem(const exattn_shape* s, float scale, int mask_kind, int window,
+                     const uint32_t* bitmask) {
+  Problem p;
+  p.BH = s->batch * s->heads;
+  p.n = s->n;
+  p.d = s->d;
+  p.v = s->v;
+  p.dtype = s->dtype;
+  p.scale = scale;
+  p.mask_kind = mask_kind;
+  p.window = mask_kind == EXATTN_MASK_WINDOW ? window : 0;
+  p.words_per_row = (s->n + 31) / 32;
+  p.bitmask = mask_kind == EXATTN_MASK_BITMASK ? bitmask : nullptr;
+  return p;
+}
+
+size_t bwd_delta_offset() { return kStatusBytes; }
+size_t bwd_dqacc_offset(const exattn_shape* s) {
+  return kStatusBytes + align_up(sizeof(float) * (size_t)s->batch * s->heads * s->n, 256);
+}
+
+}  // namespace
+
+namespace exattn {
+
+void before_launch(int role, cudaStream_t s) {
+  g_launches.fetch_add(1);
+  void* ev = g_hook_start[role].exchange(nullptr);
+  if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev), s);
+}
+
+void after_launch(int role, cudaStream_t s) {
+  void* ev = g_hook_stop[role].exchange(nullptr);
+  if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev), s);
+}
+
+}  // namespace exattn
+
+extern "C" {
+
+int exattn_record_kernel_events(int which, void* start, void* stop) {
+  if (which < 0 || which >= kKernRoles) return -1;
+  g_hook_start[which].store(start);
+  g_hook_stop[which].store(stop);
+  return 0;
+}
+
+unsigned long long exattn_launch_count(void) { return g_launches.load(); }
+
+
+int exattn_set_path(int path) {
+  if (path != EXATTN_PATH_AUTO && path != EXATTN_PATH_SIMT) return -1;
+  return g_path.exchange(path);
+}
+
+size_t exattn_fwd_workspace_size(const exattn_shape* shape, int mask_kind) {
+  if (check_shape(shape) != EXATTN_OK) return 0;
+  (void)mask_kind;
+  return kStatusBytes;
+}
+
+size_t exattn_bwd_workspace_size(const exattn_shape* shape, int mask_kind) {
+  if (check_shape(shape) != EXATTN_OK) return 0;
+  (void)mask_kind;
+  return bwd_dqacc_offset(shape) +
+         sizeof(float) * (size_t)shape->batch * shape->heads * shape->n * shape->d;
+}
+
+int attn_fwd(const exattn_shape* shape, const void* Q, const void* K, const void* V,
+             float scale, int mask_kind, int window, const uint32_t* bitmask, void* Y, float* L,
+             void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  int st = check_shape(shape);
+  if (st != EXATTN_OK) return st;
+  st = check_mask(mask_kind, window, bitmask);
+  if (st != EXATTN_OK) return st;
+  if (!Q || !K || !V || !Y || !L || !workspace) return EXATTN_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Y) || !aligned16(L))
+    return EXATTN_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return EXATTN_MISALIGNED;
+  if (workspace_bytes < exattn_fwd_workspace_size(shape, mask_kind))
+    return EXATTN_WORKSPACE_TOO_SMALL;
+
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  FwdArgs a;
+  a.p = make_problem(shape, scale, mask_kind, window, bitmask);
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.Y = Y;
+  a.L = L;
+  a.status = static_cast<unsigned*>(workspace);
+  if (cudaMemsetAsync(workspace, 0, kStatusBytes, s) != cudaSuccess) return EXATTN_CUDA_ERROR;
+  cudaError_t e;
+  if (g_path.load() == EXATTN_PATH_AUTO && tc_fwd_supported(a.p))
+    e = launch_tc_fwd(a, s);
+  else
+    e = launch_simt_fwd(a, s);
+  return e == cudaSuccess ? EXATTN_OK : EXATTN_CUDA_ERROR;
+}
+
+int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void* V,
+             const void* Y, const void* dY, const float* L, float scale, int mask_kind,
+             int window, const uint32_t* bitmask, void* dQ, void* dK, void* dV, void* workspace,
+             size_t workspace_bytes, void* cuda_stream) {
+  int st = check_shape(shape);
+  if (st != EXATTN_OK) return st;
+  st = check_mask(mask_kind, window, bitmask);
+  if (st != EXATTN_OK) return st;
+  if (!Q || !K || !V || !Y || !dY || !L || !dQ || !dK || !dV || !workspace)
+    return EXATTN_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Y) || !aligned16(dY) ||
+      !aligned16(L) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
+    return EXATTN_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return EXATTN_MISALIGNED;
+  if (workspace_bytes < exattn_bwd_workspace_size(shape, mask_kind))
+    return EXATTN_WORKSPACE_TOO_SMALL;
+
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  char* ws = static_cast<char*>(workspace);
+  BwdArgs a;
+  a.p = make_problem(shape, scale, mask_kind, window, bitmask);
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.Y = Y;
+  a.dY = dY;
+  a.L = L;
+  a.dQ = dQ;
+  a.dK = dK;
+  a.dV = dV;
+  a.status = reinterpret_cast<unsigned*>(ws);
+  a.delta = reinterpret_cast<float*>(ws + bwd_delta_offset());
+  a.dQacc = reinterpret_cast<float*>(ws + bwd_dqacc_offset(shape));
+  const size_t acc_bytes = sizeof(float) * (size_t)a.p.BH * a.p.n * a.p.d;
+  if (cudaMemsetAsync(ws, 0, kStatusBytes, s) != cudaSuccess) return EXATTN_CUDA_ERROR;
+  if (cudaMemsetAsync(a.dQacc, 0, acc_bytes, s) != cudaSuccess) return EXATTN_CUDA_ERROR;
+  cudaError_t e = launch_delta(a, s);
+  if (e == cudaSuccess) {
+    if (g_path.load() == EXATTN_PATH_AUTO && tc_bwd_supported(a.p))
+      e = launch_tc_bwd(a, s);
+    else
+      e = launch_simt_bwd(a, s);
+  }
+  if (e == cudaSuccess) e = launch_dq_convert(a, s);
+  return e == cudaSuccess ? EXATTN_OK : EXATTN_CUDA_ERROR;
+}
+
+int exattn_device_status(const void* workspace, void* cuda_stream) {
+  if (!workspace) return EXATTN_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return EXATTN_CUDA_ERROR;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return EXATTN_CUDA_ERROR;
+  if (word & 2u) return EXATTN_TIMEOUT;
+  if (word & 1u) return EXATTN_EMPTY_ROW;
+  return EXATTN_OK;
+}
+
+const char* exattn_status_string(int status) {
+  switch (status) {
+    case EXATTN_OK: return "ok";
+    case EXATTN_INVALID_ARG: return "invalid argument";
+    case EXATTN_UNSUPPORTED: return "unsupported shape";
+    case EXATTN_MISALIGNED: return "misaligned pointer";
+    case EXATTN_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case EXATTN_EMPTY_ROW: return "an allowed-key set was empty";
+    case EXATTN_CUDA_ERROR: return "CUDA error";
+    case EXATTN_TIMEOUT: return "a bounded device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// Internal (host + device) declarations of libexattn: problem description and
+// the kernel launchers behind the C ABI in include/exattn.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace exattn {
+
+enum { kMaskNone = 0, kMaskCausal = 1, kMaskWindow = 2, kMaskBitmask = 3 };
+enum { kF32 = 0, kBF16 = 1 };
+
+// One attention problem: BH = batch*heads independent slices of [n][d|v].
+struct Problem {
+  int BH, n, d, v, dtype;
+  float scale;
+  int mask_kind, window, words_per_row;
+  const uint32_t* bitmask;
+};
+
+struct FwdArgs {
+  Problem p;
+  const void* Q;
+  const void* K;
+  const void* V;
+  void* Y;
+  float* L;
+  unsigned* status;
+};
+
+struct BwdArgs {
+  Problem p;
+  const void* Q;
+  const void* K;
+  const void* V;
+  const void* Y;
+  const void* dY;
+  const float* L;
+  void* dQ;
+  void* dK;
+  void* dV;
+  float* delta;   // [BH][n] workspace
+  float* dQacc;   // [BH][n][d] fp32 workspace, zeroed by the launcher
+  unsigned* status;
+};
+
+// Profiling hooks (api.cu): every kernel launch goes through these so the
+// launch counter and the one-shot event hooks see it.
+enum KernelRole { kKernFwd = 0, kKernDelta = 1, kKernBwd = 2, kKernDqConvert = 3, kKernRoles = 4 };
+void before_launch(int role, cudaStream_t s);
+void after_launch(int role, cudaStream_t s);
+
+// SIMT fp32 kernels (any dtype, d, v <= 256).
+cudaError_t launch_simt_fwd(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_simt_bwd(const BwdArgs& a, cudaStream_t s);
+
+// delta_i = dY_i . Y_i (memory-bound preprocessing of the reverse pass).
+cudaError_t launch_delta(const BwdArgs& a, cudaStream_t s);
+// dQ = dQacc converted to the output dtype.
+cudaError_t launch_dq_convert(const BwdArgs& a, cudaStream_t s);
+
+// tcgen05 / TMA / TMEM kernels (bf16, d and v multiples of 16 up to 128).
+bool tc_fwd_supported(const Problem& p);
+cudaError_t launch_tc_fwd(const FwdArgs& a, cudaStream_t s);
+bool tc_bwd_supported(const Problem& p);
+cudaError_t launch_tc_bwd(const BwdArgs& a, cudaStream_t s);
+
+}  // namespace exattn

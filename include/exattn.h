@@ -1,0 +1,159 @@
+/*
+ * exattn.h -- C ABI of libexattn.so: exact masked scaled-dot-product attention,
+ * computed tile by tile on one GB300 GPU (sm_103a).
+ *
+ * The operation is the one stated in "Exact tiled softmax attention with
+ * block-recomputed vector-Jacobian products" (alphabetamath), Inputs: matrices
+ * Q, K in R^{n x d}, V in R^{n x v}, a real scale c, and nonempty allowed-key
+ * sets A_1..A_n read on demand from caller-owned storage.  Per (batch, head):
+ *
+ *   s_ij = c <Q_i, K_j> (j in A_i),  p_ij = exp(s_ij - m_i) / l_i,
+ *   Y_i  = sum_j p_ij V_j,           L_i = m_i + ln l_i  (natural log).
+ *
+ * attn_fwd runs the Forward procedure of that page (an online-softmax
+ * recurrence over key blocks, whole blocks with I = J_t n A_i empty skipped)
+ * and retains L_i, the statistic of "python-flash-attention-online-softmax-
+ * block-recompute", The fix, item 1.  attn_bwd runs the Reverse procedure:
+ * delta_i = G_i . Y_i (HarshvardhanJ/FlashAttention, backward section), then
+ * per key block it recomputes p_ij from Q, K and the frozen L_i and adds
+ *   dQ_i += c gamma_ij K_j,  dK_j += c gamma_ij Q_i,  dV_j += p_ij G_i,
+ *   gamma_ij = p_ij (G_i . V_j - delta_i).
+ * No n x n score or probability matrix is ever stored.
+ *
+ * Layout.  Every matrix is dense, contiguous, row-major, batched as
+ * [batch][heads][n][width]: Q, K, dQ, dK are [B][H][n][d]; V, Y, dY, dV are
+ * [B][H][n][v]; L is float32 [B][H][n].  Q, K, V, Y, dY, dQ, dK, dV have the
+ * element type `dtype`; L is always float32.  Device pointers only (memory
+ * the GPU can address), 16-byte aligned.
+ *
+ * Masks (0-indexed, one mask shared by every batch and head):
+ *   EXATTN_MASK_NONE     A_i = {0 .. n-1}
+ *   EXATTN_MASK_CAUSAL   A_i = {0 .. i}
+ *   EXATTN_MASK_WINDOW   A_i = {max(0, i-window+1) .. i}, window >= 1
+ *   EXATTN_MASK_BITMASK  j in A_i iff bit (j % 32) of bitmask[i*ceil(n/32) + j/32]
+ *                        is set; `bitmask` is a device array of n*ceil(n/32)
+ *                        uint32 words owned by the caller.
+ *
+ * Ownership and streams.  The caller owns every buffer, the workspace
+ * included.  The library allocates no memory and keeps no pointer after a
+ * call returns.  Work is queued on `cuda_stream` (a cudaStream_t; NULL is the
+ * legacy default stream) and runs asynchronously; the return code covers
+ * argument checks and kernel launches only.
+ *
+ * Aliasing.  Q, K and V may alias one another (self-attention, Q = K = V = X;
+ * the caller then forms dX = dQ + dK + dV).  Outputs must not alias inputs or
+ * each other.  Two calls that share a workspace must not overlap in time.
+ *
+ * Empty allowed sets.  A nonempty A_i is a precondition.  A row that breaks
+ * it gets Y_i = 0 and L_i = -inf, contributes nothing to the gradients, and
+ * the device status word of the workspace records EXATTN_EMPTY_ROW (read it
+ * with exattn_device_status).  No NaN is produced.
+ */
+#ifndef EXATTN_H
+#define EXATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types of Q, K, V, Y, dY, dQ, dK, dV. Accumulation is always fp32. */
+enum exattn_dtype { EXATTN_F32 = 0, EXATTN_BF16 = 1 };
+
+enum exattn_mask_kind {
+  EXATTN_MASK_NONE = 0,
+  EXATTN_MASK_CAUSAL = 1,
+  EXATTN_MASK_WINDOW = 2,
+  EXATTN_MASK_BITMASK = 3
+};
+
+/* Return codes.  Host-side checks return 1-4 and 6 before queuing any work;
+ * 5 and 7 are device-side conditions reported through the status word. */
+enum exattn_status {
+  EXATTN_OK = 0,
+  EXATTN_INVALID_ARG = 1,        /* null pointer, non-positive size, bad mask kind/window */
+  EXATTN_UNSUPPORTED = 2,        /* d or v > 256, or bf16 with d or v not a multiple of 8 */
+  EXATTN_MISALIGNED = 3,         /* a pointer is not 16-byte aligned */
+  EXATTN_WORKSPACE_TOO_SMALL = 4,
+  EXATTN_EMPTY_ROW = 5,          /* some A_i was empty (status word) */
+  EXATTN_CUDA_ERROR = 6,         /* a CUDA call or launch failed */
+  EXATTN_TIMEOUT = 7             /* a bounded wait inside a kernel gave up (status word) */
+};
+
+/* Problem shape.  batch, heads, n, d, v >= 1; dtype is an exattn_dtype. */
+typedef struct exattn_shape {
+  int batch;
+  int heads;
+  int n;
+  int d;
+  int v;
+  int dtype;
+} exattn_shape;
+
+/* Kernel path selection, process-wide (default EXATTN_PATH_AUTO).
+ * AUTO uses the tcgen05/TMA/TMEM kernels where the shape allows (bf16, d and v
+ * multiples of 16 up to 128) and the SIMT fp32 kernels otherwise; SIMT forces
+ * the SIMT kernels for every shape.  Returns the previous setting, or -1 for
+ * an unknown value (setting unchanged). */
+enum exattn_path { EXATTN_PATH_AUTO = 0, EXATTN_PATH_SIMT = 1 };
+int exattn_set_path(int path);
+
+/* Workspace bytes that attn_fwd / attn_bwd need for this shape and mask kind.
+ * The workspace holds the device status word (first 256 bytes) and, for the
+ * reverse pass, delta [B][H][n] and the fp32 dQ accumulator [B][H][n][d].
+ * Returns 0 when the shape is invalid. */
+size_t exattn_fwd_workspace_size(const exattn_shape* shape, int mask_kind);
+size_t exattn_bwd_workspace_size(const exattn_shape* shape, int mask_kind);
+
+/* Forward: Y [B][H][n][v] (dtype) and L [B][H][n] (float32, natural log) from
+ * Q, K, V.  `window` is read for EXATTN_MASK_WINDOW only, `bitmask` for
+ * EXATTN_MASK_BITMASK only (may be NULL otherwise).  `workspace` is a device
+ * buffer of at least exattn_fwd_workspace_size bytes, 256-byte aligned; its
+ * status word is cleared by the call.  Returns an exattn_status. */
+int attn_fwd(const exattn_shape* shape, const void* Q, const void* K, const void* V,
+             float scale, int mask_kind, int window, const uint32_t* bitmask,
+             void* Y, float* L, void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Reverse pass for the upstream gradient dY (= G): writes dQ, dK (dtype,
+ * [B][H][n][d]) and dV (dtype, [B][H][n][v]).  Y and L must come from attn_fwd
+ * with the same Q, K, V, scale and mask.  `workspace` is a device buffer of at
+ * least exattn_bwd_workspace_size bytes, 256-byte aligned.  Returns an
+ * exattn_status. */
+int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void* V,
+             const void* Y, const void* dY, const float* L, float scale, int mask_kind,
+             int window, const uint32_t* bitmask, void* dQ, void* dK, void* dV,
+             void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Waits for `cuda_stream`, then reads the status word of `workspace` (the
+ * workspace of the last call queued on it).  Returns EXATTN_OK,
+ * EXATTN_EMPTY_ROW, EXATTN_TIMEOUT or EXATTN_CUDA_ERROR. */
+int exattn_device_status(const void* workspace, void* cuda_stream);
+
+/* Profiling aid.  Kernels of the library, by role. */
+enum exattn_kernel {
+  EXATTN_KERNEL_FWD = 0,        /* the forward kernel of attn_fwd */
+  EXATTN_KERNEL_DELTA = 1,      /* delta_i = dY_i . Y_i in attn_bwd */
+  EXATTN_KERNEL_BWD = 2,        /* the key-block reverse kernel of attn_bwd */
+  EXATTN_KERNEL_DQ_CONVERT = 3  /* fp32 dQ accumulator -> dQ in attn_bwd */
+};
+
+/* One-shot: on the next launch of kernel `which` (an exattn_kernel), record
+ * the cudaEvent_t `start` on the call's stream immediately before the launch
+ * and `stop` immediately after it, then forget both.  The events are owned by
+ * the caller.  Returns 0, or -1 for an unknown `which`.  Process-wide. */
+int exattn_record_kernel_events(int which, void* start, void* stop);
+
+/* Number of kernels this library has launched since it was loaded
+ * (process-wide, all devices). */
+unsigned long long exattn_launch_count(void);
+
+/* A static, human-readable name for a status code. */
+const char* exattn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXATTN_H */

@@ -1,0 +1,96 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/exattn.h declares, and rejects bad arguments on the host before any
+CUDA call (so these calls are safe on a machine with no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "exattn.h")
+
+
+@pytest.fixture(scope="session")
+def lib():
+    import exact_tiled_softmax_gb300 as ex
+    if not os.path.exists(ex.library_path()):
+        from exact_tiled_softmax_gb300 import build
+        build.build()
+    return ex.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text,
+                       flags=re.M)
+    return sorted(set(names) - {"defined"})
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("attn_fwd", "attn_bwd", "exattn_fwd_workspace_size",
+                 "exattn_bwd_workspace_size", "exattn_device_status", "exattn_status_string",
+                 "exattn_set_path"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert lib.exattn_status_string(code)
+    assert lib.exattn_status_string(99) == b"unknown status"
+
+
+def _shape(B=1, H=1, n=16, d=64, v=64, dtype=1):
+    import exact_tiled_softmax_gb300 as ex
+    return ex.Shape(B, H, n, d, v, dtype)
+
+
+def test_workspace_sizes_are_linear_in_n(lib):
+    import exact_tiled_softmax_gb300 as ex
+    s1 = ex.bwd_workspace_size(_shape(n=1024, d=128), "causal")
+    s2 = ex.bwd_workspace_size(_shape(n=2048, d=128), "causal")
+    s4 = ex.bwd_workspace_size(_shape(n=4096, d=128), "causal")
+    # status word + delta (4n) + dQ accumulator (4nd): no n^2 term.
+    assert s2 - s1 == 1024 * (4 + 4 * 128)
+    assert s4 - s2 == 2048 * (4 + 4 * 128)
+    assert ex.fwd_workspace_size(_shape(n=4096), "causal") == 256
+    assert ex.bwd_workspace_size(_shape(n=0), "none") == 0
+
+
+def test_host_side_argument_checks(lib):
+    """Bad arguments return a status before any device work is queued."""
+    vp = ctypes.c_void_p
+    good = vp(1 << 20)          # never dereferenced: every call below fails its checks first
+    ws = vp(1 << 21)
+
+    def fwd(shape, mask=0, window=0, bitmask=None, q=good, ws_ptr=ws, ws_bytes=1 << 20):
+        return lib.attn_fwd(ctypes.byref(shape), q, good, good, 1.0, mask, window, bitmask,
+                            good, good, ws_ptr, ws_bytes, None)
+
+    assert fwd(_shape(n=0)) == 1                      # INVALID_ARG
+    assert fwd(_shape(dtype=7)) == 1
+    assert fwd(_shape(d=300)) == 2                    # UNSUPPORTED
+    assert fwd(_shape(d=20, dtype=1)) == 2            # bf16 needs multiples of 8
+    assert fwd(_shape(), mask=9) == 1
+    assert fwd(_shape(), mask=2, window=0) == 1       # window must be >= 1
+    assert fwd(_shape(), mask=3, bitmask=None) == 1   # bitmask required
+    assert fwd(_shape(), q=None) == 1
+    assert fwd(_shape(), q=vp((1 << 20) + 2)) == 3    # MISALIGNED
+    assert fwd(_shape(), ws_ptr=vp((1 << 21) + 16)) == 3
+    assert fwd(_shape(), ws_bytes=8) == 4             # WORKSPACE_TOO_SMALL
+    assert lib.attn_bwd(None, good, good, good, good, good, good, 1.0, 0, 0, None, good, good,
+                        good, ws, 1 << 30, None) == 1
+
+
+def test_path_switch(lib):
+    import exact_tiled_softmax_gb300 as ex
+    assert ex.set_path("simt") == "auto"
+    assert ex.set_path("auto") == "simt"
+    assert lib.exattn_set_path(5) == -1
