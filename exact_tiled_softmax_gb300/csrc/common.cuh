@@ -43,14 +43,18 @@ struct MaskView {
 };
 
 template <typename T> struct Elem;
+// load(): read one element from GLOBAL memory; cvt(): convert a value already
+// in registers.
 template <> struct Elem<float> {
   static __device__ __forceinline__ float load(const float* p) { return __ldg(p); }
+  static __device__ __forceinline__ float cvt(float x) { return x; }
   static __device__ __forceinline__ void store(float* p, float x) { *p = x; }
 };
 template <> struct Elem<__nv_bfloat16> {
   static __device__ __forceinline__ float load(const __nv_bfloat16* p) {
     return __bfloat162float(*p);
   }
+  static __device__ __forceinline__ float cvt(__nv_bfloat16 x) { return __bfloat162float(x); }
   static __device__ __forceinline__ void store(__nv_bfloat16* p, float x) {
     *p = __float2bfloat16_rn(x);
   }

@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(256) delta_vec_kernel(const T* __restrict__ Y,
       const T* ea = reinterpret_cast<const T*>(&a);
       const T* eb = reinterpret_cast<const T*>(&b);
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc = fmaf(Elem<T>::load(ea + e), Elem<T>::load(eb + e), acc);
+      for (int e = 0; e < E; ++e) acc = fmaf(Elem<T>::cvt(ea[e]), Elem<T>::cvt(eb[e]), acc);
     }
   }
 #pragma unroll
