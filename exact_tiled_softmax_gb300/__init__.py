@@ -36,8 +36,10 @@ def library_path() -> str:
 class ExattnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        msg = load_library().exattn_status_string(status).decode()
-        super().__init__(f"{where}: status {status} ({msg})")
+        lib = load_library()
+        msg = lib.exattn_status_string(status).decode()
+        detail = lib.exattn_last_error().decode()
+        super().__init__(f"{where}: status {status} ({msg})" + (f": {detail}" if detail else ""))
 
 
 class Shape(ctypes.Structure):
@@ -74,6 +76,8 @@ def load_library():
     lib.exattn_record_kernel_events.restype = ci
     lib.exattn_launch_count.argtypes = []
     lib.exattn_launch_count.restype = ctypes.c_ulonglong
+    lib.exattn_last_error.argtypes = []
+    lib.exattn_last_error.restype = ctypes.c_char_p
     _lib = lib
     return lib
 

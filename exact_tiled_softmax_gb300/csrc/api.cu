@@ -70,6 +70,12 @@ size_t bwd_dqacc_offset(const exattn_shape* s) {
 
 namespace exattn {
 
+thread_local char g_last_error[256] = "";
+
+void record_error(const char* where, int code, const char* detail) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %d (%s)", where, code, detail ? detail : "");
+}
+
 void before_launch(int role, cudaStream_t s) {
   g_launches.fetch_add(1);
   void* ev = g_hook_start[role].exchange(nullptr);
@@ -93,6 +99,17 @@ int exattn_record_kernel_events(int which, void* start, void* stop) {
 }
 
 unsigned long long exattn_launch_count(void) { return g_launches.load(); }
+
+const char* exattn_last_error(void) { return g_last_error; }
+
+namespace {
+int cuda_status(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return EXATTN_OK;
+  if (exattn::g_last_error[0] == 0 || e != cudaErrorInvalidValue)
+    exattn::record_error(where, static_cast<int>(e), cudaGetErrorString(e));
+  return EXATTN_CUDA_ERROR;
+}
+}  // namespace
 
 
 int exattn_set_path(int path) {
@@ -128,6 +145,7 @@ int attn_fwd(const exattn_shape* shape, const void* Q, const void* K, const void
     return EXATTN_WORKSPACE_TOO_SMALL;
 
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  exattn::g_last_error[0] = 0;
   FwdArgs a;
   a.p = make_problem(shape, scale, mask_kind, window, bitmask);
   a.Q = Q;
@@ -136,13 +154,11 @@ int attn_fwd(const exattn_shape* shape, const void* Q, const void* K, const void
   a.Y = Y;
   a.L = L;
   a.status = static_cast<unsigned*>(workspace);
-  if (cudaMemsetAsync(workspace, 0, kStatusBytes, s) != cudaSuccess) return EXATTN_CUDA_ERROR;
-  cudaError_t e;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes, s);
+  if (e != cudaSuccess) return cuda_status(e, "attn_fwd: clearing the status word");
   if (g_path.load() == EXATTN_PATH_AUTO && tc_fwd_supported(a.p))
-    e = launch_tc_fwd(a, s);
-  else
-    e = launch_simt_fwd(a, s);
-  return e == cudaSuccess ? EXATTN_OK : EXATTN_CUDA_ERROR;
+    return cuda_status(launch_tc_fwd(a, s), "attn_fwd: tensor-core forward launch");
+  return cuda_status(launch_simt_fwd(a, s), "attn_fwd: SIMT forward launch");
 }
 
 int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void* V,
@@ -163,6 +179,7 @@ int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void
     return EXATTN_WORKSPACE_TOO_SMALL;
 
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  exattn::g_last_error[0] = 0;
   char* ws = static_cast<char*>(workspace);
   BwdArgs a;
   a.p = make_problem(shape, scale, mask_kind, window, bitmask);
@@ -179,17 +196,18 @@ int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void
   a.delta = reinterpret_cast<float*>(ws + bwd_delta_offset());
   a.dQacc = reinterpret_cast<float*>(ws + bwd_dqacc_offset(shape));
   const size_t acc_bytes = sizeof(float) * (size_t)a.p.BH * a.p.n * a.p.d;
-  if (cudaMemsetAsync(ws, 0, kStatusBytes, s) != cudaSuccess) return EXATTN_CUDA_ERROR;
-  if (cudaMemsetAsync(a.dQacc, 0, acc_bytes, s) != cudaSuccess) return EXATTN_CUDA_ERROR;
-  cudaError_t e = launch_delta(a, s);
-  if (e == cudaSuccess) {
-    if (g_path.load() == EXATTN_PATH_AUTO && tc_bwd_supported(a.p))
-      e = launch_tc_bwd(a, s);
-    else
-      e = launch_simt_bwd(a, s);
-  }
-  if (e == cudaSuccess) e = launch_dq_convert(a, s);
-  return e == cudaSuccess ? EXATTN_OK : EXATTN_CUDA_ERROR;
+  cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes, s);
+  if (e != cudaSuccess) return cuda_status(e, "attn_bwd: clearing the status word");
+  e = cudaMemsetAsync(a.dQacc, 0, acc_bytes, s);
+  if (e != cudaSuccess) return cuda_status(e, "attn_bwd: clearing the dQ accumulator");
+  e = launch_delta(a, s);
+  if (e != cudaSuccess) return cuda_status(e, "attn_bwd: delta launch");
+  if (g_path.load() == EXATTN_PATH_AUTO && tc_bwd_supported(a.p))
+    e = launch_tc_bwd(a, s);
+  else
+    e = launch_simt_bwd(a, s);
+  if (e != cudaSuccess) return cuda_status(e, "attn_bwd: reverse kernel launch");
+  return cuda_status(launch_dq_convert(a, s), "attn_bwd: dQ conversion launch");
 }
 
 int exattn_device_status(const void* workspace, void* cuda_stream) {

@@ -49,6 +49,8 @@ struct BwdArgs {
 // launch counter and the one-shot event hooks see it.
 enum KernelRole { kKernFwd = 0, kKernDelta = 1, kKernBwd = 2, kKernDqConvert = 3, kKernRoles = 4 };
 void before_launch(int role, cudaStream_t s);
+// Remember the last failing step of this host thread (exattn_last_error).
+void record_error(const char* where, int code, const char* detail);
 void after_launch(int role, cudaStream_t s);
 
 // SIMT fp32 kernels (any dtype, d, v <= 256).

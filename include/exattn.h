@@ -149,6 +149,11 @@ int exattn_record_kernel_events(int which, void* start, void* stop);
  * (process-wide, all devices). */
 unsigned long long exattn_launch_count(void);
 
+/* Text of the last CUDA failure seen by a call on this host thread (which
+ * step failed and the CUDA or driver error), or "" if none.  Valid until the
+ * next call on this thread. */
+const char* exattn_last_error(void);
+
 /* A static, human-readable name for a status code. */
 const char* exattn_status_string(int status);
 
