@@ -61,10 +61,15 @@ Problem make_problem(const exattn_shape* s, float scale, int mask_kind, int wind
   return p;
 }
 
-size_t bwd_delta_offset() { return kStatusBytes; }
-size_t bwd_dqacc_offset(const exattn_shape* s) {
-  return kStatusBytes + align_up(sizeof(float) * (size_t)s->batch * s->heads * s->n, 256);
+// Reverse-pass workspace: status word | delta [BH][npad] | lse2 [BH][npad] |
+// dQ accumulator [BH][n][d] (fp32), each part 256-byte aligned.
+size_t npad_of(const exattn_shape* s) { return ((size_t)s->n + 127) / 128 * 128; }
+size_t bwd_vec_bytes(const exattn_shape* s) {
+  return align_up(sizeof(float) * (size_t)s->batch * s->heads * npad_of(s), 256);
 }
+size_t bwd_delta_offset() { return kStatusBytes; }
+size_t bwd_lse2_offset(const exattn_shape* s) { return kStatusBytes + bwd_vec_bytes(s); }
+size_t bwd_dqacc_offset(const exattn_shape* s) { return kStatusBytes + 2 * bwd_vec_bytes(s); }
 
 }  // namespace
 
@@ -193,7 +198,9 @@ int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void
   a.dK = dK;
   a.dV = dV;
   a.status = reinterpret_cast<unsigned*>(ws);
+  a.npad = static_cast<int>(npad_of(shape));
   a.delta = reinterpret_cast<float*>(ws + bwd_delta_offset());
+  a.lse2 = reinterpret_cast<float*>(ws + bwd_lse2_offset(shape));
   a.dQacc = reinterpret_cast<float*>(ws + bwd_dqacc_offset(shape));
   const size_t acc_bytes = sizeof(float) * (size_t)a.p.BH * a.p.n * a.p.d;
   cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes, s);

@@ -40,7 +40,9 @@ struct BwdArgs {
   void* dQ;
   void* dK;
   void* dV;
-  float* delta;   // [BH][n] workspace
+  int npad;       // n rounded up to a multiple of 128
+  float* delta;   // [BH][npad] workspace: delta_i (0 on padding rows)
+  float* lse2;    // [BH][npad] workspace: L_i * log2(e); +inf on padding / empty rows
   float* dQacc;   // [BH][n][d] fp32 workspace, zeroed by the launcher
   unsigned* status;
 };
@@ -57,7 +59,8 @@ void after_launch(int role, cudaStream_t s);
 cudaError_t launch_simt_fwd(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_simt_bwd(const BwdArgs& a, cudaStream_t s);
 
-// delta_i = dY_i . Y_i (memory-bound preprocessing of the reverse pass).
+// delta_i = dY_i . Y_i and the log2-scaled row statistic (memory-bound
+// preprocessing of the reverse pass), written to padded [BH][npad] vectors.
 cudaError_t launch_delta(const BwdArgs& a, cudaStream_t s);
 // dQ = dQacc converted to the output dtype.
 cudaError_t launch_dq_convert(const BwdArgs& a, cudaStream_t s);

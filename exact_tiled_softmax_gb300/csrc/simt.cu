@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(BwdArgs a) {
   const T* Vh = static_cast<const T*>(a.V) + (size_t)bh * n * v;
   const T* dYh = static_cast<const T*>(a.dY) + (size_t)bh * n * v;
   const float* Lh = a.L + (size_t)bh * n;
-  const float* Dh = a.delta + (size_t)bh * n;
+  const float* Dh = a.delta + (size_t)bh * a.npad;
   float* dQh = a.dQacc + (size_t)bh * n * d;
   MaskView mask{p.mask_kind, n, p.window, p.words_per_row, p.bitmask};
   const float c = p.scale, sl2 = p.scale * kLog2e;
@@ -259,48 +259,79 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(BwdArgs a) {
   }
 }
 
-// delta_i = sum_a dY_ia Y_ia, one row per group of G lanes, 16-byte loads.
+// delta_i = sum_a dY_ia Y_ia and lse2_i = L_i log2(e) over padded rows
+// [BH][npad]: one row per group of G lanes, 16-byte loads.  Padding rows
+// (i >= n) get delta = 0 and lse2 = +inf, as do rows with L_i = -inf (an empty
+// allowed set), so that exp2(s - lse2) = 0 there.
+struct DeltaArgs {
+  const void* Y;
+  const void* dY;
+  const float* L;
+  float* delta;
+  float* lse2;
+  int n, npad, v;
+  size_t rows;  // BH * npad
+};
+
+__device__ __forceinline__ void delta_store(const DeltaArgs& a, size_t row, float acc) {
+  const size_t bh = row / a.npad;
+  const int i = static_cast<int>(row - bh * a.npad);
+  if (i < a.n) {
+    const float L = a.L[bh * a.n + i];
+    a.delta[row] = acc;
+    a.lse2[row] = L == -INFINITY ? INFINITY : L * kLog2e;
+  } else {
+    a.delta[row] = 0.f;
+    a.lse2[row] = INFINITY;
+  }
+}
+
 template <typename T, int G>
-__global__ void __launch_bounds__(256) delta_vec_kernel(const T* __restrict__ Y,
-                                                        const T* __restrict__ dY,
-                                                        float* __restrict__ delta, size_t rows,
-                                                        int v) {
+__global__ void __launch_bounds__(256) delta_vec_kernel(DeltaArgs a) {
   constexpr int E = 16 / sizeof(T);  // elements per 16-byte vector
   const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t row = gtid / G;
   const int lane = (int)(gtid % G);
-  const int vecs = v / E;
+  const int vecs = a.v / E;
   float acc = 0.f;
-  if (row < rows) {
-    const uint4* y = reinterpret_cast<const uint4*>(Y + row * v);
-    const uint4* g = reinterpret_cast<const uint4*>(dY + row * v);
-    for (int k = lane; k < vecs; k += G) {
-      uint4 a = __ldcs(y + k), b = __ldcs(g + k);
-      const T* ea = reinterpret_cast<const T*>(&a);
-      const T* eb = reinterpret_cast<const T*>(&b);
+  if (row < a.rows) {
+    const size_t bh = row / a.npad;
+    const int i = static_cast<int>(row - bh * a.npad);
+    if (i < a.n) {
+      const size_t src = (bh * a.n + i) * a.v;
+      const uint4* y = reinterpret_cast<const uint4*>(static_cast<const T*>(a.Y) + src);
+      const uint4* g = reinterpret_cast<const uint4*>(static_cast<const T*>(a.dY) + src);
+      for (int k = lane; k < vecs; k += G) {
+        uint4 va = __ldcs(y + k), vb = __ldcs(g + k);
+        const T* ea = reinterpret_cast<const T*>(&va);
+        const T* eb = reinterpret_cast<const T*>(&vb);
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc = fmaf(Elem<T>::cvt(ea[e]), Elem<T>::cvt(eb[e]), acc);
+        for (int e = 0; e < E; ++e) acc = fmaf(Elem<T>::cvt(ea[e]), Elem<T>::cvt(eb[e]), acc);
+      }
     }
   }
 #pragma unroll
   for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && lane == 0) delta[row] = acc;
+  if (row < a.rows && lane == 0) delta_store(a, row, acc);
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256) delta_scalar_kernel(const T* __restrict__ Y,
-                                                           const T* __restrict__ dY,
-                                                           float* __restrict__ delta,
-                                                           size_t rows, int v) {
+__global__ void __launch_bounds__(256) delta_scalar_kernel(DeltaArgs a) {
   const size_t row = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x & 31;
   float acc = 0.f;
-  if (row < rows)
-    for (int k = lane; k < v; k += 32)
-      acc = fmaf(Elem<T>::load(Y + row * v + k), Elem<T>::load(dY + row * v + k), acc);
+  if (row < a.rows) {
+    const size_t bh = row / a.npad;
+    const int i = static_cast<int>(row - bh * a.npad);
+    if (i < a.n) {
+      const T* y = static_cast<const T*>(a.Y) + (bh * a.n + i) * a.v;
+      const T* g = static_cast<const T*>(a.dY) + (bh * a.n + i) * a.v;
+      for (int k = lane; k < a.v; k += 32) acc = fmaf(Elem<T>::load(y + k), Elem<T>::load(g + k), acc);
+    }
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && lane == 0) delta[row] = acc;
+  if (row < a.rows && lane == 0) delta_store(a, row, acc);
 }
 
 template <typename T>
@@ -367,28 +398,26 @@ cudaError_t bwd_dispatch(const BwdArgs& a, cudaStream_t s) {
 template <typename T>
 cudaError_t delta_dispatch(const BwdArgs& a, cudaStream_t s) {
   const Problem& p = a.p;
-  const size_t rows = (size_t)p.BH * p.n;
-  const T* Y = static_cast<const T*>(a.Y);
-  const T* dY = static_cast<const T*>(a.dY);
+  DeltaArgs d{a.Y, a.dY, a.L, a.delta, a.lse2, p.n, a.npad, p.v, (size_t)p.BH * a.npad};
   constexpr int E = 16 / sizeof(T);
   const int vecs = p.v / E;
   before_launch(kKernDelta, s);
   if (p.v % E == 0 && (vecs & (vecs - 1)) == 0 && vecs <= 32) {
     // G lanes per row, one 16-byte vector per lane per step.
     const int G = vecs;
-    const size_t threads = rows * G;
+    const size_t threads = d.rows * G;
     const unsigned blocks = (unsigned)((threads + 255) / 256);
     switch (G) {
-      case 1: delta_vec_kernel<T, 1><<<blocks, 256, 0, s>>>(Y, dY, a.delta, rows, p.v); break;
-      case 2: delta_vec_kernel<T, 2><<<blocks, 256, 0, s>>>(Y, dY, a.delta, rows, p.v); break;
-      case 4: delta_vec_kernel<T, 4><<<blocks, 256, 0, s>>>(Y, dY, a.delta, rows, p.v); break;
-      case 8: delta_vec_kernel<T, 8><<<blocks, 256, 0, s>>>(Y, dY, a.delta, rows, p.v); break;
-      case 16: delta_vec_kernel<T, 16><<<blocks, 256, 0, s>>>(Y, dY, a.delta, rows, p.v); break;
-      default: delta_vec_kernel<T, 32><<<blocks, 256, 0, s>>>(Y, dY, a.delta, rows, p.v); break;
+      case 1: delta_vec_kernel<T, 1><<<blocks, 256, 0, s>>>(d); break;
+      case 2: delta_vec_kernel<T, 2><<<blocks, 256, 0, s>>>(d); break;
+      case 4: delta_vec_kernel<T, 4><<<blocks, 256, 0, s>>>(d); break;
+      case 8: delta_vec_kernel<T, 8><<<blocks, 256, 0, s>>>(d); break;
+      case 16: delta_vec_kernel<T, 16><<<blocks, 256, 0, s>>>(d); break;
+      default: delta_vec_kernel<T, 32><<<blocks, 256, 0, s>>>(d); break;
     }
   } else {
-    const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
-    delta_scalar_kernel<T><<<blocks, 256, 0, s>>>(Y, dY, a.delta, rows, p.v);
+    const unsigned blocks = (unsigned)((d.rows * 32 + 255) / 256);
+    delta_scalar_kernel<T><<<blocks, 256, 0, s>>>(d);
   }
   after_launch(kKernDelta, s);
   return cudaGetLastError();

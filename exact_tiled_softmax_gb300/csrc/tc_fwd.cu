@@ -532,6 +532,8 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, int width, int n, int BH) 
   return r == CUDA_SUCCESS;
 }
 
+bool tmap_encoder_available() { return encode_fn() != nullptr; }
+
 bool tc_fwd_supported(const Problem& p) {
   if (p.dtype != kBF16 || p.d != p.v || (p.d != 64 && p.d != 128)) return false;
   if (!(p.scale > 0.f)) return false;

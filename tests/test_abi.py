@@ -57,9 +57,10 @@ def test_workspace_sizes_are_linear_in_n(lib):
     s1 = ex.bwd_workspace_size(_shape(n=1024, d=128), "causal")
     s2 = ex.bwd_workspace_size(_shape(n=2048, d=128), "causal")
     s4 = ex.bwd_workspace_size(_shape(n=4096, d=128), "causal")
-    # status word + delta (4n) + dQ accumulator (4nd): no n^2 term.
-    assert s2 - s1 == 1024 * (4 + 4 * 128)
-    assert s4 - s2 == 2048 * (4 + 4 * 128)
+    # status word + delta and L log2(e) (4n each, n padded to 128) + dQ
+    # accumulator (4nd): no n^2 term.
+    assert s2 - s1 == 1024 * (8 + 4 * 128)
+    assert s4 - s2 == 2048 * (8 + 4 * 128)
     assert ex.fwd_workspace_size(_shape(n=4096), "causal") == 256
     assert ex.bwd_workspace_size(_shape(n=0), "none") == 0
 
