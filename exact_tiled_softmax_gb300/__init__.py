@@ -16,7 +16,7 @@ import torch
 
 __all__ = ["fwd", "bwd", "fwd_workspace_size", "bwd_workspace_size", "device_status",
            "set_path", "library_path", "load_library", "ExattnError", "Shape",
-           "record_kernel_events", "launch_count", "workspace",
+           "record_kernel_events", "launch_count", "workspace", "bwd_noalloc",
            "MASK_NONE", "MASK_CAUSAL", "MASK_WINDOW", "MASK_BITMASK"]
 
 MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_BITMASK = 0, 1, 2, 3
@@ -76,6 +76,8 @@ def load_library():
     lib.exattn_record_kernel_events.restype = ci
     lib.exattn_launch_count.argtypes = []
     lib.exattn_launch_count.restype = ctypes.c_ulonglong
+    lib.attn_bwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, cf, ci, ci, vp, vp, vp, vp, vp]
+    lib.attn_bwd_noalloc.restype = ci
     lib.exattn_last_error.argtypes = []
     lib.exattn_last_error.restype = ctypes.c_char_p
     _lib = lib
@@ -173,6 +175,24 @@ def bwd(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, dq=None, 
                       _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream))
     if st != 0:
         raise ExattnError(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def bwd_noalloc(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, dq=None,
+                dk=None, dv=None, stream=None):
+    """Reverse pass through attn_bwd_noalloc: no workspace is passed or allocated;
+    the library's own 64 MiB scratch array is used instead."""
+    lib = load_library()
+    shape = _shape(q, v)
+    _check((k, v, y, dy, dq, dk, dv), q.dtype, q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = lib.attn_bwd_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(y),
+                              _ptr(dy), _ptr(L), float(scale), _mask_kind(mask), int(window),
+                              _ptr(bitmask), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream))
+    if st != 0:
+        raise ExattnError(st, "attn_bwd_noalloc")
     return dq, dk, dv
 
 

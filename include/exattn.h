@@ -126,6 +126,29 @@ int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void
              int window, const uint32_t* bitmask, void* dQ, void* dK, void* dV,
              void* workspace, size_t workspace_bytes, void* cuda_stream);
 
+/* The reverse pass of attn_bwd for callers that cannot allocate device memory
+ * and so cannot pass a workspace: for example a plugin whose host gives it only
+ * its input and output buffers, or code that must not let a device allocation
+ * (which can synchronise the device or fail under a memory cap) happen on its
+ * path.  This operation has no counterpart in the pages that define the
+ * method; it is attn_bwd with its scratch moved into the library.
+ *
+ * Arguments, layouts and results are those of attn_bwd, without the workspace.
+ * The scratch is a 64 MiB array in the library's own device memory, which every
+ * GPU that loads this part of the library keeps until the process exits; the
+ * call allocates nothing.  A problem whose exattn_bwd_workspace_size exceeds
+ * 64 MiB (67108864 bytes) is rejected with EXATTN_WORKSPACE_TOO_SMALL and no
+ * work is queued.  The first call on a device looks up the array's device
+ * address with that device current; make that first call before any stream
+ * capture.  All calls share the one array (each call clears what must start at
+ * zero): calls whose work overlaps on the GPU, for example on two streams,
+ * race and must not be issued.  The device status word lives in the array; it
+ * is not readable through exattn_device_status.  Returns an exattn_status. */
+int attn_bwd_noalloc(const exattn_shape* shape, const void* Q, const void* K, const void* V,
+                     const void* Y, const void* dY, const float* L, float scale, int mask_kind,
+                     int window, const uint32_t* bitmask, void* dQ, void* dK, void* dV,
+                     void* cuda_stream);
+
 /* Waits for `cuda_stream`, then reads the status word of `workspace` (the
  * workspace of the last call queued on it).  Returns EXATTN_OK,
  * EXATTN_EMPTY_ROW, EXATTN_TIMEOUT or EXATTN_CUDA_ERROR. */
