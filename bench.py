@@ -372,7 +372,8 @@ def run_gpu(args, w):
         "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d, "v": w.v,
                    "mask": w.mask, "window": w.window, "scale": w.scale,
                    "kernel_path": args.path,
-                   "l2": "inputs larger than L2 (4 x 134 MB bf16 vs 129 MB), no flush",
+                   "l2": ("inputs larger than L2 (%d MB of Q, K, V, dY vs 129 MB), no flush"
+                          % (sum(t.numel() * t.element_size() for t in (q, k, v, dy)) >> 20)),
                    "flops_per_step": f_fwd + f_bwd},
         "fwd_tflops": tflops_fwd, "fwd_frac_of_peak": tflops_fwd / peak,
         "fwd_bwd_frac_of_peak": tflops / peak, "ms_fwd": ms_fwd / K,
@@ -403,10 +404,18 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the batch size (a smaller case of the same workload)")
+    ap.add_argument("--heads", type=int, default=None, help="override the head count")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     w = workloads.workload(args.workload, args.variant)
+    if args.batch is not None or args.heads is not None:
+        import dataclasses
+        B = args.batch if args.batch is not None else w.B
+        H = args.heads if args.heads is not None else w.H
+        w = dataclasses.replace(w, B=B, H=H, name=f"{w.name}-as-b{B}h{H}")
     if args.impl == "reference":
         run_reference(args, w)
     else:
