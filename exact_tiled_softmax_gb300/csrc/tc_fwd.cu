@@ -405,9 +405,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           for (int cc = 0; cc < 128; ++cc)
             if (!((mw[cc >> 5] >> (cc & 31)) & 1u)) s[cc] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+        // Row maximum as 8 independent chains, then a short tree.
+        float mx8[8];
 #pragma unroll
-        for (int cc = 0; cc < 128; ++cc) mx = fmaxf(mx, __uint_as_float(s[cc]));
+        for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(s[k]);
+#pragma unroll
+        for (int cc = 8; cc < 128; ++cc) mx8[cc & 7] = fmaxf(mx8[cc & 7], __uint_as_float(s[cc]));
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float tmax = mx * sl2;  // -inf stays -inf (sl2 > 0)
         const float m_new = fmaxf(m_ref, tmax);
         const bool need = (m_ref != -INFINITY) && (m_new > m_ref + kRescaleThreshold);
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           }
         }
         const float neg = m_ref == -INFINITY ? 0.f : -m_ref;
-        float rowsum = 0.f;
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t pk[32];
@@ -436,11 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           for (int e = 0; e < 32; ++e) {
             const float p0 = ex2(fmaf(__uint_as_float(s[64 * half + 2 * e]), sl2, neg));
             const float p1 = ex2(fmaf(__uint_as_float(s[64 * half + 2 * e + 1]), sl2, neg));
-            rowsum += p0 + p1;
+            sum4[e & 3] += p0 + p1;
             pk[e] = pack_bf16x2(p0, p1);
           }
           tmem_st32(t_s + 32 * half, pk);
         }
+        const float rowsum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
         tmem_st_wait();
         l += rowsum;
         tc_fence_before();
