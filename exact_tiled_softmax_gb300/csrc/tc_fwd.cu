@@ -218,35 +218,42 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 
   if (warp >= 8) {
     regs_dec<kProducerRegs>();
+    // The producer warps run their loops on all 32 lanes (warp-uniform state,
+    // descriptors in uniform registers); one elected lane issues.
+    const bool leader = elect_one();
     if (warp == kWarpTMA) {
-      if (lane == 0) {
+      if (leader) {
         prefetch_tmap(&p.tq);
         prefetch_tmap(&p.tk);
         prefetch_tmap(&p.tv);
-        const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
-        const int nq = rows[1].valid ? 2 : 1;
+      }
+      const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
+      const int nq = rows[1].valid ? 2 : 1;
+      if (leader) {
         mbar_arrive_expect_tx(bar(Lay::B_Q), nq * Lay::QTILE);
         for (int X = 0; X < nq; ++X)
           for (int c = 0; c < Lay::DCH; ++c)
             tma_load_3d(sbase + Lay::Q_OFF + X * Lay::QTILE + c * 16384, &p.tq, bar(Lay::B_Q),
                         64 * c, q0 + X * kBM, bh, stream);
-        int it = 0;
-        int last_phase[NS];
-        for (int s = 0; s < NS; ++s) last_phase[s] = -1;
-        bool ok = true;
-        for (int kt = kt_begin; kt < kt_end && ok; ++kt) {
-          const int c0 = classify(p, rows[0], 0, kt, cls_any, cls_all);
-          const int c1 = classify(p, rows[1], 1, kt, cls_any, cls_all);
-          if (c0 == kEmpty && c1 == kEmpty) continue;
-  #pragma unroll
-          for (int kv = 0; kv < 2 && ok; ++kv) {
-            const int slot = it % NS, phase = (it / NS) & 1;
-            ++it;
-            if (!mbar_wait(bar(Lay::B_KVE + slot), phase ^ 1, abort_flag)) {
-              ok = false;
-              break;
-            }
-            const uint32_t dst = sbase + Lay::SLOT_OFF + slot * Lay::SLOT;
+      }
+      int it = 0;
+      int last_phase[NS];
+      for (int s = 0; s < NS; ++s) last_phase[s] = -1;
+      bool ok = true;
+      for (int kt = kt_begin; kt < kt_end && ok; ++kt) {
+        const int c0 = classify(p, rows[0], 0, kt, cls_any, cls_all);
+        const int c1 = classify(p, rows[1], 1, kt, cls_any, cls_all);
+        if (c0 == kEmpty && c1 == kEmpty) continue;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+          const int slot = it % NS, phase = (it / NS) & 1;
+          ++it;
+          if (!mbar_wait(bar(Lay::B_KVE + slot), phase ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = sbase + Lay::SLOT_OFF + slot * Lay::SLOT;
+          if (leader) {
             if (kv == 0) {
               mbar_arrive_expect_tx(bar(Lay::B_KVF + slot), Lay::KBYTES);
               for (int c = 0; c < Lay::DCH; ++c)
@@ -258,104 +265,115 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 tma_load_3d(dst + c * 16384, &p.tv, bar(Lay::B_KVF + slot), 64 * c, kt * kBN, bh,
                             keep);
             }
-            last_phase[slot] = phase;
           }
+          last_phase[slot] = phase;
         }
-        if (!ok) {
-          raise_status(p.status, kStatusTimeout);
-          *abort_flag = 1;
-        }
-        // Never leave with copies in flight: wait (bounded) for the last fill of
-        // every slot and for Q.
-        for (int s = 0; s < NS; ++s)
-          if (last_phase[s] >= 0) mbar_wait(bar(Lay::B_KVF + s), last_phase[s], abort_flag);
-        mbar_wait(bar(Lay::B_Q), 0, abort_flag);
       }
+      __syncwarp();
+      if (!ok && leader) {
+        raise_status(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      // Never leave with copies in flight: wait (bounded) for the last fill of
+      // every slot and for Q.
+      for (int s = 0; s < NS; ++s)
+        if (last_phase[s] >= 0) mbar_wait(bar(Lay::B_KVF + s), last_phase[s], abort_flag);
+      mbar_wait(bar(Lay::B_Q), 0, abort_flag);
     } else if (warp == kWarpMMA) {
-      if (lane == 0) {
-        constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);
-        constexpr uint32_t kIdescPV = idesc_bf16(kBM, V, false, true);
-        bool ok = mbar_wait(bar(Lay::B_Q), 0, abort_flag);
-        tc_fence_after();
-        int it = 0, cnt[2] = {0, 0};
-        bool first_pv[2] = {true, true};
-        bool pend_b = false, have_prev = false;
-        int pend_b_phase = 0, pend_vslot = 0;
-        auto issue_s = [&](int X, int kslot) {
-          const uint32_t qa = sbase + Lay::Q_OFF + X * Lay::QTILE;
-          const uint32_t kb = sbase + Lay::SLOT_OFF + kslot * Lay::SLOT;
-  #pragma unroll
+      constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);
+      constexpr uint32_t kIdescPV = idesc_bf16(kBM, V, false, true);
+      // Descriptors of the Q tiles and of slot 0; slot s and K-step kk only add
+      // constants to the start-address field (units of 16 bytes).
+      const uint64_t dq0 = sdesc_sw128(sbase + Lay::Q_OFF, 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(sbase + Lay::SLOT_OFF, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(sbase + Lay::SLOT_OFF, 16384, 1024);
+      bool ok = mbar_wait(bar(Lay::B_Q), 0, abort_flag);
+      tc_fence_after();
+      int it = 0, cnt[2] = {0, 0};
+      bool first_pv[2] = {true, true};
+      bool pend_b = false, have_prev = false;
+      int pend_b_phase = 0, pend_vslot = 0;
+      auto issue_s = [&](int X, int kslot) {
+        const uint64_t a0 = dq0 + static_cast<uint64_t>(X * (Lay::QTILE >> 4));
+        const uint64_t b0 = dk0 + static_cast<uint64_t>(kslot * (Lay::SLOT >> 4));
+        if (leader) {
+#pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tmem + X * kBN, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                   kIdescS, kk > 0 ? 1u : 0u);
+            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + X * kBN, a0 + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
           }
-        };
-        auto issue_pv = [&](int X, int vslot) {
-          const uint32_t vb = sbase + Lay::SLOT_OFF + vslot * Lay::SLOT;
-  #pragma unroll
+        }
+      };
+      auto issue_pv = [&](int X, int vslot) {
+        const uint64_t b0 = dv0 + static_cast<uint64_t>(vslot * (Lay::SLOT >> 4));
+        const uint32_t acc0 = first_pv[X] ? 0u : 1u;
+        if (leader) {
+#pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts(tmem + 2 * kBN + X * V, tmem + X * kBN + kk * 8,
-                   sdesc_sw128(vb + kk * 16 * 128, 16384, 1024), kIdescPV,
-                   (first_pv[X] && kk == 0) ? 0u : 1u);
-          first_pv[X] = false;
-        };
-        for (int kt = kt_begin; kt < kt_end && ok; ++kt) {
-          const int c0 = classify(p, rows[0], 0, kt, cls_any, cls_all);
-          const int c1 = classify(p, rows[1], 1, kt, cls_any, cls_all);
-          if (c0 == kEmpty && c1 == kEmpty) continue;
-          const int kslot = it % NS, kphase = (it / NS) & 1;
-          ++it;
-          const int vslot = it % NS, vphase = (it / NS) & 1;
-          ++it;
-          if (!(ok = mbar_wait(bar(Lay::B_KVF + kslot), kphase, abort_flag))) break;
+            mma_ts(tmem + 2 * kBN + X * V, tmem + X * kBN + kk * 8, b0 + kk * 128, kIdescPV,
+                   kk == 0 ? acc0 : 1u);
+        }
+        first_pv[X] = false;
+      };
+      auto commit = [&](int b) {
+        if (leader) tc_commit(bar(b));
+      };
+      for (int kt = kt_begin; kt < kt_end && ok; ++kt) {
+        const int c0 = classify(p, rows[0], 0, kt, cls_any, cls_all);
+        const int c1 = classify(p, rows[1], 1, kt, cls_any, cls_all);
+        if (c0 == kEmpty && c1 == kEmpty) continue;
+        const int kslot = it % NS, kphase = (it / NS) & 1;
+        ++it;
+        const int vslot = it % NS, vphase = (it / NS) & 1;
+        ++it;
+        if (!(ok = mbar_wait(bar(Lay::B_KVF + kslot), kphase, abort_flag))) break;
+        tc_fence_after();
+        if (c0 != kEmpty) {
+          issue_s(0, kslot);
+          commit(Lay::B_S + 0);
+        }
+        if (pend_b) {
+          if (!(ok = mbar_wait(bar(Lay::B_P + 1), pend_b_phase, abort_flag))) break;
           tc_fence_after();
-          if (c0 != kEmpty) {
-            issue_s(0, kslot);
-            tc_commit(bar(Lay::B_S + 0));
-          }
-          if (pend_b) {
-            if (!(ok = mbar_wait(bar(Lay::B_P + 1), pend_b_phase, abort_flag))) break;
-            tc_fence_after();
-            issue_pv(1, pend_vslot);
-          }
-          if (have_prev) tc_commit(bar(Lay::B_KVE + pend_vslot));
-          if (c1 != kEmpty) {
-            issue_s(1, kslot);
-            tc_commit(bar(Lay::B_S + 1));
-          }
-          tc_commit(bar(Lay::B_KVE + kslot));
-          if (!(ok = mbar_wait(bar(Lay::B_KVF + vslot), vphase, abort_flag))) break;
+          issue_pv(1, pend_vslot);
+        }
+        if (have_prev) commit(Lay::B_KVE + pend_vslot);
+        if (c1 != kEmpty) {
+          issue_s(1, kslot);
+          commit(Lay::B_S + 1);
+        }
+        commit(Lay::B_KVE + kslot);
+        if (!(ok = mbar_wait(bar(Lay::B_KVF + vslot), vphase, abort_flag))) break;
+        tc_fence_after();
+        if (c0 != kEmpty) {
+          if (!(ok = mbar_wait(bar(Lay::B_P + 0), cnt[0] & 1, abort_flag))) break;
           tc_fence_after();
-          if (c0 != kEmpty) {
-            if (!(ok = mbar_wait(bar(Lay::B_P + 0), cnt[0] & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_pv(0, vslot);
-            ++cnt[0];
-          }
-          pend_b = c1 != kEmpty;
-          pend_b_phase = cnt[1] & 1;
-          if (pend_b) ++cnt[1];
-          pend_vslot = vslot;
-          have_prev = true;
+          issue_pv(0, vslot);
+          ++cnt[0];
         }
-        if (ok && pend_b) {
-          if ((ok = mbar_wait(bar(Lay::B_P + 1), pend_b_phase, abort_flag))) {
-            tc_fence_after();
-            issue_pv(1, pend_vslot);
-          }
-        }
-        if (ok && have_prev) tc_commit(bar(Lay::B_KVE + pend_vslot));
-        tc_commit(bar(Lay::B_O + 0));
-        tc_commit(bar(Lay::B_O + 1));
-        if (!ok) {
-          raise_status(p.status, kStatusTimeout);
-          *abort_flag = 1;
-        }
-        // Drain: every MMA issued by this thread has completed before teardown.
-        tc_commit(bar(Lay::B_DRAIN));
-        mbar_wait(bar(Lay::B_DRAIN), 0, abort_flag);
+        pend_b = c1 != kEmpty;
+        pend_b_phase = cnt[1] & 1;
+        if (pend_b) ++cnt[1];
+        pend_vslot = vslot;
+        have_prev = true;
       }
+      if (ok && pend_b) {
+        if ((ok = mbar_wait(bar(Lay::B_P + 1), pend_b_phase, abort_flag))) {
+          tc_fence_after();
+          issue_pv(1, pend_vslot);
+        }
+      }
+      if (ok && have_prev) commit(Lay::B_KVE + pend_vslot);
+      commit(Lay::B_O + 0);
+      commit(Lay::B_O + 1);
+      __syncwarp();
+      if (!ok && leader) {
+        raise_status(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      // Drain: every MMA issued by this warp has completed before teardown.
+      commit(Lay::B_DRAIN);
+      mbar_wait(bar(Lay::B_DRAIN), 0, abort_flag);
     }
   } else {
     // Softmax warpgroups: thread = one query row of tile X.
