@@ -359,11 +359,14 @@ def run_gpu(args, w):
     dom_flops = f_fwd if dom == ex.KERNEL_FWD else f_bwd
     dom_name = "fwd" if dom == ex.KERNEL_FWD else "bwd"
     achieved = dom_flops / (kern_ms[dom] * 1e-3) / 1e12
-    tc = args.path == "auto" and w.dtype == "bf16"
-    roofline = {"kernel": f"{'tc' if tc else 'simt'}_{dom_name}",
+    tc = args.path != "simt" and w.dtype == "bf16" and w.d == w.v and w.d in (64, 128)
+    tag = f"{'tc' if tc else 'simt'}_{dom_name}"
+    if tc and dom_name == "bwd":
+        tag += "_atomic" if args.path == "atomic_dq" else "_split"
+    roofline = {"kernel": tag,
                 "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_kind": f"bf16 dense burst, of {peak_kind}",
-                "traffic": read_traffic(f"{'tc' if tc else 'simt'}_{dom_name}"),
+                "traffic": read_traffic(tag),
                 "kernel_ms": {"fwd": kern_ms[ex.KERNEL_FWD], "bwd": kern_ms[ex.KERNEL_BWD]}}
     line = {
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
@@ -399,7 +402,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=3)
     ap.add_argument("--variant", default="")
-    ap.add_argument("--path", choices=["auto", "simt"], default="auto")
+    ap.add_argument("--path", choices=["auto", "simt", "atomic_dq"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)

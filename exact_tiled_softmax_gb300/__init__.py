@@ -23,7 +23,7 @@ MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_BITMASK = 0, 1, 2, 3
 _MASKS = {"none": MASK_NONE, "causal": MASK_CAUSAL, "window": MASK_WINDOW,
           "bitmask": MASK_BITMASK}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
-_PATHS = {"auto": 0, "simt": 1}
+_PATHS = {"auto": 0, "simt": 1, "atomic_dq": 2}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lib = None
@@ -85,7 +85,8 @@ def load_library():
 
 
 def set_path(path: str) -> str:
-    """Process-wide kernel path: "auto" (tensor-core kernels where supported) or "simt"."""
+    """Process-wide kernel path: "auto" (tensor-core kernels where supported), "simt",
+    or "atomic_dq" (auto, with the fp32-atomic dQ form of the reverse pass)."""
     prev = load_library().exattn_set_path(_PATHS[path])
     return {v: k for k, v in _PATHS.items()}[prev]
 
@@ -196,7 +197,7 @@ def bwd_noalloc(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, d
     return dq, dk, dv
 
 
-KERNEL_FWD, KERNEL_DELTA, KERNEL_BWD, KERNEL_DQ_CONVERT = 0, 1, 2, 3
+KERNEL_FWD, KERNEL_DELTA, KERNEL_BWD, KERNEL_DQ_CONVERT, KERNEL_BWD_Q = 0, 1, 2, 3, 4
 
 
 def record_kernel_events(which: int, start, stop) -> None:

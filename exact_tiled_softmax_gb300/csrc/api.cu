@@ -118,7 +118,8 @@ int cuda_status(cudaError_t e, const char* where) {
 
 
 int exattn_set_path(int path) {
-  if (path != EXATTN_PATH_AUTO && path != EXATTN_PATH_SIMT) return -1;
+  if (path != EXATTN_PATH_AUTO && path != EXATTN_PATH_SIMT && path != EXATTN_PATH_ATOMIC_DQ)
+    return -1;
   return g_path.exchange(path);
 }
 
@@ -161,7 +162,7 @@ int attn_fwd(const exattn_shape* shape, const void* Q, const void* K, const void
   a.status = static_cast<unsigned*>(workspace);
   cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes, s);
   if (e != cudaSuccess) return cuda_status(e, "attn_fwd: clearing the status word");
-  if (g_path.load() == EXATTN_PATH_AUTO && tc_fwd_supported(a.p))
+  if (g_path.load() != EXATTN_PATH_SIMT && tc_fwd_supported(a.p))
     return cuda_status(launch_tc_fwd(a, s), "attn_fwd: tensor-core forward launch");
   return cuda_status(launch_simt_fwd(a, s), "attn_fwd: SIMT forward launch");
 }
@@ -205,11 +206,18 @@ int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void
   const size_t acc_bytes = sizeof(float) * (size_t)a.p.BH * a.p.n * a.p.d;
   cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes, s);
   if (e != cudaSuccess) return cuda_status(e, "attn_bwd: clearing the status word");
+  const int path = g_path.load();
+  if (path == EXATTN_PATH_AUTO && tc_bwd_split_supported(a.p)) {
+    // Split form: dQ is written directly, no accumulator.
+    e = launch_delta(a, s);
+    if (e != cudaSuccess) return cuda_status(e, "attn_bwd: delta launch");
+    return cuda_status(launch_tc_bwd_split(a, s), "attn_bwd: reverse kernel launch");
+  }
   e = cudaMemsetAsync(a.dQacc, 0, acc_bytes, s);
   if (e != cudaSuccess) return cuda_status(e, "attn_bwd: clearing the dQ accumulator");
   e = launch_delta(a, s);
   if (e != cudaSuccess) return cuda_status(e, "attn_bwd: delta launch");
-  if (g_path.load() == EXATTN_PATH_AUTO && tc_bwd_supported(a.p))
+  if (path != EXATTN_PATH_SIMT && tc_bwd_supported(a.p))
     e = launch_tc_bwd(a, s);
   else
     e = launch_simt_bwd(a, s);

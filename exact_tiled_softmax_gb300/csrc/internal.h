@@ -49,7 +49,14 @@ struct BwdArgs {
 
 // Profiling hooks (api.cu): every kernel launch goes through these so the
 // launch counter and the one-shot event hooks see it.
-enum KernelRole { kKernFwd = 0, kKernDelta = 1, kKernBwd = 2, kKernDqConvert = 3, kKernRoles = 4 };
+enum KernelRole {
+  kKernFwd = 0,
+  kKernDelta = 1,
+  kKernBwd = 2,
+  kKernDqConvert = 3,
+  kKernBwdQ = 4,
+  kKernRoles = 5
+};
 void before_launch(int role, cudaStream_t s);
 // Remember the last failing step of this host thread (exattn_last_error).
 void record_error(const char* where, int code, const char* detail);
@@ -65,7 +72,12 @@ cudaError_t launch_delta(const BwdArgs& a, cudaStream_t s);
 // dQ = dQacc converted to the output dtype.
 cudaError_t launch_dq_convert(const BwdArgs& a, cudaStream_t s);
 
-// tcgen05 / TMA / TMEM kernels (bf16, d and v multiples of 16 up to 128).
+// tcgen05 / TMA / TMEM kernels (bf16, d = v in {64, 128}).
+// The reverse pass has two forms: the split form (a key-major dK/dV kernel and
+// a query-major dQ kernel, no atomics; the default) and the atomic form (one
+// key-major kernel adding dQ into an fp32 accumulator).
+bool tc_bwd_split_supported(const Problem& p);
+cudaError_t launch_tc_bwd_split(const BwdArgs& a, cudaStream_t s);
 bool tc_fwd_supported(const Problem& p);
 cudaError_t launch_tc_fwd(const FwdArgs& a, cudaStream_t s);
 bool tc_bwd_supported(const Problem& p);

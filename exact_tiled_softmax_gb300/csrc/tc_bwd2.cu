@@ -1,0 +1,888 @@
+// Reverse pass on the sm_103a tensor cores as two kernels without atomics.
+//
+// Implements the Reverse procedure of "Exact tiled softmax attention with
+// block-recomputed vector-Jacobian products" with frozen statistics:
+//   p_ij = exp(s_ij - L_i),  gamma_ij = p_ij (G_i . V_j - delta_i),
+//   dK_j += c gamma_ij Q_i,  dV_j += p_ij G_i     (tc_bwd_kv_kernel, key-major)
+//   dQ_i += c gamma_ij K_j                         (tc_bwd_q_kernel, query-major)
+// with delta_i = G_i . Y_i (HarshvardhanJ/FlashAttention, backward section).
+// Each kernel recomputes the probability block it needs; neither stores an
+// n x n matrix, and dQ is written once per query block, so no fp32
+// accumulator or reductions are needed.
+//
+// tc_bwd_kv_kernel -- one CTA per 128-key block, loop over query blocks.
+//   TMEM: A [0,128) S^T then P^T (bf16), B [128,256) dP^T then dS^T (bf16),
+//   dV [256, 256+V), dK [256+V, 256+V+D).  S^T and dP^T are computed in two
+//   64-query halves so that the elementwise work of one half overlaps the MMAs
+//   of the other; dV and dK then take each half as a K = 64 contraction.
+// tc_bwd_q_kernel -- one CTA per 128-query block, loop over key blocks.
+//   K/V ring order V(0), K(0), V(1), K(1), ...
+//   TMEM: S [0,128), dP double buffer [128,256) and [256,384) (dS bf16 is
+//   written over its own dP), dQ [384, 384+D).  S(t+1) is issued as soon as
+//   the elementwise warps have read S(t); dP(t+1) into the other buffer even
+//   earlier.
+// Warp roles (both kernels, 18 warps): warps 0-15 elementwise, four groups of
+// 32 columns (group = warp / 4, TMEM lane quarter = warp % 4); warp 16 TMA;
+// warp 17 MMA.  The producer warps run warp-uniform loops and one elected
+// lane issues.  Every mbarrier wait is bounded (1 s).
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace exattn {
+
+bool make_tmap_bf16(CUtensorMap* m, const void* base, int width, int n, int BH);
+bool tmap_encoder_available();
+
+namespace {
+
+using namespace tc;
+
+constexpr int kBM = 128;  // queries per block
+constexpr int kBN = 128;  // keys per block
+constexpr int kThreads = 576;
+constexpr int kEwWarps = 16;
+constexpr int kWarpTMA = 16;
+constexpr int kWarpMMA = 17;
+constexpr int kMaxBlocks = 256;  // blocks covered by the in-kernel bitmask tile table
+constexpr uint32_t kTmemCols = 512;
+
+enum : int { kEmpty = 0, kFull = 1, kPartial = 2 };
+
+struct Bwd2Params {
+  CUtensorMap tq, tk, tv, tdy;
+  int n, npad, BH, mask_kind, window, words_per_row;
+  const uint32_t* bits;
+  const float* delta;  // [BH][npad]
+  const float* lse2;   // [BH][npad]  L log2(e), +inf on padding / empty rows
+  float sl2;           // c log2(e)
+  float scale;         // c
+  __nv_bfloat16* dQ;
+  __nv_bfloat16* dK;
+  __nv_bfloat16* dV;
+  unsigned* status;
+};
+
+__device__ __forceinline__ uint32_t range_bits(int a, int b) {
+  a = max(a, 0);
+  b = min(b, 31);
+  if (a > b) return 0u;
+  const uint32_t width = static_cast<uint32_t>(b - a + 1);
+  const uint32_t m = width == 32 ? 0xFFFFFFFFu : ((1u << width) - 1u);
+  return m << a;
+}
+
+// Classification of the (query block qb, key block kb) tile.  Bitmask tiles
+// come from a table the kernel builds (bit t of any/notall for block t of the
+// loop dimension).
+__device__ __forceinline__ int classify_tile(const Bwd2Params& p, int qb, int kb, bool any_bit,
+                                             bool notall_bit) {
+  const int n = p.n;
+  const int k0 = kb * kBN;
+  const bool key_tail = k0 + kBN > n;
+  const int k1 = min(k0 + kBN, n) - 1;
+  const int q0 = qb * kBM;
+  const int q1 = min(q0 + kBM, n) - 1;
+  switch (p.mask_kind) {
+    case kMaskCausal:
+      if (q1 < k0) return kEmpty;
+      return (q0 >= k0 + kBN - 1 && !key_tail) ? kFull : kPartial;
+    case kMaskWindow:
+      if (q1 < k0 || q0 > k1 + p.window - 1) return kEmpty;
+      return (q0 >= k0 + kBN - 1 && q1 <= k0 + p.window - 1 && !key_tail) ? kFull : kPartial;
+    case kMaskBitmask:
+      if (!any_bit) return kEmpty;
+      return (notall_bit || key_tail) ? kPartial : kFull;
+    default:
+      return key_tail ? kPartial : kFull;
+  }
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Bitmask tile table for one CTA: for each block t of the loop range, does any
+// (query, key) pair of the tile allow attention, and is some existing pair
+// not allowed?  key_major: the CTA owns key block `fixed` and loops over query
+// blocks; otherwise it owns query block `fixed` and loops over key blocks.
+__device__ void build_bitmask_table(const Bwd2Params& p, bool key_major, int fixed, int t_begin,
+                                    int t_end, uint32_t* anyb, uint32_t* notallb) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = p.n;
+  if (key_major) {
+    // One warp = 32 query rows of one query block; key words of block `fixed`.
+    for (int i0 = t_begin * kBM + warp * 32; i0 < t_end * kBM; i0 += kThreads) {
+      const int i = i0 + lane;
+      bool any = false, all = true;
+      if (i < n) {
+        const uint32_t* row = p.bits + static_cast<size_t>(i) * p.words_per_row;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int w = fixed * 4 + q;
+          const uint32_t valid = range_bits(0, n - 1 - 32 * w);
+          const uint32_t word = w < p.words_per_row ? __ldg(row + w) & valid : 0u;
+          any |= word != 0u;
+          all &= word == valid;
+        }
+      }
+      const int t = i0 / kBM;
+      const bool wany = __any_sync(0xFFFFFFFFu, any);
+      const bool wnotall = __any_sync(0xFFFFFFFFu, i < n && !all);
+      if (lane == 0 && wany) atomicOr(&anyb[t >> 5], 1u << (t & 31));
+      if (lane == 0 && wnotall) atomicOr(&notallb[t >> 5], 1u << (t & 31));
+    }
+  } else {
+    // The CTA's 128 query rows; thread = (row, key block) pairs.
+    for (int idx = threadIdx.x; idx < kBM * (t_end - t_begin); idx += kThreads) {
+      const int r = idx % kBM;
+      const int t = t_begin + idx / kBM;
+      const int i = fixed * kBM + r;
+      if (i >= n) continue;
+      const uint32_t* row = p.bits + static_cast<size_t>(i) * p.words_per_row;
+      bool any = false, all = true;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int w = t * 4 + q;
+        const uint32_t valid = range_bits(0, n - 1 - 32 * w);
+        const uint32_t word = w < p.words_per_row ? __ldg(row + w) & valid : 0u;
+        any |= word != 0u;
+        all &= word == valid;
+      }
+      if (any) atomicOr(&anyb[t >> 5], 1u << (t & 31));
+      if (!all) atomicOr(&notallb[t >> 5], 1u << (t & 31));
+    }
+  }
+}
+
+// =========================================================================
+// Key-major kernel: dK, dV
+// =========================================================================
+template <int D, int V>
+struct KvLayout {
+  static constexpr int KBYTES = kBN * D * 2;
+  static constexpr int VBYTES = kBN * V * 2;
+  static constexpr int QBYTES = kBM * D * 2;
+  static constexpr int YBYTES = kBM * V * 2;
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + KBYTES;
+  static constexpr int STAGE_OFF = V_OFF + VBYTES;
+  static constexpr int STAGE = QBYTES + YBYTES;
+  static constexpr int NST = 2;
+  static constexpr int VEC_OFF = STAGE_OFF + NST * STAGE;  // per stage: delta[128], lse2[128]
+  static constexpr int BAR_OFF = VEC_OFF + NST * 1024;
+  static constexpr int B_KV = 0, B_QF = 1, B_QE = B_QF + NST, B_SDP = B_QE + NST, B_DS = B_SDP + 2,
+                       B_DONE = B_DS + 2, B_DRAIN = B_DONE + 1, NBAR = B_DRAIN + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int CLS_OFF = MISC_OFF + 16;
+  static constexpr int TOTAL = CLS_OFF + 2 * (kMaxBlocks / 32) * 4;
+  static_assert(TOTAL <= 232448, "shared memory");
+};
+
+template <int D, int V>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_bwd_kv_kernel(const __grid_constant__ Bwd2Params p) {
+  using Lay = KvLayout<D, V>;
+  constexpr int NST = Lay::NST;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + Lay::BAR_OFF;
+  auto bar = [&](int k) { return bar0 + 8u * k; };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  uint32_t* anyb = reinterpret_cast<uint32_t*>(smem + Lay::CLS_OFF);
+  uint32_t* notallb = anyb + kMaxBlocks / 32;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kb = blockIdx.x;  // causal: low key blocks have the most query blocks
+  const int bh = blockIdx.y;
+  const int n = p.n;
+  const int k0 = kb * kBN;
+  const int nqb = (n + kBM - 1) / kBM;
+  int qb_begin = 0, qb_end = nqb;
+  if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) qb_begin = kb;
+  if (p.mask_kind == kMaskWindow)
+    qb_end = min(nqb, (min(k0 + kBN, n) - 1 + p.window - 1) / kBM + 1);
+
+  if ((sbase & 1023u) != 0u) {
+    if (threadIdx.x == 0) raise_status(p.status, kStatusTimeout);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(bar(Lay::B_KV), 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(bar(Lay::B_QF + s), 1);
+      mbar_init(bar(Lay::B_QE + s), 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(Lay::B_SDP + h), 1);
+      mbar_init(bar(Lay::B_DS + h), 8 * 32);
+    }
+    mbar_init(bar(Lay::B_DONE), 1);
+    mbar_init(bar(Lay::B_DRAIN), 1);
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMMA) {
+    tmem_alloc(sbase + Lay::MISC_OFF, kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  if (threadIdx.x < 2 * (kMaxBlocks / 32)) anyb[threadIdx.x] = 0u;
+  __syncthreads();
+  if (p.mask_kind == kMaskBitmask)
+    build_bitmask_table(p, true, kb, qb_begin, qb_end, anyb, notallb);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const uint32_t tA = tmem, tB = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + V;
+  auto cls_of = [&](int qb) {
+    return classify_tile(p, qb, kb, (anyb[qb >> 5] >> (qb & 31)) & 1u,
+                         (notallb[qb >> 5] >> (qb & 31)) & 1u);
+  };
+
+  if (warp == kWarpTMA) {
+    const bool leader = elect_one();
+    if (leader) {
+      prefetch_tmap(&p.tq);
+      prefetch_tmap(&p.tk);
+      prefetch_tmap(&p.tv);
+      prefetch_tmap(&p.tdy);
+    }
+    const uint64_t keep = policy_evict_last();
+    if (leader) {
+      mbar_arrive_expect_tx(bar(Lay::B_KV), Lay::KBYTES + Lay::VBYTES);
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(sbase + Lay::K_OFF + c * 16384, &p.tk, bar(Lay::B_KV), 64 * c, k0, bh, keep);
+      for (int c = 0; c < V / 64; ++c)
+        tma_load_3d(sbase + Lay::V_OFF + c * 16384, &p.tv, bar(Lay::B_KV), 64 * c, k0, bh, keep);
+    }
+    int it = 0;
+    int last_phase[NST];
+    for (int s = 0; s < NST; ++s) last_phase[s] = -1;
+    bool ok = true;
+    for (int qb = qb_begin; qb < qb_end; ++qb) {
+      if (cls_of(qb) == kEmpty) continue;
+      const int slot = it % NST, phase = (it / NST) & 1;
+      ++it;
+      if (!(ok = mbar_wait(bar(Lay::B_QE + slot), phase ^ 1, abort_flag))) break;
+      const uint32_t st = sbase + Lay::STAGE_OFF + slot * Lay::STAGE;
+      const uint32_t fb = bar(Lay::B_QF + slot);
+      if (leader) {
+        mbar_arrive_expect_tx(fb, Lay::QBYTES + Lay::YBYTES + 1024);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(st + c * 16384, &p.tq, fb, 64 * c, qb * kBM, bh, keep);
+        for (int c = 0; c < V / 64; ++c)
+          tma_load_3d(st + Lay::QBYTES + c * 16384, &p.tdy, fb, 64 * c, qb * kBM, bh, keep);
+        const size_t vo = static_cast<size_t>(bh) * p.npad + qb * kBM;
+        const uint32_t vec = sbase + Lay::VEC_OFF + slot * 1024;
+        bulk_load(vec, p.delta + vo, 512, fb);
+        bulk_load(vec + 512, p.lse2 + vo, 512, fb);
+      }
+      last_phase[slot] = phase;
+    }
+    __syncwarp();
+    if (!ok && leader) {
+      raise_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+    for (int s = 0; s < NST; ++s)
+      if (last_phase[s] >= 0) mbar_wait(bar(Lay::B_QF + s), last_phase[s], abort_flag);
+    mbar_wait(bar(Lay::B_KV), 0, abort_flag);
+  } else if (warp == kWarpMMA) {
+    const bool leader = elect_one();
+    constexpr uint32_t kIdHalf = idesc_bf16(kBN, 64, false, false);
+    constexpr uint32_t kIdDV = idesc_bf16(kBN, V, false, true);
+    constexpr uint32_t kIdDK = idesc_bf16(kBN, D, false, true);
+    const uint64_t dK0 = sdesc_sw128(sbase + Lay::K_OFF, 16, 1024);
+    const uint64_t dV0 = sdesc_sw128(sbase + Lay::V_OFF, 16, 1024);
+    const uint64_t dSt = sdesc_sw128(sbase + Lay::STAGE_OFF, 16, 1024);     // K-major view
+    const uint64_t dSm = sdesc_sw128(sbase + Lay::STAGE_OFF, 16384, 1024);  // MN-major view
+    constexpr uint32_t kStage16 = Lay::STAGE >> 4, kQ16 = Lay::QBYTES >> 4;
+    bool ok = mbar_wait(bar(Lay::B_KV), 0, abort_flag);
+    tc_fence_after();
+    int it = 0;
+    for (int qb = qb_begin; qb < qb_end && ok; ++qb) {
+      if (cls_of(qb) == kEmpty) continue;
+      const int slot = it % NST, phase = (it / NST) & 1;
+      if (!(ok = mbar_wait(bar(Lay::B_QF + slot), phase, abort_flag))) break;
+      tc_fence_after();
+      const uint64_t q_k = dSt + slot * kStage16;          // Q_i, K-major
+      const uint64_t y_k = dSt + slot * kStage16 + kQ16;   // dY_i, K-major
+      const uint64_t q_m = dSm + slot * kStage16;          // Q_i, MN-major
+      const uint64_t y_m = dSm + slot * kStage16 + kQ16;   // dY_i, MN-major
+      // Halves h: queries 64h..64h+63 (rows 64h of the stage tiles: +64*128 B).
+      for (int h = 0; h < 2; ++h) {
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < V / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            mma_ss(tB + 64 * h, dV0 + off, y_k + off + h * 512, kIdHalf, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            mma_ss(tA + 64 * h, dK0 + off, q_k + off + h * 512, kIdHalf, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(Lay::B_SDP + h));
+        }
+      }
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = mbar_wait(bar(Lay::B_DS + h), it & 1, abort_flag))) break;
+        tc_fence_after();
+        if (leader) {
+          // dV += P^T[:, 64h..] dY_i[64h..], dK += dS^T[:, 64h..] Q_i[64h..]  (K = 64 queries)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acol = 64 * h + 32 * (kk >> 1) + 8 * (kk & 1);
+            const uint32_t rows16 = (64 * h + 16 * kk) * 128 >> 4;
+            const uint32_t acc = (it > 0 || h > 0 || kk > 0) ? 1u : 0u;
+            mma_ts(tdV, tA + acol, y_m + rows16, kIdDV, acc);
+            mma_ts(tdK, tB + acol, q_m + rows16, kIdDK, acc);
+          }
+        }
+      }
+      if (!ok) break;
+      if (leader) tc_commit(bar(Lay::B_QE + slot));
+      ++it;
+    }
+    if (leader) tc_commit(bar(Lay::B_DONE));
+    __syncwarp();
+    if (!ok && leader) {
+      raise_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+    if (leader) tc_commit(bar(Lay::B_DRAIN));
+    mbar_wait(bar(Lay::B_DRAIN), 0, abort_flag);
+  } else {
+    // Elementwise: thread = key row r of the block; group g covers queries
+    // 32g..32g+31 (half h = g / 2).
+    const int g = warp >> 2, wl = warp & 3, h = g >> 1;
+    const int r = wl * 32 + lane;
+    const int j = k0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(wl * 32) << 16;
+    const float sl2 = p.sl2;
+    int it = 0;
+    bool ok = true;
+    for (int qb = qb_begin; qb < qb_end; ++qb) {
+      const int cls = cls_of(qb);
+      if (cls == kEmpty) continue;
+      const int slot = it % NST;
+      if (!(ok = mbar_wait(bar(Lay::B_SDP + h), it & 1, abort_flag))) break;
+      tc_fence_after();
+      const float* dvec = reinterpret_cast<const float*>(smem + Lay::VEC_OFF + slot * 1024);
+      const float* lvec = dvec + 128;
+      const int q0 = qb * kBM;
+      const int cb = 32 * g;
+      uint32_t allow = 0xFFFFFFFFu;
+      if (cls == kPartial) {
+        if (j >= n) {
+          allow = 0u;
+        } else if (p.mask_kind == kMaskCausal) {
+          allow = range_bits(j - q0 - cb, 31);
+        } else if (p.mask_kind == kMaskWindow) {
+          allow = range_bits(j - q0 - cb, j + p.window - 1 - q0 - cb);
+        } else if (p.mask_kind == kMaskBitmask) {
+          allow = 0u;
+          const uint32_t* col = p.bits + (j >> 5);
+#pragma unroll 4
+          for (int e = 0; e < 32; ++e) {
+            const int i = q0 + cb + e;
+            if (i < n)
+              allow |= ((__ldg(col + static_cast<size_t>(i) * p.words_per_row) >> (j & 31)) & 1u)
+                       << e;
+          }
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {  // two chunks of 16 queries
+        uint32_t s[16], dp[16];
+        tmem_ld16(tA + lane_off + cb + 16 * c, s);
+        tmem_ld16(tB + lane_off + cb + 16 * c, dp);
+        tmem_ld_wait();
+        reg_fence(s);
+        reg_fence(dp);
+        uint32_t pk[8], dk[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lvec + cb + 16 * c + e);
+          const float4 d4 = *reinterpret_cast<const float4*>(dvec + cb + 16 * c + e);
+          const float la[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float da[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], gv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float pp = ex2(fmaf(__uint_as_float(s[e + u]), sl2, -la[u]));
+            if (!((allow >> (16 * c + e + u)) & 1u)) pp = 0.f;
+            pv[u] = pp;
+            gv[u] = pp * (__uint_as_float(dp[e + u]) - da[u]);
+          }
+          pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
+          pk[e / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+          dk[e / 2] = pack_bf16x2(gv[0], gv[1]);
+          dk[e / 2 + 1] = pack_bf16x2(gv[2], gv[3]);
+        }
+        // P^T / dS^T (bf16 pairs) over the first 16 columns of this group's range.
+        tmem_st8(tA + lane_off + cb + 8 * c, pk);
+        tmem_st8(tB + lane_off + cb + 8 * c, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(Lay::B_DS + h));
+      ++it;
+    }
+    if (!ok) {
+      raise_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+    // Epilogue: group 0 writes dV rows, group 1 dK rows (scaled by c).
+    if (g < 2) {
+      bool have = ok && it > 0;
+      if (have) {
+        have = mbar_wait(bar(Lay::B_DONE), 0, abort_flag);
+        tc_fence_after();
+      }
+      const int W = g == 0 ? V : D;
+      const uint32_t tsrc = (g == 0 ? tdV : tdK) + lane_off;
+      const float mul = g == 0 ? 1.f : p.scale;
+      __nv_bfloat16* dst =
+          (g == 0 ? p.dV : p.dK) + (static_cast<size_t>(bh) * n + (j < n ? j : 0)) * W;
+      for (int ch = 0; ch < W / 16; ++ch) {
+        uint32_t o[16];
+        if (have) {
+          tmem_ld16(tsrc + ch * 16, o);
+          tmem_ld_wait();
+          reg_fence(o);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = 0u;
+        }
+        if (j < n) {
+          uint32_t ov[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            ov[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 16);
+          d4[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+          d4[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// =========================================================================
+// Query-major kernel: dQ
+// =========================================================================
+template <int D, int V>
+struct QLayout {
+  static constexpr int QBYTES = kBM * D * 2;
+  static constexpr int YBYTES = kBM * V * 2;
+  static constexpr int KBYTES = kBN * D * 2;
+  static constexpr int VBYTES = kBN * V * 2;
+  static constexpr int SLOT = KBYTES > VBYTES ? KBYTES : VBYTES;
+  static constexpr int NS = D == 128 ? 5 : 8;  // K and V tiles alternate in one ring
+  static constexpr int Q_OFF = 0;
+  static constexpr int Y_OFF = QBYTES;
+  static constexpr int SLOT_OFF = Y_OFF + YBYTES;
+  static constexpr int BAR_OFF = SLOT_OFF + NS * SLOT;
+  static constexpr int B_Q = 0, B_KVF = 1, B_KVE = B_KVF + NS, B_SDP = B_KVE + NS,
+                       B_DS = B_SDP + 1, B_DONE = B_DS + 1, B_DRAIN = B_DONE + 1,
+                       NBAR = B_DRAIN + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int CLS_OFF = MISC_OFF + 16;
+  static constexpr int TOTAL = CLS_OFF + 2 * (kMaxBlocks / 32) * 4;
+  static_assert(TOTAL <= 232448, "shared memory");
+};
+
+template <int D, int V>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_bwd_q_kernel(const __grid_constant__ Bwd2Params p) {
+  using Lay = QLayout<D, V>;
+  constexpr int NS = Lay::NS;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + Lay::BAR_OFF;
+  auto bar = [&](int k) { return bar0 + 8u * k; };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  uint32_t* anyb = reinterpret_cast<uint32_t*>(smem + Lay::CLS_OFF);
+  uint32_t* notallb = anyb + kMaxBlocks / 32;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nqb = (p.n + kBM - 1) / kBM;
+  const int qb = nqb - 1 - blockIdx.x;  // causal: high query blocks have the most key blocks
+  const int bh = blockIdx.y;
+  const int n = p.n;
+  const int q0 = qb * kBM;
+  const int q1 = min(q0 + kBM, n) - 1;
+  const int nkb = (n + kBN - 1) / kBN;
+  int kb_begin = 0, kb_end = nkb;
+  if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) kb_end = min(nkb, q1 / kBN + 1);
+  if (p.mask_kind == kMaskWindow) kb_begin = max(0, q0 - p.window + 1) / kBN;
+
+  if ((sbase & 1023u) != 0u) {
+    if (threadIdx.x == 0) raise_status(p.status, kStatusTimeout);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(bar(Lay::B_Q), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar(Lay::B_KVF + s), 1);
+      mbar_init(bar(Lay::B_KVE + s), 1);
+    }
+    mbar_init(bar(Lay::B_SDP), 1);
+    mbar_init(bar(Lay::B_DS), kEwWarps * 32);
+    mbar_init(bar(Lay::B_DONE), 1);
+    mbar_init(bar(Lay::B_DRAIN), 1);
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMMA) {
+    tmem_alloc(sbase + Lay::MISC_OFF, kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  if (threadIdx.x < 2 * (kMaxBlocks / 32)) anyb[threadIdx.x] = 0u;
+  __syncthreads();
+  if (p.mask_kind == kMaskBitmask)
+    build_bitmask_table(p, false, qb, kb_begin, kb_end, anyb, notallb);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const uint32_t tS = tmem, tD0 = tmem + 128, tQ = tmem + 384;
+  auto cls_of = [&](int kb) {
+    return classify_tile(p, qb, kb, (anyb[kb >> 5] >> (kb & 31)) & 1u,
+                         (notallb[kb >> 5] >> (kb & 31)) & 1u);
+  };
+
+  if (warp == kWarpTMA) {
+    const bool leader = elect_one();
+    if (leader) {
+      prefetch_tmap(&p.tq);
+      prefetch_tmap(&p.tk);
+      prefetch_tmap(&p.tv);
+      prefetch_tmap(&p.tdy);
+    }
+    const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
+    if (leader) {
+      mbar_arrive_expect_tx(bar(Lay::B_Q), Lay::QBYTES + Lay::YBYTES);
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(sbase + Lay::Q_OFF + c * 16384, &p.tq, bar(Lay::B_Q), 64 * c, q0, bh, stream);
+      for (int c = 0; c < V / 64; ++c)
+        tma_load_3d(sbase + Lay::Y_OFF + c * 16384, &p.tdy, bar(Lay::B_Q), 64 * c, q0, bh, stream);
+    }
+    int it = 0;
+    int last_phase[NS];
+    for (int s = 0; s < NS; ++s) last_phase[s] = -1;
+    bool ok = true;
+    for (int kb = kb_begin; kb < kb_end && ok; ++kb) {
+      if (cls_of(kb) == kEmpty) continue;
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        const int slot = it % NS, phase = (it / NS) & 1;
+        ++it;
+        if (!mbar_wait(bar(Lay::B_KVE + slot), phase ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = sbase + Lay::SLOT_OFF + slot * Lay::SLOT;
+        if (leader) {
+          // V(t) first, then K(t): V(t) is needed one step earlier (for dP(t))
+          // and each slot is then reused two steps after its last reader.
+          if (kv == 1) {
+            mbar_arrive_expect_tx(bar(Lay::B_KVF + slot), Lay::KBYTES);
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(dst + c * 16384, &p.tk, bar(Lay::B_KVF + slot), 64 * c, kb * kBN, bh,
+                          keep);
+          } else {
+            mbar_arrive_expect_tx(bar(Lay::B_KVF + slot), Lay::VBYTES);
+            for (int c = 0; c < V / 64; ++c)
+              tma_load_3d(dst + c * 16384, &p.tv, bar(Lay::B_KVF + slot), 64 * c, kb * kBN, bh,
+                          keep);
+          }
+        }
+        last_phase[slot] = phase;
+      }
+    }
+    __syncwarp();
+    if (!ok && leader) {
+      raise_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+    for (int s = 0; s < NS; ++s)
+      if (last_phase[s] >= 0) mbar_wait(bar(Lay::B_KVF + s), last_phase[s], abort_flag);
+    mbar_wait(bar(Lay::B_Q), 0, abort_flag);
+  } else if (warp == kWarpMMA) {
+    const bool leader = elect_one();
+    constexpr uint32_t kIdSS = idesc_bf16(kBM, kBN, false, false);
+    constexpr uint32_t kIdDQ = idesc_bf16(kBM, D, false, true);
+    const uint64_t dQk = sdesc_sw128(sbase + Lay::Q_OFF, 16, 1024);
+    const uint64_t dYk = sdesc_sw128(sbase + Lay::Y_OFF, 16, 1024);
+    const uint64_t dSk = sdesc_sw128(sbase + Lay::SLOT_OFF, 16, 1024);
+    const uint64_t dSm = sdesc_sw128(sbase + Lay::SLOT_OFF, 16384, 1024);
+    constexpr uint32_t kSlot16 = Lay::SLOT >> 4;
+    bool ok = mbar_wait(bar(Lay::B_Q), 0, abort_flag);
+    tc_fence_after();
+    // Compact list of the key blocks to visit: recomputed on the fly.
+    auto next_kb = [&](int kb) {
+      for (++kb; kb < kb_end; ++kb)
+        if (cls_of(kb) != kEmpty) return kb;
+      return kb_end;
+    };
+    int kb = next_kb(kb_begin - 1);
+    int t = 0;
+    // Prologue: dP(0) -> D0, S(0) -> S.
+    if (ok && kb < kb_end) {
+      const int vs = 0, ks = 1;
+      if ((ok = mbar_wait(bar(Lay::B_KVF + ks), 0, abort_flag)) &&
+          (ok = mbar_wait(bar(Lay::B_KVF + vs), 0, abort_flag))) {
+        tc_fence_after();
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < V / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            mma_ss(tD0, dYk + off, dSk + vs * kSlot16 + off, kIdSS, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            mma_ss(tS, dQk + off, dSk + ks * kSlot16 + off, kIdSS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(Lay::B_SDP));
+          tc_commit(bar(Lay::B_KVE + vs));  // V(0) is no longer needed once dP(0) is done
+        }
+      }
+    }
+    while (ok && kb < kb_end) {
+      const int kb_next = next_kb(kb);
+      const int ks = (2 * t + 1) % NS;
+      if (kb_next < kb_end) {
+        // dP(t+1) -> the other buffer (its dS(t-1) was read by dQ(t-1), issued earlier).
+        const int it1 = 2 * (t + 1);
+        const int vs1 = it1 % NS, vp1 = (it1 / NS) & 1;
+        const int ks1 = (it1 + 1) % NS, kp1 = ((it1 + 1) / NS) & 1;
+        if (!(ok = mbar_wait(bar(Lay::B_KVF + vs1), vp1, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t tD = tD0 + 128 * ((t + 1) & 1);
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < V / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            mma_ss(tD, dYk + off, dSk + vs1 * kSlot16 + off, kIdSS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(Lay::B_KVE + vs1));
+        }
+        // S(t+1) once the elementwise warps have read S(t) and written dS(t).
+        if (!(ok = mbar_wait(bar(Lay::B_DS), t & 1, abort_flag))) break;
+        if (!(ok = mbar_wait(bar(Lay::B_KVF + ks1), kp1, abort_flag))) break;
+        tc_fence_after();
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            mma_ss(tS, dQk + off, dSk + ks1 * kSlot16 + off, kIdSS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(Lay::B_SDP));
+        }
+      } else {
+        if (!(ok = mbar_wait(bar(Lay::B_DS), t & 1, abort_flag))) break;
+        tc_fence_after();
+      }
+      // dQ += dS(t) K_t  (A = dS bf16 in TMEM over dP(t), keys packed; B = K_t MN-major)
+      const uint32_t tD = tD0 + 128 * (t & 1);
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tQ, tD + 32 * (kk >> 1) + 8 * (kk & 1), dSm + ks * kSlot16 + kk * 128, kIdDQ,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar(Lay::B_KVE + ks));
+      }
+      kb = kb_next;
+      ++t;
+    }
+    if (leader) tc_commit(bar(Lay::B_DONE));
+    __syncwarp();
+    if (!ok && leader) {
+      raise_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+    if (leader) tc_commit(bar(Lay::B_DRAIN));
+    mbar_wait(bar(Lay::B_DRAIN), 0, abort_flag);
+  } else {
+    // Elementwise: thread = query row r; group g covers keys 32g..32g+31.
+    const int g = warp >> 2, wl = warp & 3;
+    const int r = wl * 32 + lane;
+    const int i = q0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(wl * 32) << 16;
+    const float sl2 = p.sl2;
+    const size_t vo = static_cast<size_t>(bh) * p.npad + q0 + r;
+    const float lse2 = p.lse2[vo];   // +inf on padding rows and empty rows: p = 0
+    const float dl = p.delta[vo];
+    int t = 0;
+    bool ok = true;
+    for (int kb = kb_begin; kb < kb_end; ++kb) {
+      const int cls = cls_of(kb);
+      if (cls == kEmpty) continue;
+      if (!(ok = mbar_wait(bar(Lay::B_SDP), t & 1, abort_flag))) break;
+      tc_fence_after();
+      const int kc = kb * kBN + 32 * g;  // first key of this group
+      uint32_t allow = 0xFFFFFFFFu;
+      if (cls == kPartial) {
+        int lo = 0, hi = n - 1;
+        if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) hi = min(hi, i);
+        if (p.mask_kind == kMaskWindow) lo = max(lo, i - p.window + 1);
+        allow = range_bits(lo - kc, hi - kc);
+        if (p.mask_kind == kMaskBitmask) {
+          const int w = kb * 4 + g;
+          allow &= (i < n && w < p.words_per_row)
+                       ? __ldg(p.bits + static_cast<size_t>(i) * p.words_per_row + w)
+                       : 0u;
+        }
+      }
+      const uint32_t tD = tD0 + 128 * (t & 1) + lane_off;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t s[16], dp[16];
+        tmem_ld16(tS + lane_off + 32 * g + 16 * c, s);
+        tmem_ld16(tD + 32 * g + 16 * c, dp);
+        tmem_ld_wait();
+        reg_fence(s);
+        reg_fence(dp);
+        uint32_t dk[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, -lse2));
+          float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -lse2));
+          if (!((allow >> (16 * c + e)) & 1u)) p0 = 0.f;
+          if (!((allow >> (16 * c + e + 1)) & 1u)) p1 = 0.f;
+          dk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dl),
+                                  p1 * (__uint_as_float(dp[e + 1]) - dl));
+        }
+        tmem_st8(tD + 32 * g + 8 * c, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(Lay::B_DS));
+      ++t;
+    }
+    if (!ok) {
+      raise_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+    // Epilogue: dQ_i = c * acc, bf16; group g writes columns 32g.. (D = 128) or
+    // 16g.. (D = 64).
+    bool have = ok && t > 0;
+    if (have) {
+      have = mbar_wait(bar(Lay::B_DONE), 0, abort_flag);
+      tc_fence_after();
+    }
+    constexpr int CW = D / 4;  // columns per group
+    __nv_bfloat16* dst = p.dQ + (static_cast<size_t>(bh) * n + (i < n ? i : 0)) * D + CW * g;
+#pragma unroll
+    for (int ch = 0; ch < CW / 16; ++ch) {
+      uint32_t o[16];
+      if (have) {
+        tmem_ld16(tQ + lane_off + CW * g + 16 * ch, o);
+        tmem_ld_wait();
+        reg_fence(o);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[e] = 0u;
+      }
+      if (i < n) {
+        uint32_t ov[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          ov[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * p.scale,
+                              __uint_as_float(o[2 * e + 1]) * p.scale);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * ch);
+        d4[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+        d4[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
+  const Problem& pr = a.p;
+  Bwd2Params p;
+  if (!make_tmap_bf16(&p.tq, a.Q, D, pr.n, pr.BH) || !make_tmap_bf16(&p.tk, a.K, D, pr.n, pr.BH) ||
+      !make_tmap_bf16(&p.tv, a.V, D, pr.n, pr.BH) ||
+      !make_tmap_bf16(&p.tdy, a.dY, D, pr.n, pr.BH))
+    return cudaErrorInvalidValue;
+  p.n = pr.n;
+  p.npad = a.npad;
+  p.BH = pr.BH;
+  p.mask_kind = pr.mask_kind;
+  p.window = pr.window;
+  p.words_per_row = pr.words_per_row;
+  p.bits = pr.bitmask;
+  p.delta = a.delta;
+  p.lse2 = a.lse2;
+  p.sl2 = pr.scale * kLog2e;
+  p.scale = pr.scale;
+  p.dQ = static_cast<__nv_bfloat16*>(a.dQ);
+  p.dK = static_cast<__nv_bfloat16*>(a.dK);
+  p.dV = static_cast<__nv_bfloat16*>(a.dV);
+  p.status = a.status;
+  auto kv = tc_bwd_kv_kernel<D, D>;
+  auto qk = tc_bwd_q_kernel<D, D>;
+  cudaError_t e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       KvLayout<D, D>::TOTAL);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(qk, cudaFuncAttributeMaxDynamicSharedMemorySize, QLayout<D, D>::TOTAL);
+  if (e != cudaSuccess) {
+    record_error("tc_bwd2: cudaFuncSetAttribute", static_cast<int>(e), cudaGetErrorString(e));
+    return e;
+  }
+  const int nb = (pr.n + kBN - 1) / kBN;
+  before_launch(kKernBwd, s);
+  kv<<<dim3(nb, pr.BH), kThreads, KvLayout<D, D>::TOTAL, s>>>(p);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) {
+    before_launch(kKernBwdQ, s);
+    qk<<<dim3(nb, pr.BH), kThreads, QLayout<D, D>::TOTAL, s>>>(p);
+    e = cudaGetLastError();
+  }
+  after_launch(kKernBwd, s);
+  return e;
+}
+
+}  // namespace
+
+bool tc_bwd_split_supported(const Problem& p) {
+  if (p.dtype != kBF16 || p.d != p.v || (p.d != 64 && p.d != 128)) return false;
+  if (p.mask_kind == kMaskBitmask && p.n > kMaxBlocks * kBM) return false;
+  return tmap_encoder_available();
+}
+
+cudaError_t launch_tc_bwd_split(const BwdArgs& a, cudaStream_t s) {
+  return a.p.d == 128 ? launch_split<128>(a, s) : launch_split<64>(a, s);
+}
+
+}  // namespace exattn

@@ -93,11 +93,14 @@ typedef struct exattn_shape {
 } exattn_shape;
 
 /* Kernel path selection, process-wide (default EXATTN_PATH_AUTO).
- * AUTO uses the tcgen05/TMA/TMEM kernels where the shape allows (bf16, d and v
- * multiples of 16 up to 128) and the SIMT fp32 kernels otherwise; SIMT forces
- * the SIMT kernels for every shape.  Returns the previous setting, or -1 for
- * an unknown value (setting unchanged). */
-enum exattn_path { EXATTN_PATH_AUTO = 0, EXATTN_PATH_SIMT = 1 };
+ * AUTO uses the tcgen05/TMA/TMEM kernels where the shape allows (bf16 with
+ * d = v in {64, 128}) and the SIMT fp32 kernels otherwise; its reverse pass is
+ * a key-major dK/dV kernel plus a query-major dQ kernel.  SIMT forces the SIMT
+ * kernels for every shape.  ATOMIC_DQ is AUTO with the other reverse form on
+ * the tensor cores: one key-major kernel that adds dQ into an fp32 accumulator
+ * with vector reductions (kept for measurement).  Returns the previous
+ * setting, or -1 for an unknown value (setting unchanged). */
+enum exattn_path { EXATTN_PATH_AUTO = 0, EXATTN_PATH_SIMT = 1, EXATTN_PATH_ATOMIC_DQ = 2 };
 int exattn_set_path(int path);
 
 /* Workspace bytes that attn_fwd / attn_bwd need for this shape and mask kind.
@@ -158,8 +161,10 @@ int exattn_device_status(const void* workspace, void* cuda_stream);
 enum exattn_kernel {
   EXATTN_KERNEL_FWD = 0,        /* the forward kernel of attn_fwd */
   EXATTN_KERNEL_DELTA = 1,      /* delta_i = dY_i . Y_i in attn_bwd */
-  EXATTN_KERNEL_BWD = 2,        /* the key-block reverse kernel of attn_bwd */
-  EXATTN_KERNEL_DQ_CONVERT = 3  /* fp32 dQ accumulator -> dQ in attn_bwd */
+  EXATTN_KERNEL_BWD = 2,        /* the reverse kernel(s) of attn_bwd: start before the first,
+                                   stop after the last (dK/dV and dQ kernels on AUTO) */
+  EXATTN_KERNEL_DQ_CONVERT = 3, /* fp32 dQ accumulator -> dQ (SIMT and ATOMIC_DQ paths) */
+  EXATTN_KERNEL_BWD_Q = 4       /* the query-major dQ kernel alone (AUTO path) */
 };
 
 /* One-shot: on the next launch of kernel `which` (an exattn_kernel), record

@@ -139,7 +139,7 @@ def _small_inputs(case, seed):
     return w, workloads.make_inputs(w)
 
 
-@pytest.mark.parametrize("path", ["auto", "simt"])
+@pytest.mark.parametrize("path", ["auto", "simt", "atomic_dq"])
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: "-".join(map(str, c)))
 def test_small_parity(ex, case, path):
     w, x = _small_inputs(case, seed=1000 + SMALL.index(case))
