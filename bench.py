@@ -75,7 +75,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -280,6 +280,8 @@ def run_gpu(args, w):
         pairs = int(from_words)
     f_fwd, f_bwd = flops(w, pairs)
 
+    clocks = ClockSampler(dev.index)
+    clocks.__enter__()  # sampled from the warm-up through the end-to-end runs
     for _ in range(args.warmup):
         step()
     barrier()
@@ -296,15 +298,14 @@ def run_gpu(args, w):
     barrier()
     launches0 = ex.launch_count()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(dev.index) as clocks:
-        barrier()
-        start.record(stream)
-        for i in range(K):
-            for role in ev:
-                ex.record_kernel_events(role, *ev[role][i])
-            step()
-        stop.record(stream)
-        barrier()
+    barrier()
+    start.record(stream)
+    for i in range(K):
+        for role in ev:
+            ex.record_kernel_events(role, *ev[role][i])
+        step()
+    stop.record(stream)
+    barrier()
     launches = ex.launch_count() - launches0
     ms = max_over_ranks(start.elapsed_time(stop))
     kern_ms = {role: sum(a.elapsed_time(b) for a, b in ev[role]) / K for role in ev}
@@ -350,6 +351,7 @@ def run_gpu(args, w):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": ms_e2e / K}
 
+    clocks.__exit__(None, None, None)
     peaks, peak_kind = load_peaks()
     peak = float(peaks["bf16_tflops"])
     tflops = world * (f_fwd + f_bwd) * K / (ms * 1e-3) / 1e12
