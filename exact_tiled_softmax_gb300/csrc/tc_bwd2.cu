@@ -19,8 +19,8 @@
 //   K/V ring order V(0), K(0), V(1), K(1), ...
 //   TMEM: S [0,128), dP double buffer [128,256) and [256,384) (dS bf16 is
 //   written over its own dP), dQ [384, 384+D).  S(t+1) is issued as soon as
-//   the elementwise warps have read S(t); dP(t+1) into the other buffer even
-//   earlier.
+//   the elementwise warps hold S(t) in registers (before they compute dS(t));
+//   dP(t+1) goes into the other buffer even earlier.
 // Warp roles (both kernels, 18 warps): warps 0-15 elementwise, four groups of
 // 32 columns (group = warp / 4, TMEM lane quarter = warp % 4); warp 16 TMA;
 // warp 17 MMA.  The producer warps run warp-uniform loops and one elected
@@ -308,49 +308,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kStage16 = Lay::STAGE >> 4, kQ16 = Lay::QBYTES >> 4;
     bool ok = mbar_wait(bar(Lay::B_KV), 0, abort_flag);
     tc_fence_after();
+    // Per query block i and half h: A_h(i) = dP^T_h, S^T_h (N = 64) and
+    // B_h(i) = dV, dK updates from that half (K = 64).  Issue order
+    //   A0(0) A1(0) | B0(0) A0(1) B1(0) A1(1) | B0(1) A0(2) B1(1) A1(2) | ...
+    // so that each half's chain A -> elementwise -> B -> A' never waits on the
+    // other half, whose MMAs fill the tensor pipe meanwhile.
+    auto issue_a = [&](int h, int slot) {
+      const uint64_t q_k = dSt + slot * kStage16;
+      const uint64_t y_k = dSt + slot * kStage16 + kQ16;
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < V / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_ss(tB + 64 * h, dV0 + off, y_k + off + h * 512, kIdHalf, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_ss(tA + 64 * h, dK0 + off, q_k + off + h * 512, kIdHalf, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(Lay::B_SDP + h));
+      }
+    };
+    auto issue_b = [&](int h, int slot, bool first) {
+      const uint64_t q_m = dSm + slot * kStage16;
+      const uint64_t y_m = dSm + slot * kStage16 + kQ16;
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t acol = 64 * h + 32 * (kk >> 1) + 8 * (kk & 1);
+          const uint32_t rows16 = (64 * h + 16 * kk) * 128 >> 4;
+          const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
+          mma_ts(tdV, tA + acol, y_m + rows16, kIdDV, acc);
+          mma_ts(tdK, tB + acol, q_m + rows16, kIdDK, acc);
+        }
+      }
+    };
+    auto next_qb = [&](int qb) {
+      for (++qb; qb < qb_end; ++qb)
+        if (cls_of(qb) != kEmpty) return qb;
+      return qb_end;
+    };
+    int qb = next_qb(qb_begin - 1);
     int it = 0;
-    for (int qb = qb_begin; qb < qb_end && ok; ++qb) {
-      if (cls_of(qb) == kEmpty) continue;
-      const int slot = it % NST, phase = (it / NST) & 1;
-      if (!(ok = mbar_wait(bar(Lay::B_QF + slot), phase, abort_flag))) break;
-      tc_fence_after();
-      const uint64_t q_k = dSt + slot * kStage16;          // Q_i, K-major
-      const uint64_t y_k = dSt + slot * kStage16 + kQ16;   // dY_i, K-major
-      const uint64_t q_m = dSm + slot * kStage16;          // Q_i, MN-major
-      const uint64_t y_m = dSm + slot * kStage16 + kQ16;   // dY_i, MN-major
-      // Halves h: queries 64h..64h+63 (rows 64h of the stage tiles: +64*128 B).
-      for (int h = 0; h < 2; ++h) {
-        if (leader) {
-#pragma unroll
-          for (int kk = 0; kk < V / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-            mma_ss(tB + 64 * h, dV0 + off, y_k + off + h * 512, kIdHalf, kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-            mma_ss(tA + 64 * h, dK0 + off, q_k + off + h * 512, kIdHalf, kk > 0 ? 1u : 0u);
-          }
-          tc_commit(bar(Lay::B_SDP + h));
-        }
-      }
-      for (int h = 0; h < 2; ++h) {
-        if (!(ok = mbar_wait(bar(Lay::B_DS + h), it & 1, abort_flag))) break;
+    if (ok && qb < qb_end) {
+      if ((ok = mbar_wait(bar(Lay::B_QF + 0), 0, abort_flag))) {
         tc_fence_after();
-        if (leader) {
-          // dV += P^T[:, 64h..] dY_i[64h..], dK += dS^T[:, 64h..] Q_i[64h..]  (K = 64 queries)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acol = 64 * h + 32 * (kk >> 1) + 8 * (kk & 1);
-            const uint32_t rows16 = (64 * h + 16 * kk) * 128 >> 4;
-            const uint32_t acc = (it > 0 || h > 0 || kk > 0) ? 1u : 0u;
-            mma_ts(tdV, tA + acol, y_m + rows16, kIdDV, acc);
-            mma_ts(tdK, tB + acol, q_m + rows16, kIdDK, acc);
-          }
-        }
+        issue_a(0, 0);
+        issue_a(1, 0);
       }
-      if (!ok) break;
-      if (leader) tc_commit(bar(Lay::B_QE + slot));
+    }
+    while (ok && qb < qb_end) {
+      const int slot = it % NST;
+      const int qb_n = next_qb(qb);
+      const bool more = qb_n < qb_end;
+      const int slot_n = (it + 1) % NST, phase_n = ((it + 1) / NST) & 1;
+      if (!(ok = mbar_wait(bar(Lay::B_DS + 0), it & 1, abort_flag))) break;
+      tc_fence_after();
+      issue_b(0, slot, it == 0);
+      if (more) {
+        if (!(ok = mbar_wait(bar(Lay::B_QF + slot_n), phase_n, abort_flag))) break;
+        tc_fence_after();
+        issue_a(0, slot_n);
+      }
+      if (!(ok = mbar_wait(bar(Lay::B_DS + 1), it & 1, abort_flag))) break;
+      tc_fence_after();
+      issue_b(1, slot, false);
+      if (leader) tc_commit(bar(Lay::B_QE + slot));  // Q_i, dY_i no longer read
+      if (more) issue_a(1, slot_n);
+      qb = qb_n;
       ++it;
     }
     if (leader) tc_commit(bar(Lay::B_DONE));
@@ -401,14 +427,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      uint32_t sv[2][16], dpv[2][16];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tmem_ld16(tA + lane_off + cb + 16 * c, sv[c]);
+        tmem_ld16(tB + lane_off + cb + 16 * c, dpv[c]);
+      }
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        reg_fence(sv[c]);
+        reg_fence(dpv[c]);
+      }
 #pragma unroll
       for (int c = 0; c < 2; ++c) {  // two chunks of 16 queries
-        uint32_t s[16], dp[16];
-        tmem_ld16(tA + lane_off + cb + 16 * c, s);
-        tmem_ld16(tB + lane_off + cb + 16 * c, dp);
-        tmem_ld_wait();
-        reg_fence(s);
-        reg_fence(dp);
+        const uint32_t (&s)[16] = sv[c];
+        const uint32_t (&dp)[16] = dpv[c];
         uint32_t pk[8], dk[8];
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
@@ -502,8 +536,8 @@ struct QLayout {
   static constexpr int SLOT_OFF = Y_OFF + YBYTES;
   static constexpr int BAR_OFF = SLOT_OFF + NS * SLOT;
   static constexpr int B_Q = 0, B_KVF = 1, B_KVE = B_KVF + NS, B_SDP = B_KVE + NS,
-                       B_DS = B_SDP + 1, B_DONE = B_DS + 1, B_DRAIN = B_DONE + 1,
-                       NBAR = B_DRAIN + 1;
+                       B_DS = B_SDP + 1, B_SFREE = B_DS + 1, B_DONE = B_SFREE + 1,
+                       B_DRAIN = B_DONE + 1, NBAR = B_DRAIN + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int CLS_OFF = MISC_OFF + 16;
   static constexpr int TOTAL = CLS_OFF + 2 * (kMaxBlocks / 32) * 4;
@@ -548,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(Lay::B_SDP), 1);
     mbar_init(bar(Lay::B_DS), kEwWarps * 32);
+    mbar_init(bar(Lay::B_SFREE), kEwWarps * 32);
     mbar_init(bar(Lay::B_DONE), 1);
     mbar_init(bar(Lay::B_DRAIN), 1);
     misc[1] = 0;
@@ -688,8 +723,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(bar(Lay::B_KVE + vs1));
         }
-        // S(t+1) once the elementwise warps have read S(t) and written dS(t).
-        if (!(ok = mbar_wait(bar(Lay::B_DS), t & 1, abort_flag))) break;
+        // S(t+1) as soon as the elementwise warps hold S(t) in registers.
+        if (!(ok = mbar_wait(bar(Lay::B_SFREE), t & 1, abort_flag))) break;
         if (!(ok = mbar_wait(bar(Lay::B_KVF + ks1), kp1, abort_flag))) break;
         tc_fence_after();
         if (leader) {
@@ -700,10 +735,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(bar(Lay::B_SDP));
         }
-      } else {
-        if (!(ok = mbar_wait(bar(Lay::B_DS), t & 1, abort_flag))) break;
-        tc_fence_after();
       }
+      if (!(ok = mbar_wait(bar(Lay::B_DS), t & 1, abort_flag))) break;
+      tc_fence_after();
       // dQ += dS(t) K_t  (A = dS bf16 in TMEM over dP(t), keys packed; B = K_t MN-major)
       const uint32_t tD = tD0 + 128 * (t & 1);
       if (leader) {
@@ -756,14 +790,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const uint32_t tD = tD0 + 128 * (t & 1) + lane_off;
+      uint32_t sv[2][16], dpv[2][16];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        uint32_t s[16], dp[16];
-        tmem_ld16(tS + lane_off + 32 * g + 16 * c, s);
-        tmem_ld16(tD + 32 * g + 16 * c, dp);
-        tmem_ld_wait();
-        reg_fence(s);
-        reg_fence(dp);
+        tmem_ld16(tS + lane_off + 32 * g + 16 * c, sv[c]);
+        tmem_ld16(tD + 32 * g + 16 * c, dpv[c]);
+      }
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        reg_fence(sv[c]);
+        reg_fence(dpv[c]);
+      }
+      // S(t) is in registers: the MMA warp may overwrite it with S(t+1).
+      tc_fence_before();
+      mbar_arrive(bar(Lay::B_SFREE));
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t (&s)[16] = sv[c];
+        const uint32_t (&dp)[16] = dpv[c];
         uint32_t dk[8];
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {

@@ -80,7 +80,8 @@ struct Layout {
                        B_P = B_S + 2, B_O = B_P + 2, B_DRAIN = B_O + 2, NBAR = B_DRAIN + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;   // [0] tmem base, [1] abort flag
   static constexpr int CLS_OFF = (MISC_OFF + 16 + 15) / 16 * 16;
-  static constexpr int TOTAL = CLS_OFF + 2 * 2 * kMaxKT * 4;  // any[2][kMaxKT], all[2][kMaxKT]
+  // Bitmask tile table as bits: any[2][kMaxKT/32], notall[2][kMaxKT/32].
+  static constexpr int TOTAL = CLS_OFF + 2 * 2 * (kMaxKT / 32) * 4;
   static constexpr int ALLOC = TOTAL + 1024;
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(V == 64 || V == 128, "value dim");
@@ -104,7 +105,8 @@ struct TileRows {
 
 // Classification of key block kt for query tile rows [r0, r1]: EMPTY (skip
 // the block: J_t n A_i empty for every row), FULL (no masking needed) or
-// PARTIAL (mask element by element).
+// PARTIAL (mask element by element).  For the bitmask, `any` and `all` are the
+// bit tables built by the kernel (`all` holds the NOT-all bits).
 __device__ __forceinline__ int classify(const FwdParams& p, const TileRows& t, int X, int kt,
                                         const uint32_t* any, const uint32_t* all) {
   if (!t.valid) return kEmpty;
@@ -118,9 +120,11 @@ __device__ __forceinline__ int classify(const FwdParams& p, const TileRows& t, i
     case kMaskWindow:
       if (k0 > t.r1 || k1 <= t.r0 - p.window) return kEmpty;
       return (k0 + kBN - 1 <= t.r0 && k0 >= t.r1 - p.window + 1 && !tail) ? kFull : kPartial;
-    case kMaskBitmask:
-      if (!any[X * kMaxKT + kt]) return kEmpty;
-      return (all[X * kMaxKT + kt] && !tail) ? kFull : kPartial;
+    case kMaskBitmask: {
+      const int w = X * (kMaxKT / 32) + (kt >> 5);
+      if (!((any[w] >> (kt & 31)) & 1u)) return kEmpty;
+      return (((all[w] >> (kt & 31)) & 1u) || tail) ? kPartial : kFull;
+    }
     default:
       return tail ? kPartial : kFull;
   }
@@ -139,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   uint32_t* cls_any = reinterpret_cast<uint32_t*>(smem + Lay::CLS_OFF);
-  uint32_t* cls_all = cls_any + 2 * kMaxKT;
+  uint32_t* cls_all = cls_any + 2 * (kMaxKT / 32);  // bits set where NOT every pair is allowed
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qb = p.n_qblocks - 1 - blockIdx.x;  // heaviest (causal) query blocks first
@@ -183,12 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     tmem_relinquish();
     tc_fence_before();
   }
-  if (p.mask_kind == kMaskBitmask) {
-    for (int k = threadIdx.x; k < 2 * kMaxKT; k += kThreads) {
-      cls_any[k] = 0u;
-      cls_all[k] = 1u;
-    }
-  }
+  if (threadIdx.x < 4 * (kMaxKT / 32)) cls_any[threadIdx.x] = 0u;  // any and not-all bits
   __syncthreads();
   if (p.mask_kind == kMaskBitmask && threadIdx.x < 2 * kBM) {
     // Tile table: does any row of tile X allow a key of block kt, and do all
@@ -207,8 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           any |= word != 0u;
           all &= word == valid;
         }
-        if (any) atomicOr(&cls_any[X * kMaxKT + kt], 1u);
-        if (!all) atomicAnd(&cls_all[X * kMaxKT + kt], 0u);
+        const int w = X * (kMaxKT / 32) + (kt >> 5);
+        if (any) atomicOr(&cls_any[w], 1u << (kt & 31));
+        if (!all) atomicOr(&cls_all[w], 1u << (kt & 31));
       }
     }
   }
