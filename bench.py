@@ -44,6 +44,23 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(val, dist_mod=None, device=None):
+    """Largest value of a float over all ranks of the default process group
+    (the value itself without one).  Times are max-reduced: the job is as
+    slow as its slowest rank."""
+    if dist_mod is None or not dist_mod.is_available() or not dist_mod.is_initialized():
+        return float(val)
+    t = torch.tensor([float(val)], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step, steps, world, ms_max):
+    """Whole-job throughput: every rank processes its own batch (weak scaling),
+    timed by the slowest rank."""
+    return world * flops_per_rank_step * steps / (ms_max * 1e-3) / 1e12
+
+
 def flops(w: workloads.Workload, allowed_pairs=None):
     """(forward, reverse) flop counts of one step of workload ``w``."""
     heads = w.B * w.H
@@ -267,12 +284,8 @@ def run_gpu(args, w):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def max_over_ranks(val):
-        if dist is None:
-            return val
-        t = torch.tensor([val], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def rank_max(val):
+        return max_over_ranks(val, dist, dev)
 
     pairs = None
     if w.mask == "bitmask":
@@ -307,7 +320,7 @@ def run_gpu(args, w):
     stop.record(stream)
     barrier()
     launches = ex.launch_count() - launches0
-    ms = max_over_ranks(start.elapsed_time(stop))
+    ms = rank_max(start.elapsed_time(stop))
     kern_ms = {role: sum(a.elapsed_time(b) for a, b in ev[role]) / K for role in ev}
 
     # Forward alone.
@@ -320,7 +333,7 @@ def run_gpu(args, w):
         fwd_only()
     e2.record(stream)
     barrier()
-    ms_fwd = max_over_ranks(s2.elapsed_time(e2))
+    ms_fwd = rank_max(s2.elapsed_time(e2))
 
     # End to end through the public API: pinned host inputs in, results out.
     e2e = None
@@ -346,16 +359,16 @@ def run_gpu(args, w):
             e2e_step()
         e3.record(stream)
         barrier()
-        ms_e2e = max_over_ranks(s3.elapsed_time(e3))
-        e2e = {"value": world * (f_fwd + f_bwd) * K / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+        ms_e2e = rank_max(s3.elapsed_time(e3))
+        e2e = {"value": whole_job_tflops(f_fwd + f_bwd, K, world, ms_e2e), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": ms_e2e / K}
 
     clocks.__exit__(None, None, None)
     peaks, peak_kind = load_peaks()
     peak = float(peaks["bf16_tflops"])
-    tflops = world * (f_fwd + f_bwd) * K / (ms * 1e-3) / 1e12
-    tflops_fwd = world * f_fwd * K / (ms_fwd * 1e-3) / 1e12
+    tflops = whole_job_tflops(f_fwd + f_bwd, K, world, ms)
+    tflops_fwd = whole_job_tflops(f_fwd, K, world, ms_fwd)
     # Dominant kernel by measured time.
     dom = max(kern_ms, key=kern_ms.get)
     dom_flops = f_fwd if dom == ex.KERNEL_FWD else f_bwd

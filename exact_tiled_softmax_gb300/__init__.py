@@ -78,6 +78,8 @@ def load_library():
     lib.exattn_launch_count.restype = ctypes.c_ulonglong
     lib.attn_bwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, cf, ci, ci, vp, vp, vp, vp, vp]
     lib.attn_bwd_noalloc.restype = ci
+    lib.exattn_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint, vp]
+    lib.exattn_selftest_wait_timeout.restype = ci
     lib.exattn_last_error.argtypes = []
     lib.exattn_last_error.restype = ctypes.c_char_p
     _lib = lib

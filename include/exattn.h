@@ -177,6 +177,18 @@ int exattn_record_kernel_events(int which, void* start, void* stop);
  * (process-wide, all devices). */
 unsigned long long exattn_launch_count(void);
 
+/* Self-test of the failure path of the tensor-core kernels, whose every
+ * device-side wait is bounded.  Launches one small kernel whose wait on a
+ * barrier that nothing arrives on gives up after `limit_us` microseconds
+ * (1..100000); it records EXATTN_TIMEOUT in the status word of `workspace`
+ * (>= 256 bytes, 256-byte aligned) and returns, and a second waiter with the
+ * normal 1 s limit stops early on the kernel's abort flag.  Words 1..3 of the
+ * workspace receive: 1 if the first wait timed out, 1 if the second stopped on
+ * the abort flag, and the second waiter's time in microseconds.  Read the
+ * status with exattn_device_status (expected EXATTN_TIMEOUT).  No trap, fault
+ * or unbounded wait is involved. */
+int exattn_selftest_wait_timeout(void* workspace, unsigned limit_us, void* cuda_stream);
+
 /* Text of the last CUDA failure seen by a call on this host thread (which
  * step failed and the CUDA or driver error), or "" if none.  Valid until the
  * next call on this thread. */

@@ -312,3 +312,24 @@ def test_workload3_full_size_sampled_heads(ex):
 def test_workload4_full_size_sampled_head(ex, variant):
     w = workloads.workload(4, variant)
     _sampled_heads(ex, w, [w.B * w.H - 1])
+
+
+def test_bounded_wait_times_out_and_reports(ex):
+    """A device wait on a barrier nothing arrives on gives up after its limit,
+    records EXATTN_TIMEOUT and returns; the context stays usable."""
+    import ctypes
+    dev = torch.device("cuda:0")
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    lib = ex.load_library()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.exattn_selftest_wait_timeout(ctypes.c_void_p(ws.data_ptr()), 2000, stream) == 0
+    assert ex.device_status(ws) == 7
+    words = ws.view(torch.int32).cpu().tolist()
+    assert words[1] == 1 and words[2] == 1
+    assert words[3] < 500_000          # the second waiter stopped long before its 1 s limit
+    # The context is still usable: a normal call afterwards succeeds.
+    w = workloads.small(1, 1, 128, 64, 64, "bf16", "causal", 0.125)
+    x = workloads.make_inputs(w)
+    y, L = ex.fwd(x.Q.to(dev), x.K.to(dev), x.V.to(dev), w.scale, "causal")
+    torch.cuda.synchronize()
+    assert torch.isfinite(y.float()).all()
