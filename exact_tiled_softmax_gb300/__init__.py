@@ -17,6 +17,7 @@ import torch
 __all__ = ["fwd", "bwd", "fwd_workspace_size", "bwd_workspace_size", "device_status",
            "set_path", "library_path", "load_library", "ExattnError", "Shape",
            "record_kernel_events", "launch_count", "workspace", "bwd_noalloc",
+           "fwd_splitkv", "QKShape",
            "MASK_NONE", "MASK_CAUSAL", "MASK_WINDOW", "MASK_BITMASK"]
 
 MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_BITMASK = 0, 1, 2, 3
@@ -40,6 +41,12 @@ class ExattnError(RuntimeError):
         msg = lib.exattn_status_string(status).decode()
         detail = lib.exattn_last_error().decode()
         super().__init__(f"{where}: status {status} ({msg})" + (f": {detail}" if detail else ""))
+
+
+class QKShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("heads", ctypes.c_int), ("nq", ctypes.c_int),
+                ("nk", ctypes.c_int), ("d", ctypes.c_int), ("v", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
 
 
 class Shape(ctypes.Structure):
@@ -80,6 +87,11 @@ def load_library():
     lib.attn_bwd_noalloc.restype = ci
     lib.exattn_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint, vp]
     lib.exattn_selftest_wait_timeout.restype = ci
+    qp = ctypes.POINTER(QKShape)
+    lib.exattn_splitkv_workspace_size.argtypes = [qp, ci]
+    lib.exattn_splitkv_workspace_size.restype = sz
+    lib.attn_fwd_splitkv.argtypes = [qp, vp, vp, vp, cf, ci, ci, vp, ci, vp, vp, vp, sz, vp]
+    lib.attn_fwd_splitkv.restype = ci
     lib.exattn_last_error.argtypes = []
     lib.exattn_last_error.restype = ctypes.c_char_p
     _lib = lib
@@ -179,6 +191,32 @@ def bwd(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, dq=None, 
     if st != 0:
         raise ExattnError(st, "attn_bwd")
     return dq, dk, dv
+
+
+def fwd_splitkv(q, k, v, scale, mask="none", window=0, bitmask=None, num_splits=1, y=None,
+                L=None, ws=None, stream=None):
+    """Split-KV forward -> (Y, L) for q [B,H,nq,d] against k [B,H,nk,d], v [B,H,nk,v];
+    the queries are the last nq positions of the key sequence."""
+    lib = load_library()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("expected [batch, heads, n, width] tensors")
+    _check((k, v, y), q.dtype, q.device)
+    B, H, nq, d = q.shape
+    shape = QKShape(B, H, nq, k.shape[2], d, v.shape[-1], _DTYPES[q.dtype])
+    kind = _mask_kind(mask)
+    if y is None:
+        y = torch.empty((B, H, nq, v.shape[-1]), dtype=q.dtype, device=q.device)
+    if L is None:
+        L = torch.empty((B, H, nq), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(lib.exattn_splitkv_workspace_size(ctypes.byref(shape), int(num_splits)),
+                       q.device)
+    st = lib.attn_fwd_splitkv(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale), kind,
+                              int(window), _ptr(bitmask), int(num_splits), _ptr(y), _ptr(L),
+                              _ptr(ws), ws.numel(), _stream(stream))
+    if st != 0:
+        raise ExattnError(st, "attn_fwd_splitkv")
+    return y, L
 
 
 def bwd_noalloc(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, dq=None,

@@ -225,6 +225,85 @@ int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void
   return cuda_status(launch_dq_convert(a, s), "attn_bwd: dQ conversion launch");
 }
 
+namespace {
+
+int check_qk_shape(const exattn_qk_shape* s) {
+  if (!s) return EXATTN_INVALID_ARG;
+  if (s->batch < 1 || s->heads < 1 || s->nq < 1 || s->nk < 1 || s->d < 1 || s->v < 1)
+    return EXATTN_INVALID_ARG;
+  if (s->dtype != EXATTN_F32 && s->dtype != EXATTN_BF16) return EXATTN_INVALID_ARG;
+  if (s->nq > splitkv_max_queries() || s->d > kMaxWidth || s->v > kMaxWidth || s->nk > kMaxN)
+    return EXATTN_UNSUPPORTED;
+  if ((long long)s->batch * s->heads > 65535) return EXATTN_UNSUPPORTED;
+  // K and V rows are staged in 16-byte pieces.
+  const int per16 = s->dtype == EXATTN_BF16 ? 8 : 4;
+  if (s->d % per16 != 0 || s->v % per16 != 0) return EXATTN_UNSUPPORTED;
+  if (splitkv_smem_bytes(s->nq, s->d, s->v, s->dtype == EXATTN_BF16 ? 2 : 4) > 200 * 1024)
+    return EXATTN_UNSUPPORTED;
+  return EXATTN_OK;
+}
+
+// Keys per chunk (a multiple of 32) and the number of chunks actually used.
+void split_plan(int nk, int num_splits, int* chunk, int* splits) {
+  int c = (nk + num_splits - 1) / num_splits;
+  c = (c + 31) / 32 * 32;
+  *chunk = c;
+  *splits = (nk + c - 1) / c;
+}
+
+}  // namespace
+
+size_t exattn_splitkv_workspace_size(const exattn_qk_shape* shape, int num_splits) {
+  if (check_qk_shape(shape) != EXATTN_OK || num_splits < 1 || num_splits > 4096) return 0;
+  int chunk, splits;
+  split_plan(shape->nk, num_splits, &chunk, &splits);
+  const size_t rows = (size_t)shape->batch * shape->heads * splits * shape->nq;
+  return kStatusBytes + 2 * align_up(sizeof(float) * rows, 256) + sizeof(float) * rows * shape->v;
+}
+
+int attn_fwd_splitkv(const exattn_qk_shape* shape, const void* Q, const void* K, const void* V,
+                     float scale, int mask_kind, int window, const uint32_t* bitmask,
+                     int num_splits, void* Y, float* L, void* workspace, size_t workspace_bytes,
+                     void* cuda_stream) {
+  int st = check_qk_shape(shape);
+  if (st != EXATTN_OK) return st;
+  st = check_mask(mask_kind, window, bitmask);
+  if (st != EXATTN_OK) return st;
+  if (num_splits < 1 || num_splits > 4096) return EXATTN_INVALID_ARG;
+  if (!Q || !K || !V || !Y || !L || !workspace) return EXATTN_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Y) || !aligned16(L))
+    return EXATTN_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return EXATTN_MISALIGNED;
+  if (workspace_bytes < exattn_splitkv_workspace_size(shape, num_splits))
+    return EXATTN_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  exattn::g_last_error[0] = 0;
+  SplitArgs a;
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.BH = shape->batch * shape->heads;
+  a.nq = shape->nq;
+  a.nk = shape->nk;
+  a.d = shape->d;
+  a.v = shape->v;
+  a.mask_kind = mask_kind;
+  a.window = mask_kind == EXATTN_MASK_WINDOW ? window : 0;
+  a.words_per_row = (shape->nk + 31) / 32;
+  a.bits = mask_kind == EXATTN_MASK_BITMASK ? bitmask : nullptr;
+  a.sl2 = scale * 1.4426950408889634f;
+  split_plan(shape->nk, num_splits, &a.chunk, &a.splits);
+  const size_t rows = (size_t)a.BH * a.splits * a.nq;
+  char* ws = static_cast<char*>(workspace);
+  a.pm = reinterpret_cast<float*>(ws + kStatusBytes);
+  a.pl = reinterpret_cast<float*>(ws + kStatusBytes + align_up(sizeof(float) * rows, 256));
+  a.pz = reinterpret_cast<float*>(ws + kStatusBytes + 2 * align_up(sizeof(float) * rows, 256));
+  cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes, s);
+  if (e != cudaSuccess) return cuda_status(e, "attn_fwd_splitkv: clearing the status word");
+  return cuda_status(launch_splitkv(a, shape->dtype, Y, L, static_cast<unsigned*>(workspace), s),
+                     "attn_fwd_splitkv: launch");
+}
+
 int exattn_device_status(const void* workspace, void* cuda_stream) {
   if (!workspace) return EXATTN_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);

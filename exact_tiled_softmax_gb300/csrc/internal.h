@@ -55,7 +55,9 @@ enum KernelRole {
   kKernBwd = 2,
   kKernDqConvert = 3,
   kKernBwdQ = 4,
-  kKernRoles = 5
+  kKernSplitPartial = 5,
+  kKernSplitMerge = 6,
+  kKernRoles = 7
 };
 void before_launch(int role, cudaStream_t s);
 // Remember the last failing step of this host thread (exattn_last_error).
@@ -82,5 +84,22 @@ bool tc_fwd_supported(const Problem& p);
 cudaError_t launch_tc_fwd(const FwdArgs& a, cudaStream_t s);
 bool tc_bwd_supported(const Problem& p);
 cudaError_t launch_tc_bwd(const BwdArgs& a, cudaStream_t s);
+
+// Split-KV forward (nq queries aligned to the end of nk keys).
+struct SplitArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  int BH, nq, nk, d, v, mask_kind, window, words_per_row, splits, chunk;
+  const uint32_t* bits;  // [nq][ceil(nk/32)]
+  float sl2;             // scale * log2(e)
+  float* pm;             // [BH][splits][nq] running max (exp2 domain)
+  float* pl;             // [BH][splits][nq] running sum
+  float* pz;             // [BH][splits][nq][v] unnormalised output
+};
+size_t splitkv_smem_bytes(int nq, int d, int v, int elem_bytes);
+int splitkv_max_queries();
+cudaError_t launch_splitkv(const SplitArgs& a, int dtype, void* Y, float* L, unsigned* status,
+                           cudaStream_t s);
 
 }  // namespace exattn

@@ -152,6 +152,47 @@ int attn_bwd_noalloc(const exattn_shape* shape, const void* Q, const void* K, co
                      int window, const uint32_t* bitmask, void* dQ, void* dK, void* dV,
                      void* cuda_stream);
 
+/* ---------------------------------------------------------------------------
+ * Split-KV forward: a few queries against a long key sequence (a decode step).
+ *
+ * The Forward procedure of "Exact tiled softmax attention with block-
+ * recomputed vector-Jacobian products" keeps a per-row summary of the key
+ * blocks seen and merges it with each new block's summary (the star merge).
+ * attn_fwd_splitkv cuts the keys into `num_splits` contiguous chunks handled
+ * in parallel, writes every chunk's summary (running max, running sum,
+ * unnormalised output) per query row to the workspace, and a second kernel
+ * merges the summaries of all chunks, skipping empty ones, into Y and L.  The
+ * result is the same attention for every num_splits (up to rounding).
+ *
+ * Shapes: Q [B][H][nq][d], K [B][H][nk][d], V [B][H][nk][v], Y [B][H][nq][v]
+ * (dtype), L fp32 [B][H][nq] (natural log).  Query i sits at absolute position
+ * i + nk - nq (the queries are the last nq positions): CAUSAL allows
+ * j <= i + nk - nq, WINDOW w the w keys ending there, BITMASK reads bit rows
+ * [nq][ceil(nk/32)].  Limits: 1 <= nq <= 64, nk >= 1, d, v <= 256 and rows of
+ * whole 16-byte pieces (d, v multiples of 8 for bf16, of 4 for fp32),
+ * 1 <= num_splits <= 4096 (chunks are whole multiples of 32 keys, so fewer
+ * chunks may be used than asked for).  Rows with an empty
+ * allowed set get Y_i = 0, L_i = -inf and the EXATTN_EMPTY_ROW status.
+ * Ownership, streams and errors as for attn_fwd.
+ * ------------------------------------------------------------------------- */
+typedef struct exattn_qk_shape {
+  int batch;
+  int heads;
+  int nq;
+  int nk;
+  int d;
+  int v;
+  int dtype;
+} exattn_qk_shape;
+
+/* Workspace bytes of attn_fwd_splitkv (status word + summaries); 0 if invalid. */
+size_t exattn_splitkv_workspace_size(const exattn_qk_shape* shape, int num_splits);
+
+int attn_fwd_splitkv(const exattn_qk_shape* shape, const void* Q, const void* K, const void* V,
+                     float scale, int mask_kind, int window, const uint32_t* bitmask,
+                     int num_splits, void* Y, float* L, void* workspace, size_t workspace_bytes,
+                     void* cuda_stream);
+
 /* Waits for `cuda_stream`, then reads the status word of `workspace` (the
  * workspace of the last call queued on it).  Returns EXATTN_OK,
  * EXATTN_EMPTY_ROW, EXATTN_TIMEOUT or EXATTN_CUDA_ERROR. */
@@ -164,7 +205,9 @@ enum exattn_kernel {
   EXATTN_KERNEL_BWD = 2,        /* the reverse kernel(s) of attn_bwd: start before the first,
                                    stop after the last (dK/dV and dQ kernels on AUTO) */
   EXATTN_KERNEL_DQ_CONVERT = 3, /* fp32 dQ accumulator -> dQ (SIMT and ATOMIC_DQ paths) */
-  EXATTN_KERNEL_BWD_Q = 4       /* the query-major dQ kernel alone (AUTO path) */
+  EXATTN_KERNEL_BWD_Q = 4,      /* the query-major dQ kernel alone (AUTO path) */
+  EXATTN_KERNEL_SPLIT_PARTIAL = 5, /* per-chunk summaries of attn_fwd_splitkv */
+  EXATTN_KERNEL_SPLIT_MERGE = 6    /* the merge kernel of attn_fwd_splitkv */
 };
 
 /* One-shot: on the next launch of kernel `which` (an exattn_kernel), record

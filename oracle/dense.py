@@ -136,3 +136,23 @@ def row_forward(Q, K, V, c, allowed_row, i):
     e = np.exp(s - m)
     l = e.sum()
     return (e @ V) / l, m + np.log(l)
+
+
+def forward_rect(Q, K, V, c, mask_kind, window=0, bitmask=None):
+    """Forward for nq queries against nk keys ([B,H,nq,d], [B,H,nk,d], [B,H,nk,v]),
+    queries aligned to the end of the keys (masks.allowed_matrix_rect).
+    Rows whose allowed set is empty get Y_i = 0 and L_i = -inf (the library's
+    convention for inputs outside the method's domain)."""
+    from .masks import allowed_matrix_rect
+    nq, nk = Q.shape[-2], K.shape[-2]
+    allowed = allowed_matrix_rect(nq, nk, mask_kind, window, bitmask)
+    q, k, vv = _heads(Q), _heads(K), _heads(V)
+    Y = np.zeros((q.shape[0], nq, vv.shape[-1]))
+    L = np.full((q.shape[0], nq), -np.inf)
+    rows = allowed.any(axis=1)
+    for h in range(q.shape[0]):
+        if rows.any():
+            y, l = head_forward(q[h][rows], k[h], vv[h], c, allowed[rows])
+            Y[h][rows] = y
+            L[h][rows] = l
+    return Y.reshape(V.shape[:-2] + (nq, V.shape[-1])), L.reshape(Q.shape[:-1])

@@ -454,3 +454,65 @@ def test_unfaulted_copy_passes():
 @pytest.mark.parametrize("fault", FAULTS)
 def test_planted_mistakes_are_caught(fault):
     assert pin_failures(*_mutant(fault)), f"no pin caught {fault}"
+
+
+# --------------------------------------------------------------------------- #
+# Queries aligned to the end of a longer key sequence (decode / split-KV)
+# --------------------------------------------------------------------------- #
+
+def test_rect_mask_reading_reduces_to_square_and_to_last_rows():
+    n = 70
+    r = _rng(12)
+    a = r.random((n, n)) < 0.3
+    np.fill_diagonal(a, True)
+    for kind, kw in ((masks.NONE, {}), (masks.CAUSAL, {}), (masks.WINDOW, dict(window=9)),
+                     (masks.BITMASK, dict(bitmask=pack_bitmask(a)))):
+        sq = masks.allowed_matrix(n, kind, **kw)
+        assert np.array_equal(masks.allowed_matrix_rect(n, n, kind, **kw), sq)
+        # The last nq rows of the square problem are the nq-query problem
+        # (bit rows restricted to those queries).
+        nq = 5
+        if kind == masks.BITMASK:
+            kw = dict(bitmask=pack_bitmask(a[-nq:]))
+        assert np.array_equal(masks.allowed_matrix_rect(nq, n, kind, **kw), sq[-nq:])
+    # Plain membership check of the causal decode reading.
+    got = masks.allowed_matrix_rect(3, 10, masks.CAUSAL)
+    for i in range(3):
+        assert set(np.nonzero(got[i])[0]) == set(range(0, 10 - 3 + i + 1))
+
+
+def test_rect_forward_equals_last_rows_of_square_forward():
+    r = _rng(13)
+    B, H, n, d, v, nq = 1, 2, 50, 6, 5, 7
+    Q, K, V = r.normal(size=(B, H, n, d)), r.normal(size=(B, H, n, d)), r.normal(size=(B, H, n, v))
+    for kind in (masks.NONE, masks.CAUSAL, masks.WINDOW):
+        Y, L = dense.forward(Q, K, V, 0.4, kind, 8)
+        Yr, Lr = dense.forward_rect(Q[:, :, -nq:], K, V, 0.4, kind, 8)
+        assert _rel(Yr, Y[:, :, -nq:]) <= 1e-15 and _rel(Lr, L[:, :, -nq:]) <= 1e-15
+
+
+def test_split_merge_is_exact_for_every_split():
+    """Summaries of disjoint key chunks merged with the star rule give the
+    dense result, whatever the chunks (the split-KV reading of the Forward
+    procedure)."""
+    r = _rng(14)
+    nq, nk, d, v, c = 4, 45, 5, 3, 0.6
+    Q, K, V = r.normal(size=(nq, d)), r.normal(size=(nk, d)), r.normal(size=(nk, v))
+    allowed = masks.allowed_matrix_rect(nq, nk, masks.CAUSAL)
+    Y, L = dense.head_forward(Q, K, V, c, allowed)
+    for splits in (1, 2, 3, 7, 45):
+        bounds = np.linspace(0, nk, splits + 1).astype(int)
+        m = np.full(nq, -np.inf)
+        l = np.zeros(nq)
+        z = np.zeros((nq, v))
+        for a0, a1 in zip(bounds[:-1], bounds[1:]):
+            s = c * Q @ K[a0:a1].T
+            bm, bl, bz = tiled.block_summary(s, allowed[:, a0:a1], V[a0:a1])
+            ne = allowed[:, a0:a1].any(axis=1)
+            first = ne & ~np.isfinite(m)
+            both = ne & np.isfinite(m)
+            m[first], l[first], z[first] = bm[first], bl[first], bz[first]
+            if both.any():
+                mm, ml, mz = tiled.merge(m[both], l[both], z[both], bm[both], bl[both], bz[both])
+                m[both], l[both], z[both] = mm, ml, mz
+        assert _rel(z / l[:, None], Y) <= 1e-12 and _rel(m + np.log(l), L) <= 1e-12

@@ -112,12 +112,13 @@ def workload(k: int, variant: str = "") -> Workload:
 
 
 def pack_bitmask(allowed: np.ndarray) -> np.ndarray:
-    """Pack a boolean [n, n] allowed matrix into uint32 bit rows [n, ceil(n/32)]."""
-    n = allowed.shape[0]
-    W = (n + 31) // 32
-    padded = np.zeros((n, W * 32), dtype=bool)
-    padded[:, :n] = allowed
-    bits = padded.reshape(n, W, 32).astype(np.uint64)
+    """Pack a boolean [rows, cols] allowed matrix into uint32 bit rows
+    [rows, ceil(cols/32)] (bit j % 32 of word j // 32 is key j)."""
+    rows, cols = allowed.shape
+    W = (cols + 31) // 32
+    padded = np.zeros((rows, W * 32), dtype=bool)
+    padded[:, :cols] = allowed
+    bits = padded.reshape(rows, W, 32).astype(np.uint64)
     weights = (np.uint64(1) << np.arange(32, dtype=np.uint64))
     return (bits * weights).sum(axis=2).astype(np.uint32)
 
@@ -165,6 +166,24 @@ def make_inputs(w: Workload, heads: int | None = None) -> Inputs:
         np.fill_diagonal(allowed, True)
         bitmask = pack_bitmask(allowed)
     return Inputs(Q, K, V, dY, bitmask)
+
+
+def make_decode_inputs(B, H, nq, nk, d, v, dtype, mask="none", seed=1, p_allow=0.3):
+    """Q [B,H,nq,d], K [B,H,nk,d], V [B,H,nk,v] (N(0,1), drawn in that order) for
+    nq queries at the end of an nk-key sequence, plus bit rows [nq][ceil(nk/32)]
+    for the bitmask (each key allowed with p_allow, the query's own position
+    always allowed)."""
+    g = torch.Generator().manual_seed(seed)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    Q = torch.randn(B, H, nq, d, generator=g).to(tdt)
+    K = torch.randn(B, H, nk, d, generator=g).to(tdt)
+    V = torch.randn(B, H, nk, v, generator=g).to(tdt)
+    bitmask = None
+    if mask == "bitmask":
+        allowed = (torch.rand(nq, nk, generator=g) < p_allow).numpy()
+        allowed[np.arange(nq), nk - nq + np.arange(nq)] = True
+        bitmask = pack_bitmask(allowed)
+    return Q, K, V, bitmask
 
 
 def random_bitmask(n: int, p_allow: float, seed: int, diagonal: bool = True) -> np.ndarray:
