@@ -12,6 +12,11 @@ masks the algorithmic 2 |A| (d+v) is used instead (|A| = allowed pairs).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the float64 CPU
 oracle instead, on a bounded sample of the same workload.
+
+``--decode`` times the split-KV forward instead: nq (default 1) queries at the
+end of nk=16384 keys, B=8, H=32, d=v=128, bf16, causal; the metric is the
+algorithmic HBM bytes (read Q, K, V, write Y, L) per second against the
+measured copy bandwidth.
 """
 from __future__ import annotations
 
@@ -409,6 +414,189 @@ def run_gpu(args, w):
         dist.destroy_process_group()
 
 
+# --------------------------------------------------------------------------- #
+# Decode mode: the split-KV forward (a few queries against a long key sequence)
+# --------------------------------------------------------------------------- #
+
+DECODE_METRIC = ("decode attention HBM GB/s (split-KV forward + star merge) at 1 GB300; "
+                 "% of measured copy bandwidth")
+
+
+def decode_inputs(w, heads=None):
+    B, H = (w.B, w.H) if heads is None else (1, heads)
+    return workloads.make_decode_inputs(B, H, w.nq, w.nk, w.d, w.v, w.dtype, w.mask,
+                                        seed=w.seed)
+
+
+def oracle_decode_sample(w, Q, K, V):
+    """Oracle forward of every query of one (batch, head) slice; returns the
+    algorithmic bytes of that slice (same convention as the GPU metric)."""
+    from oracle import dense
+    dense.forward_rect(Q, K, V, w.scale, workloads.MASK_KINDS[w.mask], w.window)
+    return w.bytes_moved() / (w.B * w.H)
+
+
+def decode_cpu_run(w, steps=None, budget_s=12.0, warmup=0):
+    """Oracle over single slices (drawn once, float64): a bounded sample."""
+    Q, K, V, _ = decode_inputs(w, heads=1)
+    Q, K, V = (t.to(torch.float64).numpy() for t in (Q, K, V))
+    for _ in range(warmup):
+        oracle_decode_sample(w, Q, K, V)
+    t0, done, n = time.perf_counter(), 0.0, 0
+    while True:
+        done += oracle_decode_sample(w, Q, K, V)
+        n += 1
+        el = time.perf_counter() - t0
+        if (steps is not None and n >= steps) or (steps is None and el >= budget_s):
+            break
+    return done / el / 1e9, n, el
+
+
+def run_reference_decode(args, w):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    value, n, el = decode_cpu_run(w, steps=args.steps, warmup=args.warmup)
+    sample = f"{n} x (all {w.nq} queries of one batch*head slice, nk={w.nk}, float64 NumPy)"
+    line = {
+        "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / n * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "step": "oracle forward of one batch*head slice"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": host_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu_decode(args, w):
+    import exact_tiled_softmax_gb300 as ex
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    Qh, Kh, Vh, _ = decode_inputs(w)
+    q, k, v = (t.to(dev) for t in (Qh, Kh, Vh))
+    stream = torch.cuda.current_stream(dev)
+    y = torch.empty((w.B, w.H, w.nq, w.v), dtype=q.dtype, device=dev)
+    L = torch.empty((w.B, w.H, w.nq), dtype=torch.float32, device=dev)
+    shape = ex.QKShape(w.B, w.H, w.nq, w.nk, w.d, w.v, 0 if w.dtype == "f32" else 1)
+    ws = ex.workspace(ex.load_library().exattn_splitkv_workspace_size(
+        __import__("ctypes").byref(shape), args.splits), dev)
+
+    def step():
+        ex.fwd_splitkv(q, k, v, w.scale, w.mask, w.window, None, num_splits=args.splits, y=y,
+                       L=L, ws=ws, stream=stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(dev.index)
+    clocks.__enter__()
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    K = args.steps
+    roles = (ex.KERNEL_SPLIT_PARTIAL, ex.KERNEL_SPLIT_MERGE)
+    ev = {r: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)] for r in roles}
+    for pairs_ in ev.values():
+        for a, b in pairs_:
+            a.record(stream)
+            b.record(stream)
+    barrier()
+    launches0 = ex.launch_count()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(K):
+        for r in roles:
+            ex.record_kernel_events(r, *ev[r][i])
+        step()
+    stop.record(stream)
+    barrier()
+    launches = ex.launch_count() - launches0
+    ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
+    kern_ms = {r: sum(a.elapsed_time(b) for a, b in ev[r]) / K for r in roles}
+    total_bytes = w.bytes_moved()
+    value = total_bytes * world * K / (ms * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        pin = [t.pin_memory() for t in (Qh, Kh, Vh)]
+        outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (y, L)]
+        h2d = sum(t.numel() * t.element_size() for t in pin)
+        d2h = sum(t.numel() * t.element_size() for t in outs)
+
+        def e2e_step():
+            for dst, src in zip((q, k, v), pin):
+                dst.copy_(src, non_blocking=True)
+            step()
+            for dst, src in zip(outs, (y, L)):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        barrier()
+        s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s3.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e3.record(stream)
+        barrier()
+        ms_e2e = max_over_ranks(s3.elapsed_time(e3), dist, dev)
+        e2e = {"value": total_bytes * world * K / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e / K}
+    clocks.__exit__(None, None, None)
+
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks["hbm_gbs"])
+    e = 4 if w.dtype == "f32" else 2
+    partial_bytes = w.B * w.H * (w.nq * w.d * e + w.nk * (w.d + w.v) * e)
+    achieved = partial_bytes / (kern_ms[ex.KERNEL_SPLIT_PARTIAL] * 1e-3) / 1e9
+    kind = "reg" if w.nq <= 4 else "smem"
+    roofline = {"kernel": f"splitkv_partial_{kind}", "bound": "hbm", "achieved": achieved,
+                "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_kind": f"copy bandwidth, of {peak_kind}",
+                "traffic": read_traffic(f"splitkv_partial_{kind}"),
+                "kernel_ms": {"partial": kern_ms[ex.KERNEL_SPLIT_PARTIAL],
+                              "merge": kern_ms[ex.KERNEL_SPLIT_MERGE]}}
+    line = {
+        "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "nq": w.nq, "nk": w.nk, "d": w.d,
+                   "v": w.v, "mask": w.mask, "num_splits": args.splits,
+                   "bytes_per_step": total_bytes,
+                   "l2": "inputs larger than L2 (%d MB of K and V vs 129 MB), no flush"
+                         % ((k.numel() * k.element_size() + v.numel() * v.element_size()) >> 20)},
+        "frac_of_hbm": value / peak,
+        "gpu_launches": launches,
+        "roofline": roofline,
+        "e2e": e2e,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu:
+        cv, n, el = decode_cpu_run(w, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": cv, "unit": "GB/s", "cores": host_cores(),
+                                "kind": "oracle",
+                                "sample": f"{n} x (all {w.nq} queries of one batch*head slice, "
+                                          f"nk={w.nk}, float64 NumPy), {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -425,9 +613,23 @@ def main():
     ap.add_argument("--batch", type=int, default=None,
                     help="override the batch size (a smaller case of the same workload)")
     ap.add_argument("--heads", type=int, default=None, help="override the head count")
+    ap.add_argument("--decode", action="store_true",
+                    help="time the split-KV decode forward instead (B=8, H=32, nk=16384)")
+    ap.add_argument("--nq", type=int, default=1, help="queries per slice in --decode mode")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="key chunks in --decode mode (0: the library chooses)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.decode:
+        dw = workloads.decode_workload(args.nq)
+        if args.batch is not None or args.heads is not None:
+            import dataclasses
+            B = args.batch if args.batch is not None else dw.B
+            H = args.heads if args.heads is not None else dw.H
+            dw = dataclasses.replace(dw, B=B, H=H, name=f"{dw.name}-as-b{B}h{H}")
+        (run_reference_decode if args.impl == "reference" else run_gpu_decode)(args, dw)
+        return
     w = workloads.workload(args.workload, args.variant)
     if args.batch is not None or args.heads is not None:
         import dataclasses

@@ -193,10 +193,11 @@ def bwd(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, dq=None, 
     return dq, dk, dv
 
 
-def fwd_splitkv(q, k, v, scale, mask="none", window=0, bitmask=None, num_splits=1, y=None,
+def fwd_splitkv(q, k, v, scale, mask="none", window=0, bitmask=None, num_splits=0, y=None,
                 L=None, ws=None, stream=None):
     """Split-KV forward -> (Y, L) for q [B,H,nq,d] against k [B,H,nk,d], v [B,H,nk,v];
-    the queries are the last nq positions of the key sequence."""
+    the queries are the last nq positions of the key sequence.  ``num_splits``
+    0 lets the library choose the number of key chunks."""
     lib = load_library()
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("expected [batch, heads, n, width] tensors")
@@ -238,11 +239,12 @@ def bwd_noalloc(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, d
 
 
 KERNEL_FWD, KERNEL_DELTA, KERNEL_BWD, KERNEL_DQ_CONVERT, KERNEL_BWD_Q = 0, 1, 2, 3, 4
+KERNEL_SPLIT_PARTIAL, KERNEL_SPLIT_MERGE = 5, 6
 
 
 def record_kernel_events(which: int, start, stop) -> None:
     """One-shot: record torch.cuda.Event ``start``/``stop`` around the next launch
-    of kernel ``which`` (KERNEL_FWD, KERNEL_DELTA, KERNEL_BWD, KERNEL_DQ_CONVERT)."""
+    of kernel ``which`` (one of the KERNEL_* roles)."""
     for e in (start, stop):
         if e.cuda_event == 0:
             raise ValueError("events must be created (record or query them once) first")

@@ -243,6 +243,21 @@ int check_qk_shape(const exattn_qk_shape* s) {
   return EXATTN_OK;
 }
 
+// num_splits == 0: enough chunks for about 32 CTAs per SM of the 152-SM part
+// (8 waves of the decode kernel's 4 resident CTAs per SM, so the last wave is
+// a small part of the run) over all batch*head slices, with at least 256 keys
+// per chunk.
+constexpr int kAutoSplitCtas = 32 * 152;
+constexpr int kAutoMinChunk = 256;
+
+int resolve_splits(const exattn_qk_shape* s, int num_splits) {
+  if (num_splits != 0) return num_splits;
+  const int bh = s->batch * s->heads;
+  const int want = (kAutoSplitCtas + bh - 1) / bh;
+  const int most = (s->nk + kAutoMinChunk - 1) / kAutoMinChunk;
+  return want < 1 ? 1 : (want > most ? most : want);
+}
+
 // Keys per chunk (a multiple of 32) and the number of chunks actually used.
 void split_plan(int nk, int num_splits, int* chunk, int* splits) {
   int c = (nk + num_splits - 1) / num_splits;
@@ -254,7 +269,8 @@ void split_plan(int nk, int num_splits, int* chunk, int* splits) {
 }  // namespace
 
 size_t exattn_splitkv_workspace_size(const exattn_qk_shape* shape, int num_splits) {
-  if (check_qk_shape(shape) != EXATTN_OK || num_splits < 1 || num_splits > 4096) return 0;
+  if (check_qk_shape(shape) != EXATTN_OK || num_splits < 0 || num_splits > 4096) return 0;
+  num_splits = resolve_splits(shape, num_splits);
   int chunk, splits;
   split_plan(shape->nk, num_splits, &chunk, &splits);
   const size_t rows = (size_t)shape->batch * shape->heads * splits * shape->nq;
@@ -269,7 +285,7 @@ int attn_fwd_splitkv(const exattn_qk_shape* shape, const void* Q, const void* K,
   if (st != EXATTN_OK) return st;
   st = check_mask(mask_kind, window, bitmask);
   if (st != EXATTN_OK) return st;
-  if (num_splits < 1 || num_splits > 4096) return EXATTN_INVALID_ARG;
+  if (num_splits < 0 || num_splits > 4096) return EXATTN_INVALID_ARG;
   if (!Q || !K || !V || !Y || !L || !workspace) return EXATTN_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Y) || !aligned16(L))
     return EXATTN_MISALIGNED;
@@ -292,7 +308,7 @@ int attn_fwd_splitkv(const exattn_qk_shape* shape, const void* Q, const void* K,
   a.words_per_row = (shape->nk + 31) / 32;
   a.bits = mask_kind == EXATTN_MASK_BITMASK ? bitmask : nullptr;
   a.sl2 = scale * 1.4426950408889634f;
-  split_plan(shape->nk, num_splits, &a.chunk, &a.splits);
+  split_plan(shape->nk, resolve_splits(shape, num_splits), &a.chunk, &a.splits);
   const size_t rows = (size_t)a.BH * a.splits * a.nq;
   char* ws = static_cast<char*>(workspace);
   a.pm = reinterpret_cast<float*>(ws + kStatusBytes);

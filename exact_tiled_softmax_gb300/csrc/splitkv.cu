@@ -58,6 +58,14 @@ __device__ __forceinline__ void stage_tile(uint8_t* dst, int ld_bytes, const T* 
   }
 }
 
+// 2^x with one MUFU operation (ex2.approx.ftz: relative error about 2^-22,
+// 2^-inf = +0, which the empty-summary handling relies on).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <typename T>
 __device__ __forceinline__ float to_f(T x) {
   return Elem<T>::cvt(x);
@@ -330,13 +338,13 @@ __global__ void __launch_bounds__(32 * kRegWarps) splitkv_reg_kernel(SplitArgs a
       // A group that has seen no allowed key keeps its empty state (ref = 0
       // makes every factor exp2(-inf) = 0 without producing NaN).
       const float ref = mx == -INFINITY ? 0.f : mx;
-      const float alpha = exp2f(m[q] - ref);
+      const float alpha = fast_exp2(m[q] - ref);
       float psum = 0.f;
 #pragma unroll
       for (int e = 0; e < W; ++e) z[q][e] *= alpha;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const float p = exp2f(s[u] - ref);
+        const float p = fast_exp2(s[u] - ref);
         psum += p;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
@@ -358,7 +366,7 @@ __global__ void __launch_bounds__(32 * kRegWarps) splitkv_reg_kernel(SplitArgs a
     float M = m[q];
 #pragma unroll
     for (int o = G; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-    const float f = M == -INFINITY ? 0.f : exp2f(m[q] - M);
+    const float f = M == -INFINITY ? 0.f : fast_exp2(m[q] - M);
     float lq = l[q] * f;
 #pragma unroll
     for (int o = G; o < 32; o <<= 1) lq += __shfl_xor_sync(0xFFFFFFFFu, lq, o);
@@ -394,7 +402,7 @@ __global__ void __launch_bounds__(32 * kRegWarps) splitkv_reg_kernel(SplitArgs a
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kRegWarps; ++w) {
-        const float f = exp2f(red_m[w][q] - M);
+        const float f = fast_exp2(red_m[w][q] - M);
         zc = fmaf(f, red_z[w][q][col], zc);
         lq = fmaf(f, red_l[w][q], lq);
       }
@@ -456,7 +464,7 @@ __global__ void __launch_bounds__(256) splitkv_merge_kernel(SplitArgs a, T* Y, f
   for (int s = 0; s < a.splits; ++s) {
     const size_t r = base + static_cast<size_t>(s) * a.nq;
     const float ms = a.pm[r];
-    if (ms != -INFINITY) lsum += exp2f(ms - M) * a.pl[r];
+    if (ms != -INFINITY) lsum += fast_exp2(ms - M) * a.pl[r];
   }
   const float inv = 1.f / lsum;
   for (int c = lane; c < a.v; c += 32) {
@@ -464,7 +472,7 @@ __global__ void __launch_bounds__(256) splitkv_merge_kernel(SplitArgs a, T* Y, f
     for (int s = 0; s < a.splits; ++s) {
       const size_t r = base + static_cast<size_t>(s) * a.nq;
       const float ms = a.pm[r];
-      if (ms != -INFINITY) z = fmaf(exp2f(ms - M), a.pz[r * a.v + c], z);
+      if (ms != -INFINITY) z = fmaf(fast_exp2(ms - M), a.pz[r * a.v + c], z);
     }
     Elem<T>::store(yrow + c, z * inv);
   }

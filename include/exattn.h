@@ -170,8 +170,10 @@ int attn_bwd_noalloc(const exattn_shape* shape, const void* Q, const void* K, co
  * j <= i + nk - nq, WINDOW w the w keys ending there, BITMASK reads bit rows
  * [nq][ceil(nk/32)].  Limits: 1 <= nq <= 64, nk >= 1, d, v <= 256 and rows of
  * whole 16-byte pieces (d, v multiples of 8 for bf16, of 4 for fp32),
- * 1 <= num_splits <= 4096 (chunks are whole multiples of 32 keys, so fewer
- * chunks may be used than asked for).  Rows with an empty
+ * 0 <= num_splits <= 4096 (chunks are whole multiples of 32 keys, so fewer
+ * chunks may be used than asked for; 0 picks enough chunks for about 4864
+ * CTAs over all batch*head slices, at least 256 keys each, from the shape
+ * alone, so the workspace query and the call agree).  Rows with an empty
  * allowed set get Y_i = 0, L_i = -inf and the EXATTN_EMPTY_ROW status.
  * Ownership, streams and errors as for attn_fwd.
  * ------------------------------------------------------------------------- */

@@ -95,3 +95,63 @@ def test_path_switch(lib):
     assert ex.set_path("simt") == "auto"
     assert ex.set_path("auto") == "simt"
     assert lib.exattn_set_path(5) == -1
+
+
+def _qk(B=1, H=1, nq=1, nk=1000, d=128, v=128, dtype=1):
+    import exact_tiled_softmax_gb300 as ex
+    return ex.QKShape(B, H, nq, nk, d, v, dtype)
+
+
+def test_splitkv_workspace_and_split_plan(lib):
+    """Summaries are 4 (2 + v) bytes per (slice, chunk, query) plus the status
+    word; chunks are whole multiples of 32 keys; 0 picks the count from the
+    shape alone."""
+    size = lambda shape, splits: lib.exattn_splitkv_workspace_size(ctypes.byref(shape), splits)
+
+    def chunks(shape, splits):
+        rows = shape.batch * shape.heads * shape.nq
+        body = size(shape, splits) - 256
+        per = 4 * (2 + shape.v)
+        for c in range(1, 5000):  # padding of the m and l arrays is < 2 x 256 bytes
+            if 0 <= body - c * rows * per < 512:
+                return c
+        raise AssertionError(body)
+
+    assert chunks(_qk(nk=1000), 1) == 1
+    assert chunks(_qk(nk=1000), 4) == 4        # 250 keys -> chunks of 256
+    assert chunks(_qk(nk=1000), 16) == 16      # 63 -> 64 keys per chunk
+    assert chunks(_qk(nk=1000), 40) == 32      # 25 -> 32 keys: only 32 chunks
+    assert chunks(_qk(nk=1000), 4096) == 32
+    # auto: 4864 CTAs over the slices, >= 256 keys per chunk
+    assert chunks(_qk(B=8, H=32, nk=16384), 0) == 19
+    assert chunks(_qk(B=1, H=1, nk=1000), 0) == 4
+    assert chunks(_qk(B=64, H=64, nk=1000), 0) == 2
+    assert chunks(_qk(B=128, H=64, nk=1000), 0) == 1
+    assert size(_qk(nq=65), 1) == 0            # more than 64 queries
+    assert size(_qk(d=20, dtype=1), 1) == 0    # bf16 rows need 8-element pieces
+    assert size(_qk(d=20, dtype=0), 1) != 0    # fp32: 4-element pieces
+    assert size(_qk(d=18, dtype=0), 1) == 0
+    assert size(_qk(), -1) == 0
+    assert size(_qk(), 4097) == 0
+
+
+def test_splitkv_host_side_argument_checks(lib):
+    vp = ctypes.c_void_p
+    good = vp(1 << 20)
+    ws = vp(1 << 21)
+
+    def call(shape, mask=0, window=0, bitmask=None, q=good, splits=1, ws_ptr=ws,
+             ws_bytes=1 << 30):
+        return lib.attn_fwd_splitkv(ctypes.byref(shape), q, good, good, 1.0, mask, window,
+                                    bitmask, splits, good, good, ws_ptr, ws_bytes, None)
+
+    assert call(_qk(nq=0)) == 1
+    assert call(_qk(nq=65)) == 2
+    assert call(_qk(d=264)) == 2
+    assert call(_qk(), mask=2, window=0) == 1
+    assert call(_qk(), mask=3) == 1
+    assert call(_qk(), splits=-1) == 1
+    assert call(_qk(), q=None) == 1
+    assert call(_qk(), q=vp((1 << 20) + 8)) == 3
+    assert call(_qk(), ws_ptr=vp((1 << 21) + 64)) == 3
+    assert call(_qk(), ws_bytes=100) == 4

@@ -186,6 +186,36 @@ def make_decode_inputs(B, H, nq, nk, d, v, dtype, mask="none", seed=1, p_allow=0
     return Q, K, V, bitmask
 
 
+@dataclass
+class DecodeWorkload:
+    """nq new queries at the end of an nk-key sequence (a decode step)."""
+    name: str
+    B: int
+    H: int
+    nq: int
+    nk: int
+    d: int
+    v: int
+    dtype: str
+    mask: str
+    scale: float
+    window: int = 0
+    seed: int = SEED_BASE + 100
+
+    def bytes_moved(self) -> int:
+        """Algorithmic HBM bytes of one step: read Q, K, V once, write Y and L."""
+        e = 4 if self.dtype == "f32" else 2
+        per = self.nq * self.d * e + self.nk * (self.d + self.v) * e + self.nq * (self.v * e + 4)
+        return self.B * self.H * per
+
+
+def decode_workload(nq: int = 1) -> DecodeWorkload:
+    """Decode step of the long-context training shape: B=8, H=32, d=v=128,
+    bf16, causal, nk=16384 keys (K and V 1 GiB each, far beyond L2)."""
+    return DecodeWorkload(f"decode-b8h32-nq{nq}-nk16384-d128-bf16-causal", 8, 32, nq, 16384,
+                          128, 128, "bf16", "causal", 1.0 / math.sqrt(128.0))
+
+
 def random_bitmask(n: int, p_allow: float, seed: int, diagonal: bool = True) -> np.ndarray:
     """A seeded random bit-row mask (diagonal forced on unless ``diagonal`` is False)."""
     g = torch.Generator().manual_seed(seed)
