@@ -506,7 +506,10 @@ def run_gpu_decode(args, w):
         step()
     barrier()
     K = args.steps
-    roles = (ex.KERNEL_SPLIT_PARTIAL, ex.KERNEL_SPLIT_MERGE)
+    # For nq <= 4 the chunk kernel merges in its last CTA per slice: no merge launch.
+    fused = w.nq <= 4
+    roles = (ex.KERNEL_SPLIT_PARTIAL,) if fused else (ex.KERNEL_SPLIT_PARTIAL,
+                                                     ex.KERNEL_SPLIT_MERGE)
     ev = {r: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(K)] for r in roles}
     for pairs_ in ev.values():
@@ -568,7 +571,8 @@ def run_gpu_decode(args, w):
                 "peak_kind": f"copy bandwidth, of {peak_kind}",
                 "traffic": read_traffic(f"splitkv_partial_{kind}"),
                 "kernel_ms": {"partial": kern_ms[ex.KERNEL_SPLIT_PARTIAL],
-                              "merge": kern_ms[ex.KERNEL_SPLIT_MERGE]}}
+                              "merge": "in the chunk kernel" if fused
+                              else kern_ms[ex.KERNEL_SPLIT_MERGE]}}
     line = {
         "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,

@@ -273,8 +273,10 @@ size_t exattn_splitkv_workspace_size(const exattn_qk_shape* shape, int num_split
   num_splits = resolve_splits(shape, num_splits);
   int chunk, splits;
   split_plan(shape->nk, num_splits, &chunk, &splits);
-  const size_t rows = (size_t)shape->batch * shape->heads * splits * shape->nq;
-  return kStatusBytes + 2 * align_up(sizeof(float) * rows, 256) + sizeof(float) * rows * shape->v;
+  const size_t bh = (size_t)shape->batch * shape->heads;
+  const size_t rows = bh * splits * shape->nq;
+  return kStatusBytes + align_up(sizeof(unsigned) * bh, 256) +
+         2 * align_up(sizeof(float) * rows, 256) + sizeof(float) * rows * shape->v;
 }
 
 int attn_fwd_splitkv(const exattn_qk_shape* shape, const void* Q, const void* K, const void* V,
@@ -309,12 +311,19 @@ int attn_fwd_splitkv(const exattn_qk_shape* shape, const void* Q, const void* K,
   a.bits = mask_kind == EXATTN_MASK_BITMASK ? bitmask : nullptr;
   a.sl2 = scale * 1.4426950408889634f;
   split_plan(shape->nk, resolve_splits(shape, num_splits), &a.chunk, &a.splits);
+  // Workspace: status word | chunk counters [BH] | m | l | z (each 256-byte aligned).
   const size_t rows = (size_t)a.BH * a.splits * a.nq;
-  char* ws = static_cast<char*>(workspace);
-  a.pm = reinterpret_cast<float*>(ws + kStatusBytes);
-  a.pl = reinterpret_cast<float*>(ws + kStatusBytes + align_up(sizeof(float) * rows, 256));
-  a.pz = reinterpret_cast<float*>(ws + kStatusBytes + 2 * align_up(sizeof(float) * rows, 256));
-  cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes, s);
+  const size_t cnt_bytes = align_up(sizeof(unsigned) * a.BH, 256);
+  char* ws = static_cast<char*>(workspace) + kStatusBytes;
+  a.counters = reinterpret_cast<unsigned*>(ws);
+  ws += cnt_bytes;
+  a.pm = reinterpret_cast<float*>(ws);
+  a.pl = reinterpret_cast<float*>(ws + align_up(sizeof(float) * rows, 256));
+  a.pz = reinterpret_cast<float*>(ws + 2 * align_up(sizeof(float) * rows, 256));
+  a.Y = Y;
+  a.L = L;
+  a.status = static_cast<unsigned*>(workspace);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes + cnt_bytes, s);
   if (e != cudaSuccess) return cuda_status(e, "attn_fwd_splitkv: clearing the status word");
   return cuda_status(launch_splitkv(a, shape->dtype, Y, L, static_cast<unsigned*>(workspace), s),
                      "attn_fwd_splitkv: launch");

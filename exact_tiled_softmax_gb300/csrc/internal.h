@@ -96,6 +96,10 @@ struct SplitArgs {
   float* pm;             // [BH][splits][nq] running max (exp2 domain)
   float* pl;             // [BH][splits][nq] running sum
   float* pz;             // [BH][splits][nq][v] unnormalised output
+  unsigned* counters;    // [BH] chunks finished (zeroed before the launch)
+  void* Y;               // outputs, for the kernels that merge in their last CTA
+  float* L;
+  unsigned* status;
 };
 size_t splitkv_smem_bytes(int nq, int d, int v, int elem_bytes);
 int splitkv_max_queries();

@@ -71,6 +71,93 @@ __device__ __forceinline__ float to_f(T x) {
   return Elem<T>::cvt(x);
 }
 
+// Star merge of the chunk summaries of one (slice, query) row by one warp.
+// Lanes split the chunks for the maximum and the sum; for z each lane owns 4
+// columns and walks the chunks with unconditional 16-byte loads (an empty
+// chunk's z is all zeros and its factor 2^(m_s - M) is 0), the factor
+// broadcast from the lane that computed it.  kCoherent reads through L2 only,
+// for summaries written by other CTAs of the same launch.
+template <bool kCoherent>
+__device__ __forceinline__ float ld_sum(const float* p) {
+  if constexpr (kCoherent) return __ldcg(p);
+  else return *p;
+}
+template <bool kCoherent>
+__device__ __forceinline__ float4 ld_sum4(const float* p) {
+  if constexpr (kCoherent) return __ldcg(reinterpret_cast<const float4*>(p));
+  else return *reinterpret_cast<const float4*>(p);
+}
+
+template <typename T, bool kCoherent>
+__device__ void merge_row(const SplitArgs& a, int bh, int q, T* Y, float* L, unsigned* status) {
+  const int lane = threadIdx.x & 31;
+  const int S = a.splits, v = a.v;
+  const size_t base = static_cast<size_t>(bh) * S * a.nq + q;  // row of chunk 0
+  const size_t stride = a.nq;                                   // rows between chunks
+  const size_t row = static_cast<size_t>(bh) * a.nq + q;
+  float M = -INFINITY;
+  for (int s = lane; s < S; s += 32) M = fmaxf(M, ld_sum<kCoherent>(a.pm + base + s * stride));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+  T* yrow = Y + row * v;
+  if (M == -INFINITY) {  // every chunk's summary is empty: the row's allowed set is empty
+    for (int c = lane; c < v; c += 32) Elem<T>::store(yrow + c, 0.f);
+    if (lane == 0) {
+      L[row] = -INFINITY;
+      raise_status(status, kStatusEmptyRow);
+    }
+    return;
+  }
+  float lsum = 0.f;
+  for (int s = lane; s < S; s += 32) {
+    const float ms = ld_sum<kCoherent>(a.pm + base + s * stride);
+    if (ms != -INFINITY) lsum += fast_exp2(ms - M) * ld_sum<kCoherent>(a.pl + base + s * stride);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
+  const float inv = 1.f / lsum;
+  for (int c0 = 4 * lane; c0 - 4 * lane < v; c0 += 128) {  // warp-uniform trip count
+    const int cl = c0 < v ? c0 : 0;                          // lanes past v read column 0
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      float f_own = 0.f;
+      if (s0 + lane < S) {
+        const float ms = ld_sum<kCoherent>(a.pm + base + (s0 + lane) * stride);
+        f_own = ms == -INFINITY ? 0.f : fast_exp2(ms - M);
+      }
+      const int cnt = min(32, S - s0);
+#pragma unroll 8
+      for (int k = 0; k < cnt; ++k) {
+        const float f = __shfl_sync(0xFFFFFFFFu, f_own, k);
+        const float4 z = ld_sum4<kCoherent>(a.pz + (base + (s0 + k) * stride) * v + cl);
+        acc.x = fmaf(f, z.x, acc.x);
+        acc.y = fmaf(f, z.y, acc.y);
+        acc.z = fmaf(f, z.z, acc.z);
+        acc.w = fmaf(f, z.w, acc.w);
+      }
+    }
+    if (c0 < v) {
+      Elem<T>::store(yrow + c0, acc.x * inv);
+      Elem<T>::store(yrow + c0 + 1, acc.y * inv);
+      Elem<T>::store(yrow + c0 + 2, acc.z * inv);
+      Elem<T>::store(yrow + c0 + 3, acc.w * inv);
+    }
+  }
+  if (lane == 0) L[row] = (M + log2f(lsum)) * kLn2;
+}
+
+// Separate merge pass (after splitkv_partial_kernel): one warp per row.
+constexpr int kMergeThreads = 64;
+
+template <typename T>
+__global__ void __launch_bounds__(kMergeThreads) splitkv_merge_kernel(SplitArgs a, T* Y, float* L,
+                                                                      unsigned* status) {
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (gw >= a.BH * a.nq) return;
+  const int bh = gw / a.nq;
+  merge_row<T, false>(a, bh, gw - bh * a.nq, Y, L, status);
+}
+
 // One warp per (batch*head, chunk): every query row of the chunk, lane = key
 // of the current 32-key tile.  K and V tiles are double-buffered in shared
 // memory (raw elements, rows padded by 16 bytes): tile t+1 streams in with
@@ -414,6 +501,16 @@ __global__ void __launch_bounds__(32 * kRegWarps) splitkv_reg_kernel(SplitArgs a
       a.pl[row] = lq;
     }
   }
+  // The last CTA of this slice to finish merges all of its chunk summaries
+  // (each CTA publishes its summary with a fence before counting itself).
+  __shared__ bool s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(a.counters + bh, 1u) == static_cast<unsigned>(a.splits - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (warp < nq) merge_row<T, true>(a, bh, warp, static_cast<T*>(a.Y), a.L, a.status);
 }
 
 template <typename T, int G, int CPL>
@@ -440,45 +537,6 @@ cudaError_t reg_dispatch(const SplitArgs& a, cudaStream_t s) {
   }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(256) splitkv_merge_kernel(SplitArgs a, T* Y, float* L,
-                                                            unsigned* status) {
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int rows = a.BH * a.nq;
-  if (gw >= rows) return;
-  const int bh = gw / a.nq, q = gw - bh * a.nq;
-  const size_t base = static_cast<size_t>(bh) * a.splits * a.nq + q;  // row of split 0
-  float M = -INFINITY;
-  for (int s = 0; s < a.splits; ++s) M = fmaxf(M, a.pm[base + static_cast<size_t>(s) * a.nq]);
-  T* yrow = Y + static_cast<size_t>(gw) * a.v;
-  if (M == -INFINITY) {  // every chunk's summary is empty: the row's allowed set is empty
-    for (int c = lane; c < a.v; c += 32) Elem<T>::store(yrow + c, 0.f);
-    if (lane == 0) {
-      L[gw] = -INFINITY;
-      raise_status(status, kStatusEmptyRow);
-    }
-    return;
-  }
-  float lsum = 0.f;
-  for (int s = 0; s < a.splits; ++s) {
-    const size_t r = base + static_cast<size_t>(s) * a.nq;
-    const float ms = a.pm[r];
-    if (ms != -INFINITY) lsum += fast_exp2(ms - M) * a.pl[r];
-  }
-  const float inv = 1.f / lsum;
-  for (int c = lane; c < a.v; c += 32) {
-    float z = 0.f;
-    for (int s = 0; s < a.splits; ++s) {
-      const size_t r = base + static_cast<size_t>(s) * a.nq;
-      const float ms = a.pm[r];
-      if (ms != -INFINITY) z = fmaf(fast_exp2(ms - M), a.pz[r * a.v + c], z);
-    }
-    Elem<T>::store(yrow + c, z * inv);
-  }
-  if (lane == 0) L[gw] = (M + log2f(lsum)) * kLn2;
-}
-
 template <typename T, int VPL>
 cudaError_t partial_launch(const SplitArgs& a, cudaStream_t s) {
   const size_t smem = splitkv_smem_bytes(a.nq, a.d, a.v, static_cast<int>(sizeof(T)));
@@ -495,17 +553,17 @@ cudaError_t partial_launch(const SplitArgs& a, cudaStream_t s) {
 template <typename T>
 cudaError_t splitkv_launch_t(const SplitArgs& a, void* Y, float* L, unsigned* status,
                              cudaStream_t s) {
+  if (a.nq <= kRegMaxNq) return reg_dispatch<T>(a, s);  // merges in its last CTA per slice
   cudaError_t e;
-  if (a.nq <= kRegMaxNq) e = reg_dispatch<T>(a, s);
-  else if (a.v <= 32) e = partial_launch<T, 1>(a, s);
+  if (a.v <= 32) e = partial_launch<T, 1>(a, s);
   else if (a.v <= 64) e = partial_launch<T, 2>(a, s);
   else if (a.v <= 128) e = partial_launch<T, 4>(a, s);
   else e = partial_launch<T, 8>(a, s);
   if (e != cudaSuccess) return e;
   const int rows = a.BH * a.nq;
   before_launch(kKernSplitMerge, s);
-  splitkv_merge_kernel<T><<<(rows * 32 + 255) / 256, 256, 0, s>>>(a, static_cast<T*>(Y), L,
-                                                                  status);
+  splitkv_merge_kernel<T><<<(rows * 32 + kMergeThreads - 1) / kMergeThreads, kMergeThreads, 0,
+                            s>>>(a, static_cast<T*>(Y), L, status);
   after_launch(kKernSplitMerge, s);
   return cudaGetLastError();
 }

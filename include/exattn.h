@@ -160,8 +160,9 @@ int attn_bwd_noalloc(const exattn_shape* shape, const void* Q, const void* K, co
  * blocks seen and merges it with each new block's summary (the star merge).
  * attn_fwd_splitkv cuts the keys into `num_splits` contiguous chunks handled
  * in parallel, writes every chunk's summary (running max, running sum,
- * unnormalised output) per query row to the workspace, and a second kernel
- * merges the summaries of all chunks, skipping empty ones, into Y and L.  The
+ * unnormalised output) per query row to the workspace; the summaries of all
+ * chunks are then merged, skipping empty ones, into Y and L (for nq <= 4 by the
+ * last CTA of each slice to finish, otherwise by a second kernel).  The
  * result is the same attention for every num_splits (up to rounding).
  *
  * Shapes: Q [B][H][nq][d], K [B][H][nk][d], V [B][H][nk][v], Y [B][H][nq][v]
@@ -187,7 +188,8 @@ typedef struct exattn_qk_shape {
   int dtype;
 } exattn_qk_shape;
 
-/* Workspace bytes of attn_fwd_splitkv (status word + summaries); 0 if invalid. */
+/* Workspace bytes of attn_fwd_splitkv (status word, a chunk counter per slice and
+ * the chunk summaries); 0 if invalid. */
 size_t exattn_splitkv_workspace_size(const exattn_qk_shape* shape, int num_splits);
 
 int attn_fwd_splitkv(const exattn_qk_shape* shape, const void* Q, const void* K, const void* V,
@@ -209,7 +211,7 @@ enum exattn_kernel {
   EXATTN_KERNEL_DQ_CONVERT = 3, /* fp32 dQ accumulator -> dQ (SIMT and ATOMIC_DQ paths) */
   EXATTN_KERNEL_BWD_Q = 4,      /* the query-major dQ kernel alone (AUTO path) */
   EXATTN_KERNEL_SPLIT_PARTIAL = 5, /* per-chunk summaries of attn_fwd_splitkv */
-  EXATTN_KERNEL_SPLIT_MERGE = 6    /* the merge kernel of attn_fwd_splitkv */
+  EXATTN_KERNEL_SPLIT_MERGE = 6    /* the merge kernel of attn_fwd_splitkv (nq > 4) */
 };
 
 /* One-shot: on the next launch of kernel `which` (an exattn_kernel), record

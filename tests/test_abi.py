@@ -104,13 +104,14 @@ def _qk(B=1, H=1, nq=1, nk=1000, d=128, v=128, dtype=1):
 
 def test_splitkv_workspace_and_split_plan(lib):
     """Summaries are 4 (2 + v) bytes per (slice, chunk, query) plus the status
-    word; chunks are whole multiples of 32 keys; 0 picks the count from the
+    word and a chunk counter per slice; chunks are whole multiples of 32 keys; 0 picks the count from the
     shape alone."""
     size = lambda shape, splits: lib.exattn_splitkv_workspace_size(ctypes.byref(shape), splits)
 
     def chunks(shape, splits):
         rows = shape.batch * shape.heads * shape.nq
-        body = size(shape, splits) - 256
+        counters = (4 * shape.batch * shape.heads + 255) // 256 * 256
+        body = size(shape, splits) - 256 - counters
         per = 4 * (2 + shape.v)
         for c in range(1, 5000):  # padding of the m and l arrays is < 2 x 256 bytes
             if 0 <= body - c * rows * per < 512:
