@@ -19,10 +19,12 @@ Modules:
   dense  -- the plain dense definition (forms whole rows of S); the oracle proper
   tiled  -- the pages' block procedures (summary, merge, skip, recompute
             reverse), used only to pin ``dense`` against the pages
+  philox -- the counter-based generator (Philox-4x32-10) and the dropout keep
+            mask that the dropout forms of ``dense`` replay in both passes
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
 reference arm of ``bench.py`` may import this package.  It shares no code with
 the CUDA path and never imports it.  Every function here is pinned by the CPU
 tests in ``tests/test_oracle.py``; none is "parity unpinned".
 """
-from . import dense, masks, tiled  # noqa: F401
+from . import dense, masks, philox, tiled  # noqa: F401

@@ -156,3 +156,103 @@ def forward_rect(Q, K, V, c, mask_kind, window=0, bitmask=None):
             Y[h][rows] = y
             L[h][rows] = l
     return Y.reshape(V.shape[:-2] + (nq, V.shape[-1])), L.reshape(Q.shape[:-1])
+
+
+# --------------------------------------------------------------------------- #
+# Dropout with a replayed mask ("Exact tiled softmax attention with block-
+# recomputed vector-Jacobian products", Reverse procedure, closing remark: the
+# reverse pass must use the forward pass's realised mask).  Reading: the mask
+# xi acts on the normalised probabilities, kept entries scaled by
+# s = 1 / (1 - q):
+#
+#   Y_i = sum_j p_ij xi_ij s V_j,     L_i = m_i + ln l_i  (undropped statistics)
+#
+# whose vector-Jacobian product for G = dY is
+#
+#   dV_j += p_ij xi_ij s G_i,   dP_ij = xi_ij s G_i . V_j,
+#   delta_i = sum_j p_ij dP_ij  (= G_i . Y_i),   gamma_ij = p_ij (dP_ij - delta_i),
+#   dQ_i += c gamma_ij K_j,     dK_j += c gamma_ij Q_i.
+# --------------------------------------------------------------------------- #
+
+def head_forward_dropout(Q, K, V, c, allowed, keep, kscale):
+    """One head with the realised keep mask ``keep`` [n,n] and factor ``kscale``."""
+    _check_rows(allowed)
+    n = Q.shape[0]
+    Y = np.empty((n, V.shape[1]))
+    L = np.empty(n)
+    for r0 in range(0, n, ROW_GROUP):
+        r1 = min(n, r0 + ROW_GROUP)
+        s = np.where(allowed[r0:r1], c * (Q[r0:r1] @ K.T), -np.inf)
+        m = s.max(axis=1)
+        e = np.exp(s - m[:, None])
+        l = e.sum(axis=1)
+        P = e / l[:, None]
+        Y[r0:r1] = (P * keep[r0:r1] * kscale) @ V
+        L[r0:r1] = m + np.log(l)
+    return Y, L
+
+
+def head_backward_dropout(Q, K, V, G, c, allowed, keep, kscale):
+    """One head: (dQ, dK, dV, delta) with the same realised mask as the forward."""
+    _check_rows(allowed)
+    n = Q.shape[0]
+    dQ = np.zeros_like(Q)
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    delta = np.empty(n)
+    for r0 in range(0, n, ROW_GROUP):
+        r1 = min(n, r0 + ROW_GROUP)
+        s = np.where(allowed[r0:r1], c * (Q[r0:r1] @ K.T), -np.inf)
+        e = np.exp(s - s.max(axis=1)[:, None])
+        P = e / e.sum(axis=1)[:, None]
+        xs = keep[r0:r1] * kscale
+        Gr = G[r0:r1]
+        dV += (P * xs).T @ Gr
+        dP = (Gr @ V.T) * xs
+        dl = (P * dP).sum(axis=1)
+        dS = P * (dP - dl[:, None])
+        dQ[r0:r1] = c * (dS @ K)
+        dK += c * (dS.T @ Q[r0:r1])
+        delta[r0:r1] = dl
+    return dQ, dK, dV, delta
+
+
+def _dropout_heads(Q, n, q, seed, idx):
+    from .philox import keep_mask, keep_scale
+    return [keep_mask(h, n, n, q, seed) for h in idx], keep_scale(q)
+
+
+def forward_dropout(Q, K, V, c, mask_kind, window=0, bitmask=None, q=0.0, seed=0, heads=None):
+    """Batched dropout forward; the mask of flat head h is philox.keep_mask(h, ...)."""
+    n = Q.shape[-2]
+    allowed = allowed_matrix(n, mask_kind, window, bitmask)
+    qh, kh, vh = _heads(Q), _heads(K), _heads(V)
+    idx = list(range(qh.shape[0])) if heads is None else list(heads)
+    keeps, ks = _dropout_heads(Q, n, q, seed, idx)
+    out = [head_forward_dropout(qh[h], kh[h], vh[h], c, allowed, kp, ks)
+           for h, kp in zip(idx, keeps)]
+    Y = np.stack([o[0] for o in out])
+    L = np.stack([o[1] for o in out])
+    if heads is None:
+        Y = Y.reshape(V.shape[:-2] + Y.shape[-2:])
+        L = L.reshape(Q.shape[:-1])
+    return Y, L
+
+
+def backward_dropout(Q, K, V, G, c, mask_kind, window=0, bitmask=None, q=0.0, seed=0,
+                     heads=None):
+    """Batched dropout reverse pass -> (dQ, dK, dV, delta)."""
+    n = Q.shape[-2]
+    allowed = allowed_matrix(n, mask_kind, window, bitmask)
+    qh, kh, vh, gh = _heads(Q), _heads(K), _heads(V), _heads(G)
+    idx = list(range(qh.shape[0])) if heads is None else list(heads)
+    keeps, ks = _dropout_heads(Q, n, q, seed, idx)
+    out = [head_backward_dropout(qh[h], kh[h], vh[h], gh[h], c, allowed, kp, ks)
+           for h, kp in zip(idx, keeps)]
+    res = [np.stack([o[t] for o in out]) for t in range(4)]
+    if heads is None:
+        res[0] = res[0].reshape(Q.shape)
+        res[1] = res[1].reshape(K.shape)
+        res[2] = res[2].reshape(V.shape)
+        res[3] = res[3].reshape(Q.shape[:-1])
+    return tuple(res)

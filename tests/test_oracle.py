@@ -516,3 +516,193 @@ def test_split_merge_is_exact_for_every_split():
                 mm, ml, mz = tiled.merge(m[both], l[both], z[both], bm[both], bl[both], bz[both])
                 m[both], l[both], z[both] = mm, ml, mz
         assert _rel(z / l[:, None], Y) <= 1e-12 and _rel(m + np.log(l), L) <= 1e-12
+
+
+# --------------------------------------------------------------------------- #
+# Dropout with a replayed mask (oracle.philox and the dropout forms of dense)
+# --------------------------------------------------------------------------- #
+
+from oracle import philox  # noqa: E402
+
+DROPOUT_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "dropout_cases.json")
+
+
+def _hex(xs):
+    return np.array([int(x, 16) for x in xs], dtype=np.uint32)
+
+
+def test_philox_known_answer_vectors():
+    cases = json.load(open(DROPOUT_GOLDEN))["philox4x32_10"]
+    for c in cases:
+        got = philox.philox4x32_10(_hex(c["ctr"]), _hex(c["key"]))
+        assert np.array_equal(got, _hex(c["out"])), c
+
+
+def test_dropout_mask_layout_golden():
+    c = json.load(open(DROPOUT_GOLDEN))["mask_case"]
+    u = philox.random_u16(c["bh"], c["row"] + 1, 8, c["seed"])[c["row"]]
+    assert np.array_equal(u, _hex(c["u16"]))
+    assert philox.threshold(c["q"]) == c["threshold"]
+    assert philox.keep_scale(c["q"]) == c["scale"]
+    keep = philox.keep_mask(c["bh"], 1, 8, c["q"], c["seed"])[0]
+    assert keep.astype(int).tolist() == c["keep"]
+
+
+def test_dropout_mask_matches_its_stated_counter_layout():
+    """The vectorised mask equals scalar generator calls with the documented
+    counter (j // 8, i, bh, 0) and key (seed low, seed high)."""
+    seed, bh, rows, cols = 0x1234_5678_9ABC_DEF0, 37, 13, 45
+    u = philox.random_u16(bh, rows, cols, seed)
+    key = np.array([seed & 0xFFFFFFFF, seed >> 32], dtype=np.uint32)
+    for i, j in [(0, 0), (5, 9), (12, 44), (7, 31), (3, 40)]:
+        out = philox.philox4x32_10(np.array([j // 8, i, bh, 0], dtype=np.uint32), key)
+        w = out[(j % 8) // 2]
+        assert u[i, j] == ((int(w) >> (16 * (j % 2))) & 0xFFFF)
+
+
+def test_dropout_threshold_and_rate():
+    assert philox.threshold(0.0) == 0 and philox.keep_scale(0.0) == 1.0
+    assert philox.threshold(0.1) == 6554
+    assert philox.threshold(0.9999999) == 65535
+    with pytest.raises(ValueError):
+        philox.threshold(1.0)
+    with pytest.raises(ValueError):
+        philox.threshold(-0.1)
+    # Keep rate over 512 x 512 entries within 5 standard deviations of 1 - t/65536.
+    for q in (0.1, 0.5):
+        keep = philox.keep_mask(3, 512, 512, q, seed=99)
+        p = 1 - philox.threshold(q) / 65536
+        sd = math.sqrt(p * (1 - p) / keep.size)
+        assert abs(keep.mean() - p) <= 5 * sd
+    # Different slices and seeds give different masks.
+    a = philox.keep_mask(0, 64, 64, 0.5, 1)
+    assert not np.array_equal(a, philox.keep_mask(1, 64, 64, 0.5, 1))
+    assert not np.array_equal(a, philox.keep_mask(0, 64, 64, 0.5, 2))
+
+
+def _drop_case(seed=21, n=5, d=3, v=4, q=0.4):
+    r = _rng(seed)
+    Q, K, V, G = (r.normal(size=(n, d)), r.normal(size=(n, d)), r.normal(size=(n, v)),
+                  r.normal(size=(n, v)))
+    allowed = masks.allowed_matrix(n, masks.CAUSAL)
+    keep = philox.keep_mask(2, n, n, q, seed=7)
+    return Q, K, V, G, allowed, keep, philox.keep_scale(q)
+
+
+def dropout_pin_failures(fwd, bwd):
+    """The dropout pins as one list of failures (used for the planted mistakes)."""
+    fails = []
+    c = 0.7
+    # q = 0 reduces to the plain oracle.
+    Q, K, V, G, allowed, _, _ = _drop_case()
+    ones = np.ones_like(allowed)
+    Y0, L0 = dense.head_forward(Q, K, V, c, allowed)
+    Y1, L1 = fwd(Q, K, V, c, allowed, ones, 1.0)
+    if _rel(Y1, Y0) > 1e-14 or _rel(L1, L0) > 1e-14:
+        fails.append("q0_forward")
+    g0 = dense.head_backward(Q, K, V, G, c, allowed)
+    g1 = bwd(Q, K, V, G, c, allowed, ones, 1.0)
+    if any(_rel(a, b) > 1e-13 for a, b in zip(g1[:3], g0[:3])):
+        fails.append("q0_backward")
+    # Central finite differences of <G, Y> with the realised mask held fixed.
+    Q, K, V, G, allowed, keep, ks = _drop_case()
+    grads = bwd(Q, K, V, G, c, allowed, keep, ks)
+    for which, X in enumerate((Q, K, V)):
+        num = np.zeros_like(X)
+        h = 1e-6
+        for idx in np.ndindex(X.shape):
+            args = [Q.copy(), K.copy(), V.copy()]
+            args[which][idx] += h
+            yp = np.sum(G * fwd(*args, c, allowed, keep, ks)[0])
+            args[which][idx] -= 2 * h
+            ym = np.sum(G * fwd(*args, c, allowed, keep, ks)[0])
+            num[idx] = (yp - ym) / (2 * h)
+        if _rel(grads[which], num) > 1e-5:
+            fails.append(f"fd_{'QKV'[which]}")
+    # delta is G . Y with the dropped Y (the identity survives dropout).
+    Y, L = fwd(Q, K, V, c, allowed, keep, ks)
+    if _rel(grads[3], np.sum(G * Y, axis=1)) > 1e-12:
+        fails.append("delta_identity")
+    # L is the undropped statistic.
+    if _rel(L, dense.head_forward(Q, K, V, c, allowed)[1]) > 1e-14:
+        fails.append("L_undropped")
+    # Unbiased: the mean of Y over many masks approaches the plain Y.
+    n = Q.shape[0]
+    acc = np.zeros_like(Y)
+    for sd in range(400):
+        kp = philox.keep_mask(0, n, n, 0.5, seed=1000 + sd)
+        acc += fwd(Q, K, V, c, allowed, kp, philox.keep_scale(0.5))[0]
+    if _rel(acc / 400, dense.head_forward(Q, K, V, c, allowed)[0]) > 0.15:
+        fails.append("unbiased")
+    return fails
+
+
+def test_dropout_oracle_pins():
+    assert dropout_pin_failures(dense.head_forward_dropout, dense.head_backward_dropout) == []
+
+
+def _dropout_mutant(fault):
+    def fwd(Q, K, V, c, allowed, keep, ks):
+        s = np.where(allowed, c * (Q @ K.T), -np.inf)
+        m = s.max(1)
+        e = np.exp(s - m[:, None])
+        if fault == "mask_in_sum":
+            e_l = e * keep
+            l = np.where(e_l.sum(1) > 0, e_l.sum(1), 1.0)
+        else:
+            l = e.sum(1)
+        P = e / l[:, None]
+        kk = keep.T if fault == "mask_transposed" else keep
+        sc = 1.0 if fault == "no_keep_scale" else ks
+        Y = (P * kk * sc) @ V
+        return Y, m + np.log(l)
+
+    def bwd(Q, K, V, G, c, allowed, keep, ks):
+        s = np.where(allowed, c * (Q @ K.T), -np.inf)
+        e = np.exp(s - s.max(1)[:, None])
+        P = e / e.sum(1)[:, None]
+        xs = keep * ks
+        dV = (P if fault == "dV_undropped" else P * xs).T @ G
+        dP = G @ V.T
+        if fault != "dP_unmasked":
+            dP = dP * xs
+        delta = (P * dP).sum(1)
+        if fault == "delta_undropped":
+            delta = (P * (G @ V.T)).sum(1)
+        dS = P * (dP - delta[:, None])
+        return c * (dS @ K), c * (dS.T @ Q), dV, delta
+
+    return fwd, bwd
+
+
+DROPOUT_FAULTS = ["mask_in_sum", "mask_transposed", "no_keep_scale", "dV_undropped",
+                  "dP_unmasked", "delta_undropped"]
+
+
+def test_dropout_unfaulted_copy_passes():
+    assert dropout_pin_failures(*_dropout_mutant(None)) == []
+
+
+@pytest.mark.parametrize("fault", DROPOUT_FAULTS)
+def test_dropout_planted_mistakes_are_caught(fault):
+    assert dropout_pin_failures(*_dropout_mutant(fault)), f"no pin caught {fault}"
+
+
+def test_batched_dropout_uses_each_heads_own_mask():
+    r = _rng(31)
+    B, H, n, d = 2, 3, 9, 4
+    Q, K, V, G = (r.normal(size=(B, H, n, d)) for _ in range(4))
+    Y, L = dense.forward_dropout(Q, K, V, 0.5, masks.CAUSAL, q=0.3, seed=5)
+    allowed = masks.allowed_matrix(n, masks.CAUSAL)
+    for b in range(B):
+        for h in range(H):
+            keep = philox.keep_mask(b * H + h, n, n, 0.3, 5)
+            y, l = dense.head_forward_dropout(Q[b, h], K[b, h], V[b, h], 0.5, allowed, keep,
+                                              philox.keep_scale(0.3))
+            assert np.array_equal(Y[b, h], y) and np.array_equal(L[b, h], l)
+    g = dense.backward_dropout(Q, K, V, G, 0.5, masks.CAUSAL, q=0.3, seed=5, heads=[4])
+    keep = philox.keep_mask(4, n, n, 0.3, 5)
+    ref = dense.head_backward_dropout(Q[1, 1], K[1, 1], V[1, 1], G[1, 1], 0.5, allowed, keep,
+                                      philox.keep_scale(0.3))
+    for a, b_ in zip(g, ref):
+        assert np.array_equal(a[0], b_)
