@@ -75,6 +75,12 @@ def load_library():
     lib.attn_fwd.restype = ci
     lib.attn_bwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, cf, ci, ci, vp, vp, vp, vp, vp, sz, vp]
     lib.attn_bwd.restype = ci
+    u64 = ctypes.c_uint64
+    lib.attn_fwd_dropout.argtypes = [sp, vp, vp, vp, cf, ci, ci, vp, cf, u64, vp, vp, vp, sz, vp]
+    lib.attn_fwd_dropout.restype = ci
+    lib.attn_bwd_dropout.argtypes = [sp, vp, vp, vp, vp, vp, vp, cf, ci, ci, vp, cf, u64, vp, vp,
+                                     vp, vp, sz, vp]
+    lib.attn_bwd_dropout.restype = ci
     lib.exattn_device_status.argtypes = [vp, vp]
     lib.exattn_device_status.restype = ci
     lib.exattn_status_string.argtypes = [ci]
@@ -151,8 +157,10 @@ def workspace(nbytes: int, device) -> torch.Tensor:
 
 
 def fwd(q, k, v, scale, mask="none", window=0, bitmask=None, y=None, L=None, ws=None,
-        stream=None):
-    """Forward pass -> (Y, L).  q, k [B,H,n,d], v [B,H,n,v]; bitmask int32/uint32 words."""
+        stream=None, dropout_p=0.0, seed=0):
+    """Forward pass -> (Y, L).  q, k [B,H,n,d], v [B,H,n,v]; bitmask int32/uint32 words.
+    ``dropout_p`` > 0 drops probabilities with the replayable mask of ``seed``
+    (attn_fwd_dropout); the reverse pass must get the same two values."""
     lib = load_library()
     shape = _shape(q, v)
     _check((k, v, y), q.dtype, q.device)
@@ -164,17 +172,23 @@ def fwd(q, k, v, scale, mask="none", window=0, bitmask=None, y=None, L=None, ws=
     need = lib.exattn_fwd_workspace_size(ctypes.byref(shape), kind)
     if ws is None:
         ws = workspace(need, q.device)
-    st = lib.attn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale), kind,
-                      int(window), _ptr(bitmask), _ptr(y), _ptr(L), _ptr(ws), ws.numel(),
-                      _stream(stream))
+    if dropout_p:
+        st = lib.attn_fwd_dropout(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale),
+                                  kind, int(window), _ptr(bitmask), float(dropout_p), int(seed),
+                                  _ptr(y), _ptr(L), _ptr(ws), ws.numel(), _stream(stream))
+    else:
+        st = lib.attn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale), kind,
+                          int(window), _ptr(bitmask), _ptr(y), _ptr(L), _ptr(ws), ws.numel(),
+                          _stream(stream))
     if st != 0:
-        raise ExattnError(st, "attn_fwd")
+        raise ExattnError(st, "attn_fwd_dropout" if dropout_p else "attn_fwd")
     return y, L
 
 
 def bwd(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, dq=None, dk=None,
-        dv=None, ws=None, stream=None):
-    """Reverse pass -> (dQ, dK, dV) for the upstream gradient dy."""
+        dv=None, ws=None, stream=None, dropout_p=0.0, seed=0):
+    """Reverse pass -> (dQ, dK, dV) for the upstream gradient dy (with the forward
+    pass's ``dropout_p`` and ``seed`` when it used dropout)."""
     lib = load_library()
     shape = _shape(q, v)
     _check((k, v, y, dy, dq, dk, dv), q.dtype, q.device)
@@ -185,9 +199,15 @@ def bwd(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, dq=None, 
     need = lib.exattn_bwd_workspace_size(ctypes.byref(shape), kind)
     if ws is None:
         ws = workspace(need, q.device)
-    st = lib.attn_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(dy),
-                      _ptr(L), float(scale), kind, int(window), _ptr(bitmask), _ptr(dq),
-                      _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream))
+    if dropout_p:
+        st = lib.attn_bwd_dropout(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(y),
+                                  _ptr(dy), _ptr(L), float(scale), kind, int(window),
+                                  _ptr(bitmask), float(dropout_p), int(seed), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), _ptr(ws), ws.numel(), _stream(stream))
+    else:
+        st = lib.attn_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(dy),
+                          _ptr(L), float(scale), kind, int(window), _ptr(bitmask), _ptr(dq),
+                          _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream))
     if st != 0:
         raise ExattnError(st, "attn_bwd")
     return dq, dk, dv

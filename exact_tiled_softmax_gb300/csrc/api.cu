@@ -1,5 +1,6 @@
 // The C ABI of libexattn (include/exattn.h): argument checks, workspace layout
 // and kernel dispatch.  No memory is allocated here.
+#include <math.h>
 #include <stdint.h>
 #include <stdio.h>
 
@@ -58,7 +59,22 @@ Problem make_problem(const exattn_shape* s, float scale, int mask_kind, int wind
   p.window = mask_kind == EXATTN_MASK_WINDOW ? window : 0;
   p.words_per_row = (s->n + 31) / 32;
   p.bitmask = mask_kind == EXATTN_MASK_BITMASK ? bitmask : nullptr;
+  p.drop_t = 0;
+  p.drop_scale = 1.f;
+  p.seed_lo = p.seed_hi = 0;
   return p;
+}
+
+// Dropout threshold of a drop probability q in [0, 1): t = min(65535,
+// floor(q * 65536 + 1/2)); kept entries are scaled by 65536 / (65536 - t).
+bool valid_dropout(float q) { return q >= 0.f && q < 1.f; }  // false for NaN
+
+void set_dropout(Problem& p, float q, uint64_t seed) {
+  const double t = floor(static_cast<double>(q) * 65536.0 + 0.5);
+  p.drop_t = t > 65535.0 ? 65535u : static_cast<uint32_t>(t);
+  p.drop_scale = static_cast<float>(65536.0 / (65536.0 - p.drop_t));
+  p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFu);
+  p.seed_hi = static_cast<uint32_t>(seed >> 32);
 }
 
 // Reverse-pass workspace: status word | delta [BH][npad] | lse2 [BH][npad] |
@@ -136,13 +152,16 @@ size_t exattn_bwd_workspace_size(const exattn_shape* shape, int mask_kind) {
          sizeof(float) * (size_t)shape->batch * shape->heads * shape->n * shape->d;
 }
 
-int attn_fwd(const exattn_shape* shape, const void* Q, const void* K, const void* V,
-             float scale, int mask_kind, int window, const uint32_t* bitmask, void* Y, float* L,
-             void* workspace, size_t workspace_bytes, void* cuda_stream) {
+namespace {
+
+int fwd_impl(const exattn_shape* shape, const void* Q, const void* K, const void* V, float scale,
+             int mask_kind, int window, const uint32_t* bitmask, float dropout_p, uint64_t seed,
+             void* Y, float* L, void* workspace, size_t workspace_bytes, void* cuda_stream) {
   int st = check_shape(shape);
   if (st != EXATTN_OK) return st;
   st = check_mask(mask_kind, window, bitmask);
   if (st != EXATTN_OK) return st;
+  if (!valid_dropout(dropout_p)) return EXATTN_INVALID_ARG;
   if (!Q || !K || !V || !Y || !L || !workspace) return EXATTN_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Y) || !aligned16(L))
     return EXATTN_MISALIGNED;
@@ -154,6 +173,7 @@ int attn_fwd(const exattn_shape* shape, const void* Q, const void* K, const void
   exattn::g_last_error[0] = 0;
   FwdArgs a;
   a.p = make_problem(shape, scale, mask_kind, window, bitmask);
+  if (dropout_p > 0.f) set_dropout(a.p, dropout_p, seed);
   a.Q = Q;
   a.K = K;
   a.V = V;
@@ -167,14 +187,15 @@ int attn_fwd(const exattn_shape* shape, const void* Q, const void* K, const void
   return cuda_status(launch_simt_fwd(a, s), "attn_fwd: SIMT forward launch");
 }
 
-int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void* V,
+int bwd_impl(const exattn_shape* shape, const void* Q, const void* K, const void* V,
              const void* Y, const void* dY, const float* L, float scale, int mask_kind,
-             int window, const uint32_t* bitmask, void* dQ, void* dK, void* dV, void* workspace,
-             size_t workspace_bytes, void* cuda_stream) {
+             int window, const uint32_t* bitmask, float dropout_p, uint64_t seed, void* dQ,
+             void* dK, void* dV, void* workspace, size_t workspace_bytes, void* cuda_stream) {
   int st = check_shape(shape);
   if (st != EXATTN_OK) return st;
   st = check_mask(mask_kind, window, bitmask);
   if (st != EXATTN_OK) return st;
+  if (!valid_dropout(dropout_p)) return EXATTN_INVALID_ARG;
   if (!Q || !K || !V || !Y || !dY || !L || !dQ || !dK || !dV || !workspace)
     return EXATTN_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Y) || !aligned16(dY) ||
@@ -189,6 +210,7 @@ int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void
   char* ws = static_cast<char*>(workspace);
   BwdArgs a;
   a.p = make_problem(shape, scale, mask_kind, window, bitmask);
+  if (dropout_p > 0.f) set_dropout(a.p, dropout_p, seed);
   a.Q = Q;
   a.K = K;
   a.V = V;
@@ -223,6 +245,40 @@ int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void
     e = launch_simt_bwd(a, s);
   if (e != cudaSuccess) return cuda_status(e, "attn_bwd: reverse kernel launch");
   return cuda_status(launch_dq_convert(a, s), "attn_bwd: dQ conversion launch");
+}
+
+}  // namespace
+
+int attn_fwd(const exattn_shape* shape, const void* Q, const void* K, const void* V,
+             float scale, int mask_kind, int window, const uint32_t* bitmask, void* Y, float* L,
+             void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  return fwd_impl(shape, Q, K, V, scale, mask_kind, window, bitmask, 0.f, 0, Y, L, workspace,
+                  workspace_bytes, cuda_stream);
+}
+
+int attn_fwd_dropout(const exattn_shape* shape, const void* Q, const void* K, const void* V,
+                     float scale, int mask_kind, int window, const uint32_t* bitmask,
+                     float dropout_p, uint64_t seed, void* Y, float* L, void* workspace,
+                     size_t workspace_bytes, void* cuda_stream) {
+  return fwd_impl(shape, Q, K, V, scale, mask_kind, window, bitmask, dropout_p, seed, Y, L,
+                  workspace, workspace_bytes, cuda_stream);
+}
+
+int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void* V,
+             const void* Y, const void* dY, const float* L, float scale, int mask_kind,
+             int window, const uint32_t* bitmask, void* dQ, void* dK, void* dV, void* workspace,
+             size_t workspace_bytes, void* cuda_stream) {
+  return bwd_impl(shape, Q, K, V, Y, dY, L, scale, mask_kind, window, bitmask, 0.f, 0, dQ, dK,
+                  dV, workspace, workspace_bytes, cuda_stream);
+}
+
+int attn_bwd_dropout(const exattn_shape* shape, const void* Q, const void* K, const void* V,
+                     const void* Y, const void* dY, const float* L, float scale, int mask_kind,
+                     int window, const uint32_t* bitmask, float dropout_p, uint64_t seed,
+                     void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
+                     void* cuda_stream) {
+  return bwd_impl(shape, Q, K, V, Y, dY, L, scale, mask_kind, window, bitmask, dropout_p, seed,
+                  dQ, dK, dV, workspace, workspace_bytes, cuda_stream);
 }
 
 namespace {

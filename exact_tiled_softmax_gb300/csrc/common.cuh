@@ -42,6 +42,45 @@ struct MaskView {
   }
 };
 
+// Philox-4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC 2011): each round multiplies counter words
+// 0 and 2 by the round multipliers (keeping both 32-bit halves of the
+// products), mixes the high halves into words 1 and 3 with the key, and the
+// key advances by the Weyl increments between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = c.x * 0xD2511F53u, hi0 = __umulhi(c.x, 0xD2511F53u);
+    const uint32_t lo1 = c.z * 0xCD9E8D57u, hi1 = __umulhi(c.z, 0xCD9E8D57u);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// Dropout keep bits of keys 8*jb .. 8*jb+7 of row i in slice bh: bit t is set
+// when key 8*jb + t is kept.  Counter (jb, i, bh, 0), key (seed low, seed
+// high); key 8*jb + t reads half t%2 of output word t/2 (low half first) and
+// is kept when that 16-bit value is >= drop_t ("Exact tiled softmax attention
+// with block-recomputed vector-Jacobian products", Reverse procedure: the
+// reverse pass replays exactly these decisions).
+__device__ __forceinline__ uint32_t keep_byte(uint32_t drop_t, uint32_t seed_lo, uint32_t seed_hi,
+                                              int bh, int i, int jb) {
+  const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(jb), static_cast<uint32_t>(i),
+                                           static_cast<uint32_t>(bh), 0u),
+                                seed_lo, seed_hi);
+  const uint32_t th = drop_t << 16;  // word >= t * 2^16  <=>  high half >= t
+  return static_cast<uint32_t>((w.x & 0xFFFFu) >= drop_t) |
+         (static_cast<uint32_t>(w.x >= th) << 1) |
+         (static_cast<uint32_t>((w.y & 0xFFFFu) >= drop_t) << 2) |
+         (static_cast<uint32_t>(w.y >= th) << 3) |
+         (static_cast<uint32_t>((w.z & 0xFFFFu) >= drop_t) << 4) |
+         (static_cast<uint32_t>(w.z >= th) << 5) |
+         (static_cast<uint32_t>((w.w & 0xFFFFu) >= drop_t) << 6) |
+         (static_cast<uint32_t>(w.w >= th) << 7);
+}
+
 template <typename T> struct Elem;
 // load(): read one element from GLOBAL memory; cvt(): convert a value already
 // in registers.

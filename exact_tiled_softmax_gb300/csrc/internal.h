@@ -17,6 +17,11 @@ struct Problem {
   float scale;
   int mask_kind, window, words_per_row;
   const uint32_t* bitmask;
+  // Dropout (drop_t == 0: none): key j of row i in slice bh is kept when the
+  // 16-bit Philox value u_ij >= drop_t; kept entries are scaled by drop_scale.
+  uint32_t drop_t;
+  float drop_scale;
+  uint32_t seed_lo, seed_hi;
 };
 
 struct FwdArgs {

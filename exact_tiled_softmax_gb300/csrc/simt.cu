@@ -78,6 +78,17 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
     load_tile(Vs, v, Vh, j0, kBK, n, v);
     __syncthreads();
 
+    // Dropout keep bits of this row for the tile's four 8-key groups: lane l8 < 4
+    // of the row draws group l8 (one Philox call), the row's lanes share them.
+    uint32_t kbits = 0xFFFFFFFFu;
+    if (p.drop_t != 0) {
+      uint32_t mine = 0;
+      if (l8 < 4 && i < n) mine = keep_byte(p.drop_t, p.seed_lo, p.seed_hi, bh, i, (j0 >> 3) + l8);
+      kbits = 0;
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        kbits |= ((__shfl_sync(0xffffffffu, mine, (tid & 24) + t) >> l8) & 1u) << t;
+    }
     float s[4];
     float tmax = -INFINITY;
 #pragma unroll
@@ -100,8 +111,8 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const float pv = exp2f(s[t] - mref);
-      psum += pv;
-      Ps[r * (kBK + 1) + l8 + 8 * t] = pv;
+      psum += pv;  // the row sum is of the undropped p
+      Ps[r * (kBK + 1) + l8 + 8 * t] = ((kbits >> t) & 1u) ? pv : 0.f;
     }
 #pragma unroll
     for (int off = 1; off < 8; off <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
@@ -122,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
 
   if (i < n) {
     T* Yr = static_cast<T*>(a.Y) + ((size_t)bh * n + i) * v;
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float inv = l > 0.f ? p.drop_scale / l : 0.f;
 #pragma unroll
     for (int t = 0; t < VPT; ++t) {
       const int col = l8 + 8 * t;
@@ -149,6 +160,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(BwdArgs a) {
   float* Ls = dSt + kBK * (kBQ + 1);
   float* Ds = Ls + kBQ;
 
+  __shared__ uint8_t kbits_s[kBQ][4];  // dropout keep bits of the current query tile
   const int bh = blockIdx.y, j0 = blockIdx.x * kBK;
   const int tid = threadIdx.x, r = tid >> 3, l8 = tid & 7;
   const int j = j0 + r;
@@ -187,6 +199,12 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(BwdArgs a) {
     __syncthreads();
     load_tile(Qs, dp, Qh, q0, kBQ, n, d);
     load_tile(dYs, vp, dYh, q0, kBQ, n, v);
+    if (p.drop_t != 0 && tid < kBQ * 4) {  // keep bits: 32 queries x four 8-key groups
+      const int qq = tid >> 2, g = tid & 3, gi = q0 + qq;
+      kbits_s[qq][g] = gi < n ? static_cast<uint8_t>(keep_byte(p.drop_t, p.seed_lo, p.seed_hi,
+                                                               bh, gi, (j0 >> 3) + g))
+                              : 0;
+    }
     if (tid < kBQ) {
       const int gi = q0 + tid;
       Ls[tid] = gi < n ? Lh[gi] * kLog2e : -INFINITY;
@@ -205,7 +223,14 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(BwdArgs a) {
         float dpv = 0.f;
         #pragma unroll 4
         for (int e = 0; e < v; ++e) dpv = fmaf(Vs[r * vp + e], dYs[qc * vp + e], dpv);
-        ds = pv * (dpv - Ds[qc]);
+        if (p.drop_t != 0) {
+          // Replayed mask: dV takes p xi s, and dP = xi s (G_i . V_j).
+          const float xs = ((kbits_s[qc][r >> 3] >> (r & 7)) & 1u) ? p.drop_scale : 0.f;
+          ds = pv * (dpv * xs - Ds[qc]);
+          pv *= xs;
+        } else {
+          ds = pv * (dpv - Ds[qc]);
+        }
       }
       Pt[r * (kBQ + 1) + qc] = pv;
       dSt[r * (kBQ + 1) + qc] = ds;

@@ -921,6 +921,7 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 bool tc_bwd_split_supported(const Problem& p) {
+  if (p.drop_t != 0) return false;  // dropout: SIMT kernels
   if (p.dtype != kBF16 || p.d != p.v || (p.d != 64 && p.d != 128)) return false;
   if (p.mask_kind == kMaskBitmask && p.n > kMaxBlocks * kBM) return false;
   return tmap_encoder_available();

@@ -559,6 +559,7 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, int width, int n, int BH) 
 bool tmap_encoder_available() { return encode_fn() != nullptr; }
 
 bool tc_fwd_supported(const Problem& p) {
+  if (p.drop_t != 0) return false;  // dropout: SIMT kernels
   if (p.dtype != kBF16 || p.d != p.v || (p.d != 64 && p.d != 128)) return false;
   if (!(p.scale > 0.f)) return false;
   if (p.mask_kind == kMaskBitmask && p.n > kMaxKT * kBN) return false;

@@ -129,6 +129,42 @@ int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void
              int window, const uint32_t* bitmask, void* dQ, void* dK, void* dV,
              void* workspace, size_t workspace_bytes, void* cuda_stream);
 
+/* ---------------------------------------------------------------------------
+ * Dropout with a replayed mask.
+ *
+ * "Exact tiled softmax attention with block-recomputed vector-Jacobian
+ * products", Reverse procedure: the base method has no dropout, and a dropout
+ * extension must replay the forward pass's realised mask in its reverse pass.
+ * Here the mask acts on the normalised probabilities:
+ *   Y_i = sum_j p_ij xi_ij s V_j,   s = 65536 / (65536 - t),
+ * with L_i the statistic of the undropped p (as in attn_fwd), and the reverse
+ * pass uses the same xi:  dV_j += p_ij xi_ij s G_i,  dP_ij = xi_ij s G_i.V_j,
+ * gamma_ij = p_ij (dP_ij - delta_i) with delta_i = G_i.Y_i.
+ *
+ * xi_ij is recomputed, never stored: key j of row i in slice bh = b*H + h is
+ * kept when u_ij >= t, where t = min(65535, floor(dropout_p * 65536 + 1/2))
+ * and u_ij is half (j % 2) (low half first) of word (j % 8) / 2 of the
+ * Philox-4x32-10 output (Salmon et al., "Parallel random numbers: as easy as
+ * 1, 2, 3", SC 2011) for counter (j / 8, i, bh, 0) and key (seed mod 2^32,
+ * seed / 2^32).  The realised drop rate is t / 65536.
+ *
+ * Arguments as attn_fwd / attn_bwd plus dropout_p in [0, 1) (otherwise
+ * EXATTN_INVALID_ARG) and the 64-bit seed; dropout_p = 0 is attn_fwd /
+ * attn_bwd exactly.  attn_bwd_dropout must get the dropout_p and seed of the
+ * attn_fwd_dropout call that produced Y and L.  Dropout runs on the tensor-core
+ * kernels where attn_fwd / attn_bwd would (the atomic dQ form excepted: with
+ * EXATTN_PATH_ATOMIC_DQ the reverse pass runs on the SIMT kernels).
+ * ------------------------------------------------------------------------- */
+int attn_fwd_dropout(const exattn_shape* shape, const void* Q, const void* K, const void* V,
+                     float scale, int mask_kind, int window, const uint32_t* bitmask,
+                     float dropout_p, uint64_t seed, void* Y, float* L, void* workspace,
+                     size_t workspace_bytes, void* cuda_stream);
+int attn_bwd_dropout(const exattn_shape* shape, const void* Q, const void* K, const void* V,
+                     const void* Y, const void* dY, const float* L, float scale, int mask_kind,
+                     int window, const uint32_t* bitmask, float dropout_p, uint64_t seed,
+                     void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
+                     void* cuda_stream);
+
 /* The reverse pass of attn_bwd for callers that cannot allocate device memory
  * and so cannot pass a workspace: for example a plugin whose host gives it only
  * its input and output buffers, or code that must not let a device allocation

@@ -24,11 +24,9 @@ import torch
 
 import workloads
 from oracle import dense, masks
+from tolerances import TOL, compare, half_ulp_bf16  # noqa: F401
 
 pytestmark = pytest.mark.gpu
-
-TOL = {"f32": dict(y=1e-5, g=1e-4, L=1e-4), "bf16": dict(y=1e-2, g=2e-2, L=1e-4)}
-
 
 @pytest.fixture(scope="module")
 def ex():
@@ -58,48 +56,6 @@ def run_gpu(ex, w, x, path="auto", self_attention=False, dy=None):
     finally:
         ex.set_path(prev)
     return dict(Y=y, L=L, dQ=dq, dK=dk, dV=dv)
-
-
-def half_ulp_bf16(x):
-    """Half the spacing of bf16 numbers at |x| (8 significant bits)."""
-    ax = np.abs(x)
-    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
-    return np.where(ax > 0, 2.0 ** (e - 8), 0.0)
-
-
-def compare(dtype, got, ref, heads=None):
-    """Assert the tolerance rules; got are torch tensors, ref numpy float64 arrays."""
-    tol = TOL[dtype]
-    errs = {}
-    gscale = max((float(np.abs(ref[k]).max()) for k in ("dQ", "dK", "dV") if k in ref),
-                 default=0.0)
-    for key in ("Y", "L", "dQ", "dK", "dV"):
-        if key not in ref:
-            continue
-        g = got[key]
-        if heads is not None:
-            g = g.reshape((-1,) + tuple(g.shape[2:]))[heads]
-        g = _np(g).reshape(ref[key].shape)
-        r = ref[key]
-        if key == "L":
-            fin = np.isfinite(r)
-            assert np.array_equal(np.isfinite(g), fin), "L finiteness differs"
-            err = float(np.abs(g[fin] - r[fin]).max()) if fin.any() else 0.0
-            bound = tol["L"]
-        elif key == "Y" and dtype == "bf16":
-            excess = np.abs(g - r) - half_ulp_bf16(r)
-            err = float(excess.max()) if excess.size else 0.0
-            bound = tol["y"]
-        elif key == "Y":
-            err = float(np.abs(g - r).max())
-            bound = tol["y"] * float(np.abs(r).max())
-        else:
-            err = float(np.abs(g - r).max())
-            bound = tol["g"] * max(float(np.abs(r).max()), 1e-3 * gscale)
-        assert np.isfinite(g).all() or key == "L", f"{key} has non-finite values"
-        errs[key] = (err, bound)
-        assert err <= bound, f"{key}: max abs err {err:.3e} > bound {bound:.3e}"
-    return errs
 
 
 def oracle_all(w, x, kind=None):
