@@ -143,8 +143,9 @@ class ClockSampler:
 # The oracle on the host cores (cpu_baseline and the reference arm)
 # --------------------------------------------------------------------------- #
 
-def oracle_sample_step(w, Q, K, V, G, rows):
+def oracle_sample_step(w, Q, K, V, G, rows, dropout=None):
     """Oracle forward + reverse over the last ``rows`` query rows of head 0.
+    ``dropout`` = (keep mask of those rows, keep scale) for the dropout forms.
 
     Returns the algorithmic flops of that sample (same convention as the GPU
     metric: 2 |A| (d+v) forward, 2.5x that reverse)."""
@@ -152,8 +153,13 @@ def oracle_sample_step(w, Q, K, V, G, rows):
     n = w.n
     r0 = n - rows
     allowed = masks.allowed_matrix(n, w.mask_kind, w.window, None)[r0:]
-    dense.head_forward(Q[r0:], K, V, w.scale, allowed)
-    dense.head_backward(Q[r0:], K, V, G[r0:], w.scale, allowed)
+    if dropout is None:
+        dense.head_forward(Q[r0:], K, V, w.scale, allowed)
+        dense.head_backward(Q[r0:], K, V, G[r0:], w.scale, allowed)
+    else:
+        keep, ks = dropout
+        dense.head_forward_dropout(Q[r0:], K, V, w.scale, allowed, keep, ks)
+        dense.head_backward_dropout(Q[r0:], K, V, G[r0:], w.scale, allowed, keep, ks)
     f = 2.0 * float(allowed.sum()) * (w.d + w.v)
     return 3.5 * f
 
@@ -162,11 +168,21 @@ def oracle_inputs(w, x):
     return tuple(t[0, 0].to(torch.float64).numpy() for t in (x.Q, x.K, x.V, x.dY))
 
 
-def cpu_baseline(w, x, budget_s=12.0, rows=512):
+def oracle_dropout(w, rows, q, seed):
+    """Keep mask of the last ``rows`` rows of head 0, and the keep scale."""
+    if not q:
+        return None
+    from oracle import philox
+    keep = philox.keep_mask(0, w.n, w.n, q, seed)[w.n - rows:]
+    return keep, philox.keep_scale(q)
+
+
+def cpu_baseline(w, x, budget_s=12.0, rows=512, q=0.0, seed=0):
     Q, K, V, G = oracle_inputs(w, x)
+    drop = oracle_dropout(w, rows, q, seed)
     done_flops, t0, samples = 0.0, time.perf_counter(), 0
     while True:
-        done_flops += oracle_sample_step(w, Q, K, V, G, rows)
+        done_flops += oracle_sample_step(w, Q, K, V, G, rows, drop)
         samples += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -191,12 +207,13 @@ def run_reference(args, w):
     x = workloads.make_inputs(w, heads=1)
     Q, K, V, G = oracle_inputs(w, x)
     rows = args.ref_rows
+    drop = oracle_dropout(w, rows, args.dropout, args.seed)
     for _ in range(args.warmup):
-        oracle_sample_step(w, Q, K, V, G, rows)
+        oracle_sample_step(w, Q, K, V, G, rows, drop)
     t0 = time.perf_counter()
     total = 0.0
     for _ in range(args.steps):
-        total += oracle_sample_step(w, Q, K, V, G, rows)
+        total += oracle_sample_step(w, Q, K, V, G, rows, drop)
     el = time.perf_counter() - t0
     value = total / el / 1e12
     line = {
@@ -205,7 +222,7 @@ def run_reference(args, w):
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d, "v": w.v,
-                   "mask": w.mask, "input_dtype": w.dtype,
+                   "mask": w.mask, "input_dtype": w.dtype, "dropout_p": args.dropout,
                    "step": f"oracle fwd+bwd of the last {rows} query rows of head 0"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(),
                          "kind": "oracle",
@@ -276,13 +293,15 @@ def run_gpu(args, w):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     stream = torch.cuda.current_stream(dev)
 
+    drop = dict(dropout_p=args.dropout, seed=args.seed)
+
     def step():
-        ex.fwd(q, k, v, w.scale, w.mask, w.window, bm, y=y, L=L, ws=ws_f, stream=stream)
+        ex.fwd(q, k, v, w.scale, w.mask, w.window, bm, y=y, L=L, ws=ws_f, stream=stream, **drop)
         ex.bwd(q, k, v, y, dy, L, w.scale, w.mask, w.window, bm, dq=dq, dk=dk, dv=dv, ws=ws_b,
-               stream=stream)
+               stream=stream, **drop)
 
     def fwd_only():
-        ex.fwd(q, k, v, w.scale, w.mask, w.window, bm, y=y, L=L, ws=ws_f, stream=stream)
+        ex.fwd(q, k, v, w.scale, w.mask, w.window, bm, y=y, L=L, ws=ws_f, stream=stream, **drop)
 
     def barrier():
         if dist is not None:
@@ -394,7 +413,7 @@ def run_gpu(args, w):
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d, "v": w.v,
                    "mask": w.mask, "window": w.window, "scale": w.scale,
-                   "kernel_path": args.path,
+                   "kernel_path": args.path, "dropout_p": args.dropout,
                    "l2": ("inputs larger than L2 (%d MB of Q, K, V, dY vs 129 MB), no flush"
                           % (sum(t.numel() * t.element_size() for t in (q, k, v, dy)) >> 20)),
                    "flops_per_step": f_fwd + f_bwd},
@@ -406,7 +425,8 @@ def run_gpu(args, w):
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_budget, q=args.dropout,
+                                            seed=args.seed)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -617,6 +637,9 @@ def main():
     ap.add_argument("--batch", type=int, default=None,
                     help="override the batch size (a smaller case of the same workload)")
     ap.add_argument("--heads", type=int, default=None, help="override the head count")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="drop probability (dropout with a replayed mask), default none")
+    ap.add_argument("--seed", type=int, default=1234, help="dropout seed")
     ap.add_argument("--decode", action="store_true",
                     help="time the split-KV decode forward instead (B=8, H=32, nk=16384)")
     ap.add_argument("--nq", type=int, default=1, help="queries per slice in --decode mode")

@@ -50,8 +50,10 @@ struct MaskView {
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t lo0 = c.x * 0xD2511F53u, hi0 = __umulhi(c.x, 0xD2511F53u);
-    const uint32_t lo1 = c.z * 0xCD9E8D57u, hi1 = __umulhi(c.z, 0xCD9E8D57u);
+    const uint64_t m0 = static_cast<uint64_t>(c.x) * 0xD2511F53u;  // one wide multiply each
+    const uint64_t m1 = static_cast<uint64_t>(c.z) * 0xCD9E8D57u;
+    const uint32_t lo0 = static_cast<uint32_t>(m0), hi0 = static_cast<uint32_t>(m0 >> 32);
+    const uint32_t lo1 = static_cast<uint32_t>(m1), hi1 = static_cast<uint32_t>(m1 >> 32);
     c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
@@ -79,6 +81,15 @@ __device__ __forceinline__ uint32_t keep_byte(uint32_t drop_t, uint32_t seed_lo,
          (static_cast<uint32_t>(w.z >= th) << 5) |
          (static_cast<uint32_t>((w.w & 0xFFFFu) >= drop_t) << 6) |
          (static_cast<uint32_t>(w.w >= th) << 7);
+}
+
+// The raw Philox words of keys 8*jb .. 8*jb+7 of row i in slice bh (key 8*jb + t
+// reads half t%2 of word t/2; see keep_byte).
+__device__ __forceinline__ uint4 keep_words(uint32_t seed_lo, uint32_t seed_hi, int bh, int i,
+                                            int jb) {
+  return philox4x32_10(make_uint4(static_cast<uint32_t>(jb), static_cast<uint32_t>(i),
+                                  static_cast<uint32_t>(bh), 0u),
+                       seed_lo, seed_hi);
 }
 
 template <typename T> struct Elem;

@@ -63,7 +63,33 @@ struct Bwd2Params {
   __nv_bfloat16* dK;
   __nv_bfloat16* dV;
   unsigned* status;
+  uint32_t drop_t, seed_lo, seed_hi;  // dropout (kernel variants kDrop only)
+  float drop_scale;
 };
+
+// 32 x 32 bit-matrix transpose across a warp: on return bit e of lane L is bit
+// L of lane e's input.  Five butterfly steps, each swapping the off-diagonal
+// j x j blocks of lane pairs (L, L ^ j).
+__device__ __forceinline__ uint32_t transpose_bits32(uint32_t x, int lane) {
+  constexpr uint32_t kM[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+    const int j = 16 >> k;
+    const uint32_t m = kM[k];
+    const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, x, j);
+    x = (lane & j) ? ((x & ~m) | ((y >> j) & m)) : ((x & m) | ((y & m) << j));
+  }
+  return x;
+}
+
+// Keep bits of keys j0 .. j0+31 (j0 a multiple of 8) of query row i: bit e is key j0 + e.
+__device__ __forceinline__ uint32_t keep_word32(const Bwd2Params& p, int bh, int i, int j0) {
+  uint32_t w = 0;
+#pragma unroll 1
+  for (int g = 0; g < 4; ++g)
+    w |= keep_byte(p.drop_t, p.seed_lo, p.seed_hi, bh, i, (j0 >> 3) + g) << (8 * g);
+  return w;
+}
 
 __device__ __forceinline__ uint32_t range_bits(int a, int b) {
   a = max(a, 0);
@@ -186,7 +212,7 @@ struct KvLayout {
   static_assert(TOTAL <= 232448, "shared memory");
 };
 
-template <int D, int V>
+template <int D, int V, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kv_kernel(const __grid_constant__ Bwd2Params p) {
   using Lay = KvLayout<D, V>;
@@ -401,6 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int cls = cls_of(qb);
       if (cls == kEmpty) continue;
       const int slot = it % NST;
+      // Dropout: lane e draws the keep bits of query q0 + 32g + e for this warp's
+      // 32 keys; the transpose gives each lane (key) its bits over the 32 queries.
+      uint32_t keep = 0xFFFFFFFFu;
+      if constexpr (kDrop)
+        keep = transpose_bits32(keep_word32(p, bh, qb * kBM + 32 * g + lane, k0 + wl * 32), lane);
       if (!(ok = mbar_wait(bar(Lay::B_SDP + h), it & 1, abort_flag))) break;
       tc_fence_after();
       const float* dvec = reinterpret_cast<const float*>(smem + Lay::VEC_OFF + slot * 1024);
@@ -455,8 +486,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u = 0; u < 4; ++u) {
             float pp = ex2(fmaf(__uint_as_float(s[e + u]), sl2, -la[u]));
             if (!((allow >> (16 * c + e + u)) & 1u)) pp = 0.f;
-            pv[u] = pp;
-            gv[u] = pp * (__uint_as_float(dp[e + u]) - da[u]);
+            if constexpr (kDrop) {
+              // Replayed mask: dV takes p xi s; dP = xi s (G_i . V_j).
+              const float xs = ((keep >> (16 * c + e + u)) & 1u) ? p.drop_scale : 0.f;
+              pv[u] = pp * xs;
+              gv[u] = pp * (__uint_as_float(dp[e + u]) * xs - da[u]);
+            } else {
+              pv[u] = pp;
+              gv[u] = pp * (__uint_as_float(dp[e + u]) - da[u]);
+            }
           }
           pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
           pk[e / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
@@ -544,7 +582,7 @@ struct QLayout {
   static_assert(TOTAL <= 232448, "shared memory");
 };
 
-template <int D, int V>
+template <int D, int V, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_q_kernel(const __grid_constant__ Bwd2Params p) {
   using Lay = QLayout<D, V>;
@@ -773,9 +811,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int kb = kb_begin; kb < kb_end; ++kb) {
       const int cls = cls_of(kb);
       if (cls == kEmpty) continue;
+      const int kc = kb * kBN + 32 * g;  // first key of this group
       if (!(ok = mbar_wait(bar(Lay::B_SDP), t & 1, abort_flag))) break;
       tc_fence_after();
-      const int kc = kb * kBN + 32 * g;  // first key of this group
       uint32_t allow = 0xFFFFFFFFu;
       if (cls == kPartial) {
         int lo = 0, hi = n - 1;
@@ -810,14 +848,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t (&s)[16] = sv[c];
         const uint32_t (&dp)[16] = dpv[c];
         uint32_t dk[8];
+        uint4 rw;  // dropout: Philox words of keys kc + 16c + 8*(e/8) .. of row i
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
           float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, -lse2));
           float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -lse2));
           if (!((allow >> (16 * c + e)) & 1u)) p0 = 0.f;
           if (!((allow >> (16 * c + e + 1)) & 1u)) p1 = 0.f;
-          dk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dl),
-                                  p1 * (__uint_as_float(dp[e + 1]) - dl));
+          float dp0 = __uint_as_float(dp[e]), dp1 = __uint_as_float(dp[e + 1]);
+          if constexpr (kDrop) {
+            // Replayed mask: dP = xi s (G_i . V_j); keys e, e+1 share one word.
+            if ((e & 7) == 0) rw = keep_words(p.seed_lo, p.seed_hi, bh, i, (kc + 16 * c + e) >> 3);
+            const int wi = (e & 7) >> 1;
+            const uint32_t w = wi == 0 ? rw.x : wi == 1 ? rw.y : wi == 2 ? rw.z : rw.w;
+            dp0 *= (w & 0xFFFFu) >= p.drop_t ? p.drop_scale : 0.f;
+            dp1 *= w >= (p.drop_t << 16) ? p.drop_scale : 0.f;
+          }
+          dk[e / 2] = pack_bf16x2(p0 * (dp0 - dl), p1 * (dp1 - dl));
         }
         tmem_st8(tD + 32 * g + 8 * c, dk);
       }
@@ -895,8 +942,13 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
   p.dK = static_cast<__nv_bfloat16*>(a.dK);
   p.dV = static_cast<__nv_bfloat16*>(a.dV);
   p.status = a.status;
-  auto kv = tc_bwd_kv_kernel<D, D>;
-  auto qk = tc_bwd_q_kernel<D, D>;
+  p.drop_t = pr.drop_t;
+  p.seed_lo = pr.seed_lo;
+  p.seed_hi = pr.seed_hi;
+  p.drop_scale = pr.drop_scale;
+  const bool drop = pr.drop_t != 0;
+  auto kv = drop ? tc_bwd_kv_kernel<D, D, true> : tc_bwd_kv_kernel<D, D, false>;
+  auto qk = drop ? tc_bwd_q_kernel<D, D, true> : tc_bwd_q_kernel<D, D, false>;
   cudaError_t e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        KvLayout<D, D>::TOTAL);
   if (e == cudaSuccess)
@@ -921,7 +973,6 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 bool tc_bwd_split_supported(const Problem& p) {
-  if (p.drop_t != 0) return false;  // dropout: SIMT kernels
   if (p.dtype != kBF16 || p.d != p.v || (p.d != 64 && p.d != 128)) return false;
   if (p.mask_kind == kMaskBitmask && p.n > kMaxBlocks * kBM) return false;
   return tmap_encoder_available();

@@ -61,6 +61,8 @@ struct FwdParams {
   __nv_bfloat16* Y;
   float* L;
   unsigned* status;
+  uint32_t drop_t, seed_lo, seed_hi;  // dropout (kernel variant kDrop only)
+  float drop_scale;
 };
 
 template <int D, int V>
@@ -130,7 +132,7 @@ __device__ __forceinline__ int classify(const FwdParams& p, const TileRows& t, i
   }
 }
 
-template <int D, int V>
+template <int D, int V, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
   using Lay = Layout<D, V>;
   constexpr int NS = Lay::NSLOT;
@@ -455,12 +457,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t pk[32];
+          uint4 rw;  // dropout: Philox words of keys kt*128 + 64*half + 8*(e/4) ..
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const float p0 = ex2(fmaf(__uint_as_float(s[64 * half + 2 * e]), sl2, neg));
             const float p1 = ex2(fmaf(__uint_as_float(s[64 * half + 2 * e + 1]), sl2, neg));
-            sum4[e & 3] += p0 + p1;
-            pk[e] = pack_bf16x2(p0, p1);
+            sum4[e & 3] += p0 + p1;  // the row sum is of the undropped p
+            if constexpr (kDrop) {
+              // Keys 2e and 2e+1 of this half are the low and high halves of one word.
+              if ((e & 3) == 0)
+                rw = keep_words(p.seed_lo, p.seed_hi, bh, i, kt * (kBN / 8) + 8 * half + e / 4);
+              const uint32_t w = (e & 3) == 0 ? rw.x : (e & 3) == 1 ? rw.y : (e & 3) == 2 ? rw.z : rw.w;
+              pk[e] = pack_bf16x2((w & 0xFFFFu) >= p.drop_t ? p0 : 0.f,
+                                  w >= (p.drop_t << 16) ? p1 : 0.f);
+            } else {
+              pk[e] = pack_bf16x2(p0, p1);
+            }
           }
           tmem_st32(t_s + 32 * half, pk);
         }
@@ -482,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         tc_fence_after();
       }
       const bool valid = i < n;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? (kDrop ? p.drop_scale : 1.f) / l : 0.f;
       __nv_bfloat16* yrow = p.Y + (static_cast<size_t>(bh) * n + (valid ? i : 0)) * V;
 #pragma unroll
       for (int ch = 0; ch < V / 32; ++ch) {
@@ -559,7 +571,6 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, int width, int n, int BH) 
 bool tmap_encoder_available() { return encode_fn() != nullptr; }
 
 bool tc_fwd_supported(const Problem& p) {
-  if (p.drop_t != 0) return false;  // dropout: SIMT kernels
   if (p.dtype != kBF16 || p.d != p.v || (p.d != 64 && p.d != 128)) return false;
   if (!(p.scale > 0.f)) return false;
   if (p.mask_kind == kMaskBitmask && p.n > kMaxKT * kBN) return false;
@@ -584,8 +595,12 @@ cudaError_t launch_tc_fwd_d(const FwdArgs& a, cudaStream_t s) {
   p.Y = static_cast<__nv_bfloat16*>(a.Y);
   p.L = a.L;
   p.status = a.status;
+  p.drop_t = pr.drop_t;
+  p.seed_lo = pr.seed_lo;
+  p.seed_hi = pr.seed_hi;
+  p.drop_scale = pr.drop_scale;
   using Lay = Layout<D, D>;
-  auto kern = tc_fwd_kernel<D, D>;
+  auto kern = pr.drop_t != 0 ? tc_fwd_kernel<D, D, true> : tc_fwd_kernel<D, D, false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC);
   if (e != cudaSuccess) {
