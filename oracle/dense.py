@@ -256,3 +256,27 @@ def backward_dropout(Q, K, V, G, c, mask_kind, window=0, bitmask=None, q=0.0, se
         res[2] = res[2].reshape(V.shape)
         res[3] = res[3].reshape(Q.shape[:-1])
     return tuple(res)
+
+
+def backward_rect(Q, K, V, G, c, mask_kind, window=0, bitmask=None):
+    """Reverse pass for nq queries against nk keys (``forward_rect``'s alignment):
+    -> (dQ [..,nq,d], dK [..,nk,d], dV [..,nk,v], delta [..,nq]).  Rows whose
+    allowed set is empty contribute nothing (dQ_i = 0, delta_i = 0)."""
+    from .masks import allowed_matrix_rect
+    nq, nk = Q.shape[-2], K.shape[-2]
+    allowed = allowed_matrix_rect(nq, nk, mask_kind, window, bitmask)
+    q, k, vv, g = _heads(Q), _heads(K), _heads(V), _heads(G)
+    rows = allowed.any(axis=1)
+    dQ = np.zeros_like(q)
+    dK = np.zeros_like(k)
+    dV = np.zeros_like(vv)
+    delta = np.zeros((q.shape[0], nq))
+    for h in range(q.shape[0]):
+        if rows.any():
+            a, b, cc, dl = head_backward(q[h][rows], k[h], vv[h], g[h][rows], c, allowed[rows])
+            dQ[h][rows] = a
+            dK[h] = b
+            dV[h] = cc
+            delta[h][rows] = dl
+    return (dQ.reshape(Q.shape), dK.reshape(K.shape), dV.reshape(V.shape),
+            delta.reshape(Q.shape[:-1]))

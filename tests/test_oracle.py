@@ -706,3 +706,78 @@ def test_batched_dropout_uses_each_heads_own_mask():
                                       philox.keep_scale(0.3))
     for a, b_ in zip(g, ref):
         assert np.array_equal(a[0], b_)
+
+
+# --------------------------------------------------------------------------- #
+# Cross-attention, nq != nk (queries aligned to the end of the keys)
+# --------------------------------------------------------------------------- #
+
+def test_rect_backward_equals_square_problem_with_leading_rows_silenced():
+    """The nq-query problem is the square nk problem whose first nk - nq rows
+    get a zero upstream gradient: same dK and dV, dQ of the last nq rows."""
+    r = _rng(41)
+    B, H, nk, nq, d, v = 1, 2, 40, 13, 5, 6
+    Q = r.normal(size=(B, H, nk, d))
+    K, V, G = r.normal(size=(B, H, nk, d)), r.normal(size=(B, H, nk, v)), r.normal(size=(B, H, nk, v))
+    Gz = G.copy()
+    Gz[:, :, : nk - nq] = 0.0
+    for kind, w in ((masks.NONE, 0), (masks.CAUSAL, 0), (masks.WINDOW, 7)):
+        dQ, dK, dV, _ = dense.backward(Q, K, V, Gz, 0.3, kind, w)
+        rq, rk, rv, rd = dense.backward_rect(Q[:, :, -nq:], K, V, G[:, :, -nq:], 0.3, kind, w)
+        assert _rel(rk, dK) <= 1e-13 and _rel(rv, dV) <= 1e-13
+        assert _rel(rq, dQ[:, :, -nq:]) <= 1e-13
+        Y, _ = dense.forward_rect(Q[:, :, -nq:], K, V, 0.3, kind, w)
+        assert _rel(rd, np.sum(G[:, :, -nq:] * Y, axis=-1)) <= 1e-12
+
+
+def test_rect_matches_torch_autograd_with_explicit_mask():
+    r = _rng(42)
+    nq, nk, d, v, c = 9, 23, 4, 3, 0.45
+    Q, K, V, G = (r.normal(size=s) for s in ((nq, d), (nk, d), (nk, v), (nq, v)))
+    for kind, w in ((masks.CAUSAL, 0), (masks.WINDOW, 5)):
+        allowed = masks.allowed_matrix_rect(nq, nk, kind, w)
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (Q, K, V))
+        y = torch.nn.functional.scaled_dot_product_attention(
+            tq[None], tk[None], tv[None], attn_mask=torch.tensor(allowed)[None], scale=c)[0]
+        y.backward(torch.tensor(G))
+        Y, L = dense.forward_rect(Q[None, None], K[None, None], V[None, None], c, kind, w)
+        dQ, dK, dV, _ = dense.backward_rect(Q[None, None], K[None, None], V[None, None],
+                                            G[None, None], c, kind, w)
+        assert _rel(Y[0, 0], y.detach().numpy()) <= 1e-13
+        assert _rel(dQ[0, 0], tq.grad.numpy()) <= 1e-12
+        assert _rel(dK[0, 0], tk.grad.numpy()) <= 1e-12
+        assert _rel(dV[0, 0], tv.grad.numpy()) <= 1e-12
+
+
+def test_rect_rows_before_every_key_are_empty_and_inert():
+    """nq > nk under the causal mask: the first nq - nk queries precede every key.
+    Their Y, dQ and delta are 0, L is -inf, and the other rows' gradients are
+    those of the problem without them."""
+    r = _rng(43)
+    nq, nk, d, v = 10, 6, 3, 4
+    Q, K, V, G = (r.normal(size=(1, 1) + s) for s in ((nq, d), (nk, d), (nk, v), (nq, v)))
+    Y, L = dense.forward_rect(Q, K, V, 0.5, masks.CAUSAL)
+    dQ, dK, dV, dl = dense.backward_rect(Q, K, V, G, 0.5, masks.CAUSAL)
+    e = nq - nk
+    assert np.all(Y[0, 0, :e] == 0) and np.all(np.isneginf(L[0, 0, :e]))
+    assert np.all(dQ[0, 0, :e] == 0) and np.all(dl[0, 0, :e] == 0)
+    sq = dense.backward(Q[:, :, e:], K, V, G[:, :, e:], 0.5, masks.CAUSAL)
+    assert _rel(dK, sq[1]) <= 1e-14 and _rel(dV, sq[2]) <= 1e-14
+    assert _rel(dQ[:, :, e:], sq[0]) <= 1e-14
+
+
+def test_rect_backward_finite_differences():
+    r = _rng(44)
+    nq, nk, d, v, c = 3, 5, 2, 3, 0.8
+    Q, K, V, G = (r.normal(size=(1, 1) + s) for s in ((nq, d), (nk, d), (nk, v), (nq, v)))
+    grads = dense.backward_rect(Q, K, V, G, c, masks.CAUSAL)
+    for which, X in enumerate((Q, K, V)):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            args = [Q.copy(), K.copy(), V.copy()]
+            args[which][idx] += 1e-6
+            yp = np.sum(G * dense.forward_rect(*args, c, masks.CAUSAL)[0])
+            args[which][idx] -= 2e-6
+            ym = np.sum(G * dense.forward_rect(*args, c, masks.CAUSAL)[0])
+            num[idx] = (yp - ym) / 2e-6
+        assert _rel(grads[which], num) <= 1e-5
