@@ -81,6 +81,16 @@ def load_library():
     lib.attn_bwd_dropout.argtypes = [sp, vp, vp, vp, vp, vp, vp, cf, ci, ci, vp, cf, u64, vp, vp,
                                      vp, vp, sz, vp]
     lib.attn_bwd_dropout.restype = ci
+    qsp = ctypes.POINTER(QKShape)
+    lib.exattn_fwd_qk_workspace_size.argtypes = [qsp, ci]
+    lib.exattn_fwd_qk_workspace_size.restype = sz
+    lib.exattn_bwd_qk_workspace_size.argtypes = [qsp, ci]
+    lib.exattn_bwd_qk_workspace_size.restype = sz
+    lib.attn_fwd_qk.argtypes = [qsp, vp, vp, vp, cf, ci, ci, vp, cf, u64, vp, vp, vp, sz, vp]
+    lib.attn_fwd_qk.restype = ci
+    lib.attn_bwd_qk.argtypes = [qsp, vp, vp, vp, vp, vp, vp, cf, ci, ci, vp, cf, u64, vp, vp, vp,
+                                vp, sz, vp]
+    lib.attn_bwd_qk.restype = ci
     lib.exattn_device_status.argtypes = [vp, vp]
     lib.exattn_device_status.restype = ci
     lib.exattn_status_string.argtypes = [ci]
@@ -156,15 +166,61 @@ def workspace(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
+def _qk_shape(q, k, v) -> QKShape:
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("expected [batch, heads, n, width] tensors")
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    B, H, nq, d = q.shape
+    return QKShape(B, H, nq, k.shape[2], d, v.shape[-1], _DTYPES[q.dtype])
+
+
+def _fwd_qk(lib, q, k, v, scale, kind, window, bitmask, y, L, ws, stream, dropout_p, seed):
+    shape = _qk_shape(q, k, v)
+    if y is None:
+        y = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    if L is None:
+        L = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(lib.exattn_fwd_qk_workspace_size(ctypes.byref(shape), kind), q.device)
+    st = lib.attn_fwd_qk(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale), kind,
+                         int(window), _ptr(bitmask), float(dropout_p), int(seed), _ptr(y),
+                         _ptr(L), _ptr(ws), ws.numel(), _stream(stream))
+    if st != 0:
+        raise ExattnError(st, "attn_fwd_qk")
+    return y, L
+
+
+def _bwd_qk(lib, q, k, v, y, dy, L, scale, kind, window, bitmask, dq, dk, dv, ws, stream,
+            dropout_p, seed):
+    shape = _qk_shape(q, k, v)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if ws is None:
+        ws = workspace(lib.exattn_bwd_qk_workspace_size(ctypes.byref(shape), kind), q.device)
+    st = lib.attn_bwd_qk(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(dy),
+                         _ptr(L), float(scale), kind, int(window), _ptr(bitmask),
+                         float(dropout_p), int(seed), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                         ws.numel(), _stream(stream))
+    if st != 0:
+        raise ExattnError(st, "attn_bwd_qk")
+    return dq, dk, dv
+
+
 def fwd(q, k, v, scale, mask="none", window=0, bitmask=None, y=None, L=None, ws=None,
         stream=None, dropout_p=0.0, seed=0):
-    """Forward pass -> (Y, L).  q, k [B,H,n,d], v [B,H,n,v]; bitmask int32/uint32 words.
-    ``dropout_p`` > 0 drops probabilities with the replayable mask of ``seed``
-    (attn_fwd_dropout); the reverse pass must get the same two values."""
+    """Forward pass -> (Y, L).  q [B,H,nq,d], k [B,H,nk,d], v [B,H,nk,v]; bitmask
+    int32/uint32 words.  nq != nk runs attn_fwd_qk (queries aligned to the end of
+    the keys).  ``dropout_p`` > 0 drops probabilities with the replayable mask of
+    ``seed``; the reverse pass must get the same two values."""
     lib = load_library()
-    shape = _shape(q, v)
     _check((k, v, y), q.dtype, q.device)
     kind = _mask_kind(mask)
+    if k.shape[2] != q.shape[2]:
+        return _fwd_qk(lib, q, k, v, scale, kind, window, bitmask, y, L, ws, stream, dropout_p,
+                       seed)
+    shape = _shape(q, v)
     if y is None:
         y = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
     if L is None:
@@ -190,9 +246,12 @@ def bwd(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, dq=None, 
     """Reverse pass -> (dQ, dK, dV) for the upstream gradient dy (with the forward
     pass's ``dropout_p`` and ``seed`` when it used dropout)."""
     lib = load_library()
-    shape = _shape(q, v)
     _check((k, v, y, dy, dq, dk, dv), q.dtype, q.device)
     kind = _mask_kind(mask)
+    if k.shape[2] != q.shape[2]:
+        return _bwd_qk(lib, q, k, v, y, dy, L, scale, kind, window, bitmask, dq, dk, dv, ws,
+                       stream, dropout_p, seed)
+    shape = _shape(q, v)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv

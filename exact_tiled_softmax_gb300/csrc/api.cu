@@ -24,16 +24,27 @@ constexpr int kMaxN = 1 << 20;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-int check_shape(const exattn_shape* s) {
-  if (!s) return EXATTN_INVALID_ARG;
-  if (s->batch < 1 || s->heads < 1 || s->n < 1 || s->d < 1 || s->v < 1)
+// Problem dimensions of either shape struct (nq == nk for exattn_shape).
+struct Dims {
+  int batch, heads, nq, nk, d, v, dtype;
+};
+Dims dims_of(const exattn_shape* s) { return {s->batch, s->heads, s->n, s->n, s->d, s->v, s->dtype}; }
+Dims dims_of(const exattn_qk_shape* s) {
+  return {s->batch, s->heads, s->nq, s->nk, s->d, s->v, s->dtype};
+}
+
+int check_dims(const Dims& s) {
+  if (s.batch < 1 || s.heads < 1 || s.nq < 1 || s.nk < 1 || s.d < 1 || s.v < 1)
     return EXATTN_INVALID_ARG;
-  if (s->dtype != EXATTN_F32 && s->dtype != EXATTN_BF16) return EXATTN_INVALID_ARG;
-  if (s->d > kMaxWidth || s->v > kMaxWidth || s->n > kMaxN) return EXATTN_UNSUPPORTED;
-  if ((long long)s->batch * s->heads > 65535) return EXATTN_UNSUPPORTED;
-  if (s->dtype == EXATTN_BF16 && (s->d % 8 != 0 || s->v % 8 != 0)) return EXATTN_UNSUPPORTED;
+  if (s.dtype != EXATTN_F32 && s.dtype != EXATTN_BF16) return EXATTN_INVALID_ARG;
+  if (s.d > kMaxWidth || s.v > kMaxWidth || s.nq > kMaxN || s.nk > kMaxN)
+    return EXATTN_UNSUPPORTED;
+  if ((long long)s.batch * s.heads > 65535) return EXATTN_UNSUPPORTED;
+  if (s.dtype == EXATTN_BF16 && (s.d % 8 != 0 || s.v % 8 != 0)) return EXATTN_UNSUPPORTED;
   return EXATTN_OK;
 }
+
+int check_shape(const exattn_shape* s) { return s ? check_dims(dims_of(s)) : EXATTN_INVALID_ARG; }
 
 int check_mask(int mask_kind, int window, const uint32_t* bitmask) {
   if (mask_kind < EXATTN_MASK_NONE || mask_kind > EXATTN_MASK_BITMASK) return EXATTN_INVALID_ARG;
@@ -46,18 +57,19 @@ int check_mask(int mask_kind, int window, const uint32_t* bitmask) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-Problem make_problem(const exattn_shape* s, float scale, int mask_kind, int window,
+Problem make_problem(const Dims& s, float scale, int mask_kind, int window,
                      const uint32_t* bitmask) {
   Problem p;
-  p.BH = s->batch * s->heads;
-  p.n = s->n;
-  p.d = s->d;
-  p.v = s->v;
-  p.dtype = s->dtype;
+  p.BH = s.batch * s.heads;
+  p.n = s.nq;
+  p.nk = s.nk;
+  p.d = s.d;
+  p.v = s.v;
+  p.dtype = s.dtype;
   p.scale = scale;
   p.mask_kind = mask_kind;
   p.window = mask_kind == EXATTN_MASK_WINDOW ? window : 0;
-  p.words_per_row = (s->n + 31) / 32;
+  p.words_per_row = (s.nk + 31) / 32;
   p.bitmask = mask_kind == EXATTN_MASK_BITMASK ? bitmask : nullptr;
   p.drop_t = 0;
   p.drop_scale = 1.f;
@@ -78,14 +90,18 @@ void set_dropout(Problem& p, float q, uint64_t seed) {
 }
 
 // Reverse-pass workspace: status word | delta [BH][npad] | lse2 [BH][npad] |
-// dQ accumulator [BH][n][d] (fp32), each part 256-byte aligned.
-size_t npad_of(const exattn_shape* s) { return ((size_t)s->n + 127) / 128 * 128; }
-size_t bwd_vec_bytes(const exattn_shape* s) {
-  return align_up(sizeof(float) * (size_t)s->batch * s->heads * npad_of(s), 256);
+// dQ accumulator [BH][nq][d] (fp32), each part 256-byte aligned (npad: nq
+// rounded up to 128).
+size_t npad_of(const Dims& s) { return ((size_t)s.nq + 127) / 128 * 128; }
+size_t bwd_vec_bytes(const Dims& s) {
+  return align_up(sizeof(float) * (size_t)s.batch * s.heads * npad_of(s), 256);
 }
 size_t bwd_delta_offset() { return kStatusBytes; }
-size_t bwd_lse2_offset(const exattn_shape* s) { return kStatusBytes + bwd_vec_bytes(s); }
-size_t bwd_dqacc_offset(const exattn_shape* s) { return kStatusBytes + 2 * bwd_vec_bytes(s); }
+size_t bwd_lse2_offset(const Dims& s) { return kStatusBytes + bwd_vec_bytes(s); }
+size_t bwd_dqacc_offset(const Dims& s) { return kStatusBytes + 2 * bwd_vec_bytes(s); }
+size_t bwd_ws_bytes(const Dims& s) {
+  return bwd_dqacc_offset(s) + sizeof(float) * (size_t)s.batch * s.heads * s.nq * s.d;
+}
 
 }  // namespace
 
@@ -148,16 +164,27 @@ size_t exattn_fwd_workspace_size(const exattn_shape* shape, int mask_kind) {
 size_t exattn_bwd_workspace_size(const exattn_shape* shape, int mask_kind) {
   if (check_shape(shape) != EXATTN_OK) return 0;
   (void)mask_kind;
-  return bwd_dqacc_offset(shape) +
-         sizeof(float) * (size_t)shape->batch * shape->heads * shape->n * shape->d;
+  return bwd_ws_bytes(dims_of(shape));
+}
+
+size_t exattn_fwd_qk_workspace_size(const exattn_qk_shape* shape, int mask_kind) {
+  if (!shape || check_dims(dims_of(shape)) != EXATTN_OK) return 0;
+  (void)mask_kind;
+  return kStatusBytes;
+}
+
+size_t exattn_bwd_qk_workspace_size(const exattn_qk_shape* shape, int mask_kind) {
+  if (!shape || check_dims(dims_of(shape)) != EXATTN_OK) return 0;
+  (void)mask_kind;
+  return bwd_ws_bytes(dims_of(shape));
 }
 
 namespace {
 
-int fwd_impl(const exattn_shape* shape, const void* Q, const void* K, const void* V, float scale,
+int fwd_impl(const Dims& dims, const void* Q, const void* K, const void* V, float scale,
              int mask_kind, int window, const uint32_t* bitmask, float dropout_p, uint64_t seed,
              void* Y, float* L, void* workspace, size_t workspace_bytes, void* cuda_stream) {
-  int st = check_shape(shape);
+  int st = check_dims(dims);
   if (st != EXATTN_OK) return st;
   st = check_mask(mask_kind, window, bitmask);
   if (st != EXATTN_OK) return st;
@@ -166,13 +193,12 @@ int fwd_impl(const exattn_shape* shape, const void* Q, const void* K, const void
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Y) || !aligned16(L))
     return EXATTN_MISALIGNED;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return EXATTN_MISALIGNED;
-  if (workspace_bytes < exattn_fwd_workspace_size(shape, mask_kind))
-    return EXATTN_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < kStatusBytes) return EXATTN_WORKSPACE_TOO_SMALL;
 
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   exattn::g_last_error[0] = 0;
   FwdArgs a;
-  a.p = make_problem(shape, scale, mask_kind, window, bitmask);
+  a.p = make_problem(dims, scale, mask_kind, window, bitmask);
   if (dropout_p > 0.f) set_dropout(a.p, dropout_p, seed);
   a.Q = Q;
   a.K = K;
@@ -187,11 +213,11 @@ int fwd_impl(const exattn_shape* shape, const void* Q, const void* K, const void
   return cuda_status(launch_simt_fwd(a, s), "attn_fwd: SIMT forward launch");
 }
 
-int bwd_impl(const exattn_shape* shape, const void* Q, const void* K, const void* V,
-             const void* Y, const void* dY, const float* L, float scale, int mask_kind,
-             int window, const uint32_t* bitmask, float dropout_p, uint64_t seed, void* dQ,
-             void* dK, void* dV, void* workspace, size_t workspace_bytes, void* cuda_stream) {
-  int st = check_shape(shape);
+int bwd_impl(const Dims& dims, const void* Q, const void* K, const void* V, const void* Y,
+             const void* dY, const float* L, float scale, int mask_kind, int window,
+             const uint32_t* bitmask, float dropout_p, uint64_t seed, void* dQ, void* dK,
+             void* dV, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  int st = check_dims(dims);
   if (st != EXATTN_OK) return st;
   st = check_mask(mask_kind, window, bitmask);
   if (st != EXATTN_OK) return st;
@@ -202,14 +228,13 @@ int bwd_impl(const exattn_shape* shape, const void* Q, const void* K, const void
       !aligned16(L) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
     return EXATTN_MISALIGNED;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return EXATTN_MISALIGNED;
-  if (workspace_bytes < exattn_bwd_workspace_size(shape, mask_kind))
-    return EXATTN_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < bwd_ws_bytes(dims)) return EXATTN_WORKSPACE_TOO_SMALL;
 
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   exattn::g_last_error[0] = 0;
   char* ws = static_cast<char*>(workspace);
   BwdArgs a;
-  a.p = make_problem(shape, scale, mask_kind, window, bitmask);
+  a.p = make_problem(dims, scale, mask_kind, window, bitmask);
   if (dropout_p > 0.f) set_dropout(a.p, dropout_p, seed);
   a.Q = Q;
   a.K = K;
@@ -221,10 +246,10 @@ int bwd_impl(const exattn_shape* shape, const void* Q, const void* K, const void
   a.dK = dK;
   a.dV = dV;
   a.status = reinterpret_cast<unsigned*>(ws);
-  a.npad = static_cast<int>(npad_of(shape));
+  a.npad = static_cast<int>(npad_of(dims));
   a.delta = reinterpret_cast<float*>(ws + bwd_delta_offset());
-  a.lse2 = reinterpret_cast<float*>(ws + bwd_lse2_offset(shape));
-  a.dQacc = reinterpret_cast<float*>(ws + bwd_dqacc_offset(shape));
+  a.lse2 = reinterpret_cast<float*>(ws + bwd_lse2_offset(dims));
+  a.dQacc = reinterpret_cast<float*>(ws + bwd_dqacc_offset(dims));
   const size_t acc_bytes = sizeof(float) * (size_t)a.p.BH * a.p.n * a.p.d;
   cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes, s);
   if (e != cudaSuccess) return cuda_status(e, "attn_bwd: clearing the status word");
@@ -252,24 +277,36 @@ int bwd_impl(const exattn_shape* shape, const void* Q, const void* K, const void
 int attn_fwd(const exattn_shape* shape, const void* Q, const void* K, const void* V,
              float scale, int mask_kind, int window, const uint32_t* bitmask, void* Y, float* L,
              void* workspace, size_t workspace_bytes, void* cuda_stream) {
-  return fwd_impl(shape, Q, K, V, scale, mask_kind, window, bitmask, 0.f, 0, Y, L, workspace,
-                  workspace_bytes, cuda_stream);
+  if (!shape) return EXATTN_INVALID_ARG;
+  return fwd_impl(dims_of(shape), Q, K, V, scale, mask_kind, window, bitmask, 0.f, 0, Y, L,
+                  workspace, workspace_bytes, cuda_stream);
 }
 
 int attn_fwd_dropout(const exattn_shape* shape, const void* Q, const void* K, const void* V,
                      float scale, int mask_kind, int window, const uint32_t* bitmask,
                      float dropout_p, uint64_t seed, void* Y, float* L, void* workspace,
                      size_t workspace_bytes, void* cuda_stream) {
-  return fwd_impl(shape, Q, K, V, scale, mask_kind, window, bitmask, dropout_p, seed, Y, L,
-                  workspace, workspace_bytes, cuda_stream);
+  if (!shape) return EXATTN_INVALID_ARG;
+  return fwd_impl(dims_of(shape), Q, K, V, scale, mask_kind, window, bitmask, dropout_p, seed, Y,
+                  L, workspace, workspace_bytes, cuda_stream);
+}
+
+int attn_fwd_qk(const exattn_qk_shape* shape, const void* Q, const void* K, const void* V,
+                float scale, int mask_kind, int window, const uint32_t* bitmask, float dropout_p,
+                uint64_t seed, void* Y, float* L, void* workspace, size_t workspace_bytes,
+                void* cuda_stream) {
+  if (!shape) return EXATTN_INVALID_ARG;
+  return fwd_impl(dims_of(shape), Q, K, V, scale, mask_kind, window, bitmask, dropout_p, seed, Y,
+                  L, workspace, workspace_bytes, cuda_stream);
 }
 
 int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void* V,
              const void* Y, const void* dY, const float* L, float scale, int mask_kind,
              int window, const uint32_t* bitmask, void* dQ, void* dK, void* dV, void* workspace,
              size_t workspace_bytes, void* cuda_stream) {
-  return bwd_impl(shape, Q, K, V, Y, dY, L, scale, mask_kind, window, bitmask, 0.f, 0, dQ, dK,
-                  dV, workspace, workspace_bytes, cuda_stream);
+  if (!shape) return EXATTN_INVALID_ARG;
+  return bwd_impl(dims_of(shape), Q, K, V, Y, dY, L, scale, mask_kind, window, bitmask, 0.f, 0,
+                  dQ, dK, dV, workspace, workspace_bytes, cuda_stream);
 }
 
 int attn_bwd_dropout(const exattn_shape* shape, const void* Q, const void* K, const void* V,
@@ -277,8 +314,18 @@ int attn_bwd_dropout(const exattn_shape* shape, const void* Q, const void* K, co
                      int window, const uint32_t* bitmask, float dropout_p, uint64_t seed,
                      void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
                      void* cuda_stream) {
-  return bwd_impl(shape, Q, K, V, Y, dY, L, scale, mask_kind, window, bitmask, dropout_p, seed,
-                  dQ, dK, dV, workspace, workspace_bytes, cuda_stream);
+  if (!shape) return EXATTN_INVALID_ARG;
+  return bwd_impl(dims_of(shape), Q, K, V, Y, dY, L, scale, mask_kind, window, bitmask,
+                  dropout_p, seed, dQ, dK, dV, workspace, workspace_bytes, cuda_stream);
+}
+
+int attn_bwd_qk(const exattn_qk_shape* shape, const void* Q, const void* K, const void* V,
+                const void* Y, const void* dY, const float* L, float scale, int mask_kind,
+                int window, const uint32_t* bitmask, float dropout_p, uint64_t seed, void* dQ,
+                void* dK, void* dV, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (!shape) return EXATTN_INVALID_ARG;
+  return bwd_impl(dims_of(shape), Q, K, V, Y, dY, L, scale, mask_kind, window, bitmask,
+                  dropout_p, seed, dQ, dK, dV, workspace, workspace_bytes, cuda_stream);
 }
 
 namespace {

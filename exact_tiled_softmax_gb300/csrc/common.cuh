@@ -22,19 +22,22 @@ __device__ __forceinline__ void raise_status(unsigned* status, unsigned bit) {
 }
 
 // Membership of key j in A_i ("Exact tiled softmax attention ...", Inputs),
-// for 0 <= i, j < n.  Keys j >= n do not exist and are never allowed.
+// for query row i and key j < nk; query i sits at absolute position i + off
+// (off = nk - nq).  Keys j >= nk do not exist and are never allowed.
 struct MaskView {
   int kind;
-  int n;
+  int nk;
+  int off;
   int window;
   int words_per_row;
   const uint32_t* bits;
 
   __device__ __forceinline__ bool allowed(int i, int j) const {
-    if (j >= n || j < 0) return false;
+    if (j >= nk || j < 0) return false;
+    const int a = i + off;
     switch (kind) {
-      case kMaskCausal: return j <= i;
-      case kMaskWindow: return j <= i && j > i - window;
+      case kMaskCausal: return j <= a;
+      case kMaskWindow: return j <= a && j > a - window;
       case kMaskBitmask:
         return (__ldg(bits + (size_t)i * words_per_row + (j >> 5)) >> (j & 31)) & 1u;
       default: return true;

@@ -11,9 +11,13 @@ namespace exattn {
 enum { kMaskNone = 0, kMaskCausal = 1, kMaskWindow = 2, kMaskBitmask = 3 };
 enum { kF32 = 0, kBF16 = 1 };
 
-// One attention problem: BH = batch*heads independent slices of [n][d|v].
+// One attention problem: BH = batch*heads independent slices; n query rows
+// against nk keys (nk == n for self-attention shapes).  Query i sits at
+// absolute position i + nk - n: the causal and window masks compare keys with
+// that position, and bit rows are [n][ceil(nk/32)].
 struct Problem {
   int BH, n, d, v, dtype;
+  int nk;
   float scale;
   int mask_kind, window, words_per_row;
   const uint32_t* bitmask;

@@ -18,13 +18,16 @@ constexpr int kBQ = 32;   // query rows per tile
 constexpr int kBK = 32;   // keys per tile (one bitmask word per row)
 constexpr int kThreads = 256;
 
-// Range of key tiles [kt0, kt1) that can intersect A_i for rows [i0, i1].
+// Range of key tiles [kt0, kt1) that can intersect A_i for rows [i0, i1]
+// (absolute positions i + nk - n).
 __device__ __forceinline__ void key_tile_range(const Problem& p, int i0, int i1, int& kt0,
                                                int& kt1) {
+  const int off = p.nk - p.n;
   kt0 = 0;
-  kt1 = (p.n + kBK - 1) / kBK;
-  if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) kt1 = i1 / kBK + 1;
-  if (p.mask_kind == kMaskWindow) kt0 = max(0, i0 - p.window + 1) / kBK;
+  kt1 = (p.nk + kBK - 1) / kBK;
+  if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow)
+    kt1 = i1 + off < 0 ? 0 : min(kt1, (i1 + off) / kBK + 1);
+  if (p.mask_kind == kMaskWindow) kt0 = max(0, i0 + off - p.window + 1) / kBK;
 }
 
 template <typename T>
@@ -40,7 +43,7 @@ __device__ __forceinline__ void load_tile(float* dst, int ld, const T* src, int 
 template <typename T, int VPT>
 __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
   const Problem p = a.p;
-  const int n = p.n, d = p.d, v = p.v, dp = d + 1;
+  const int n = p.n, nk = p.nk, d = p.d, v = p.v, dp = d + 1;
   extern __shared__ float smem[];
   float* Qs = smem;
   float* Ks = Qs + kBQ * dp;
@@ -51,9 +54,9 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
   const int tid = threadIdx.x, r = tid >> 3, l8 = tid & 7;
   const int i = q0 + r;
   const T* Qh = static_cast<const T*>(a.Q) + (size_t)bh * n * d;
-  const T* Kh = static_cast<const T*>(a.K) + (size_t)bh * n * d;
-  const T* Vh = static_cast<const T*>(a.V) + (size_t)bh * n * v;
-  MaskView mask{p.mask_kind, n, p.window, p.words_per_row, p.bitmask};
+  const T* Kh = static_cast<const T*>(a.K) + (size_t)bh * nk * d;
+  const T* Vh = static_cast<const T*>(a.V) + (size_t)bh * nk * v;
+  MaskView mask{p.mask_kind, nk, nk - n, p.window, p.words_per_row, p.bitmask};
 
   load_tile(Qs, dp, Qh, q0, kBQ, n, d);
   const float sl2 = p.scale * kLog2e;
@@ -74,8 +77,8 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
       if (!__syncthreads_or(any)) continue;
     }
     __syncthreads();
-    load_tile(Ks, dp, Kh, j0, kBK, n, d);
-    load_tile(Vs, v, Vh, j0, kBK, n, v);
+    load_tile(Ks, dp, Kh, j0, kBK, nk, d);
+    load_tile(Vs, v, Vh, j0, kBK, nk, v);
     __syncthreads();
 
     // Dropout keep bits of this row for the tile's four 8-key groups: lane l8 < 4
@@ -149,7 +152,8 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
 template <typename T, int DPT, int VPT>
 __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(BwdArgs a) {
   const Problem p = a.p;
-  const int n = p.n, d = p.d, v = p.v, dp = d + 1, vp = v + 1;
+  const int n = p.n, nk = p.nk, d = p.d, v = p.v, dp = d + 1, vp = v + 1;
+  const int off = nk - n;
   extern __shared__ float smem[];
   float* Ks = smem;
   float* Vs = Ks + kBK * dp;
@@ -165,28 +169,31 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(BwdArgs a) {
   const int tid = threadIdx.x, r = tid >> 3, l8 = tid & 7;
   const int j = j0 + r;
   const T* Qh = static_cast<const T*>(a.Q) + (size_t)bh * n * d;
-  const T* Kh = static_cast<const T*>(a.K) + (size_t)bh * n * d;
-  const T* Vh = static_cast<const T*>(a.V) + (size_t)bh * n * v;
+  const T* Kh = static_cast<const T*>(a.K) + (size_t)bh * nk * d;
+  const T* Vh = static_cast<const T*>(a.V) + (size_t)bh * nk * v;
   const T* dYh = static_cast<const T*>(a.dY) + (size_t)bh * n * v;
   const float* Lh = a.L + (size_t)bh * n;
   const float* Dh = a.delta + (size_t)bh * a.npad;
   float* dQh = a.dQacc + (size_t)bh * n * d;
-  MaskView mask{p.mask_kind, n, p.window, p.words_per_row, p.bitmask};
+  MaskView mask{p.mask_kind, nk, off, p.window, p.words_per_row, p.bitmask};
   const float c = p.scale, sl2 = p.scale * kLog2e;
 
-  load_tile(Ks, dp, Kh, j0, kBK, n, d);
-  load_tile(Vs, vp, Vh, j0, kBK, n, v);
+  load_tile(Ks, dp, Kh, j0, kBK, nk, d);
+  load_tile(Vs, vp, Vh, j0, kBK, nk, v);
   float dk[DPT], dv[VPT];
 #pragma unroll
   for (int t = 0; t < DPT; ++t) dk[t] = 0.f;
 #pragma unroll
   for (int t = 0; t < VPT; ++t) dv[t] = 0.f;
 
-  // Query tiles whose rows can allow a key of [j0, j1].
-  const int j1 = min(j0 + kBK, n) - 1;
+  // Query tiles whose rows can allow a key of [j0, j1] (row i is at i + off).
+  const int j1 = min(j0 + kBK, nk) - 1;
   int qt0 = 0, qt1 = (n + kBQ - 1) / kBQ;
-  if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) qt0 = j0 / kBQ;
-  if (p.mask_kind == kMaskWindow) qt1 = min(qt1, (j1 + p.window - 1) / kBQ + 1);
+  if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) qt0 = max(0, j0 - off) / kBQ;
+  if (p.mask_kind == kMaskWindow) {
+    const int last = j1 - off + p.window - 1;  // last row whose window reaches j1
+    qt1 = last < 0 ? 0 : min(qt1, last / kBQ + 1);
+  }
 
   for (int qt = qt0; qt < qt1; ++qt) {
     const int q0 = qt * kBQ;
@@ -215,7 +222,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(BwdArgs a) {
     for (int t = 0; t < 4; ++t) {
       const int qc = l8 + 8 * t, gi = q0 + qc;
       float pv = 0.f, ds = 0.f;
-      if (gi < n && j < n && Ls[qc] != -INFINITY && mask.allowed(gi, j)) {
+      if (gi < n && j < nk && Ls[qc] != -INFINITY && mask.allowed(gi, j)) {
         float acc = 0.f;
         #pragma unroll 4
         for (int e = 0; e < d; ++e) acc = fmaf(Ks[r * dp + e], Qs[qc * dp + e], acc);
@@ -272,9 +279,9 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(BwdArgs a) {
     }
   }
 
-  if (j < n) {
-    T* dKr = static_cast<T*>(a.dK) + ((size_t)bh * n + j) * d;
-    T* dVr = static_cast<T*>(a.dV) + ((size_t)bh * n + j) * v;
+  if (j < nk) {
+    T* dKr = static_cast<T*>(a.dK) + ((size_t)bh * nk + j) * d;
+    T* dVr = static_cast<T*>(a.dV) + ((size_t)bh * nk + j) * v;
 #pragma unroll
     for (int t = 0; t < DPT; ++t)
       if (l8 + 8 * t < d) Elem<T>::store(dKr + l8 + 8 * t, c * dk[t]);
@@ -394,7 +401,7 @@ cudaError_t bwd_launch_t(const BwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((p.n + kBK - 1) / kBK, p.BH);
+  dim3 grid((p.nk + kBK - 1) / kBK, p.BH);
   before_launch(kKernBwd, s);
   kern<<<grid, kThreads, smem, s>>>(a);
   after_launch(kKernBwd, s);

@@ -534,6 +534,7 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t s) {
 
 bool tc_bwd_supported(const Problem& p) {
   if (p.drop_t != 0) return false;  // dropout: SIMT kernels
+  if (p.nk != p.n) return false;    // nq != nk: SIMT kernels
   if (p.dtype != kBF16 || p.d != p.v || (p.d != 64 && p.d != 128)) return false;
   if (p.mask_kind == kMaskBitmask && p.n > kMaxQB * kBM) return false;
   return tmap_encoder_available();

@@ -54,6 +54,7 @@ enum : int { kEmpty = 0, kFull = 1, kPartial = 2 };
 struct Bwd2Params {
   CUtensorMap tq, tk, tv, tdy;
   int n, npad, BH, mask_kind, window, words_per_row;
+  int nk, off;  // keys, and the absolute position of query 0 (nk - n)
   const uint32_t* bits;
   const float* delta;  // [BH][npad]
   const float* lse2;   // [BH][npad]  L log2(e), +inf on padding / empty rows
@@ -105,12 +106,11 @@ __device__ __forceinline__ uint32_t range_bits(int a, int b) {
 // loop dimension).
 __device__ __forceinline__ int classify_tile(const Bwd2Params& p, int qb, int kb, bool any_bit,
                                              bool notall_bit) {
-  const int n = p.n;
   const int k0 = kb * kBN;
-  const bool key_tail = k0 + kBN > n;
-  const int k1 = min(k0 + kBN, n) - 1;
-  const int q0 = qb * kBM;
-  const int q1 = min(q0 + kBM, n) - 1;
+  const bool key_tail = k0 + kBN > p.nk;
+  const int k1 = min(k0 + kBN, p.nk) - 1;
+  const int q0 = qb * kBM + p.off;                  // absolute positions of the
+  const int q1 = min(qb * kBM + kBM, p.n) - 1 + p.off;  // block's first and last rows
   switch (p.mask_kind) {
     case kMaskCausal:
       if (q1 < k0) return kEmpty;
@@ -153,7 +153,7 @@ __device__ void build_bitmask_table(const Bwd2Params& p, bool key_major, int fix
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int w = fixed * 4 + q;
-          const uint32_t valid = range_bits(0, n - 1 - 32 * w);
+          const uint32_t valid = range_bits(0, p.nk - 1 - 32 * w);
           const uint32_t word = w < p.words_per_row ? __ldg(row + w) & valid : 0u;
           any |= word != 0u;
           all &= word == valid;
@@ -177,7 +177,7 @@ __device__ void build_bitmask_table(const Bwd2Params& p, bool key_major, int fix
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int w = t * 4 + q;
-        const uint32_t valid = range_bits(0, n - 1 - 32 * w);
+        const uint32_t valid = range_bits(0, p.nk - 1 - 32 * w);
         const uint32_t word = w < p.words_per_row ? __ldg(row + w) & valid : 0u;
         any |= word != 0u;
         all &= word == valid;
@@ -229,13 +229,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kb = blockIdx.x;  // causal: low key blocks have the most query blocks
   const int bh = blockIdx.y;
-  const int n = p.n;
+  const int n = p.n, nk = p.nk, off = p.off;
   const int k0 = kb * kBN;
   const int nqb = (n + kBM - 1) / kBM;
   int qb_begin = 0, qb_end = nqb;
-  if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) qb_begin = kb;
-  if (p.mask_kind == kMaskWindow)
-    qb_end = min(nqb, (min(k0 + kBN, n) - 1 + p.window - 1) / kBM + 1);
+  // Query rows that can reach this key block (row i sits at i + off).
+  if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow)
+    qb_begin = min(nqb, max(0, k0 - off) / kBM);
+  if (p.mask_kind == kMaskWindow) {
+    const int last = min(k0 + kBN, nk) - 1 - off + p.window - 1;
+    qb_end = last < 0 ? 0 : min(nqb, last / kBM + 1);
+  }
 
   if ((sbase & 1023u) != 0u) {
     if (threadIdx.x == 0) raise_status(p.status, kStatusTimeout);
@@ -440,12 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int cb = 32 * g;
       uint32_t allow = 0xFFFFFFFFu;
       if (cls == kPartial) {
-        if (j >= n) {
+        if (j >= nk) {
           allow = 0u;
         } else if (p.mask_kind == kMaskCausal) {
-          allow = range_bits(j - q0 - cb, 31);
+          allow = range_bits(j - off - q0 - cb, 31);
         } else if (p.mask_kind == kMaskWindow) {
-          allow = range_bits(j - q0 - cb, j + p.window - 1 - q0 - cb);
+          allow = range_bits(j - off - q0 - cb, j - off + p.window - 1 - q0 - cb);
         } else if (p.mask_kind == kMaskBitmask) {
           allow = 0u;
           const uint32_t* col = p.bits + (j >> 5);
@@ -525,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tsrc = (g == 0 ? tdV : tdK) + lane_off;
       const float mul = g == 0 ? 1.f : p.scale;
       __nv_bfloat16* dst =
-          (g == 0 ? p.dV : p.dK) + (static_cast<size_t>(bh) * n + (j < n ? j : 0)) * W;
+          (g == 0 ? p.dV : p.dK) + (static_cast<size_t>(bh) * nk + (j < nk ? j : 0)) * W;
       for (int ch = 0; ch < W / 16; ++ch) {
         uint32_t o[16];
         if (have) {
@@ -536,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) o[e] = 0u;
         }
-        if (j < n) {
+        if (j < nk) {
           uint32_t ov[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e)
@@ -603,10 +607,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = p.n;
   const int q0 = qb * kBM;
   const int q1 = min(q0 + kBM, n) - 1;
-  const int nkb = (n + kBN - 1) / kBN;
+  const int nk = p.nk, off = p.off;
+  const int nkb = (nk + kBN - 1) / kBN;
   int kb_begin = 0, kb_end = nkb;
-  if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) kb_end = min(nkb, q1 / kBN + 1);
-  if (p.mask_kind == kMaskWindow) kb_begin = max(0, q0 - p.window + 1) / kBN;
+  // Key blocks that rows q0..q1 (at absolute positions q0 + off ..) can reach.
+  if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow)
+    kb_end = q1 + off < 0 ? 0 : min(nkb, (q1 + off) / kBN + 1);
+  if (p.mask_kind == kMaskWindow) kb_begin = min(kb_end, max(0, q0 + off - p.window + 1) / kBN);
 
   if ((sbase & 1023u) != 0u) {
     if (threadIdx.x == 0) raise_status(p.status, kStatusTimeout);
@@ -816,9 +823,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t allow = 0xFFFFFFFFu;
       if (cls == kPartial) {
-        int lo = 0, hi = n - 1;
-        if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) hi = min(hi, i);
-        if (p.mask_kind == kMaskWindow) lo = max(lo, i - p.window + 1);
+        int lo = 0, hi = nk - 1;
+        if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) hi = min(hi, i + off);
+        if (p.mask_kind == kMaskWindow) lo = max(lo, i + off - p.window + 1);
         allow = range_bits(lo - kc, hi - kc);
         if (p.mask_kind == kMaskBitmask) {
           const int w = kb * 4 + g;
@@ -923,11 +930,13 @@ template <int D>
 cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
   const Problem& pr = a.p;
   Bwd2Params p;
-  if (!make_tmap_bf16(&p.tq, a.Q, D, pr.n, pr.BH) || !make_tmap_bf16(&p.tk, a.K, D, pr.n, pr.BH) ||
-      !make_tmap_bf16(&p.tv, a.V, D, pr.n, pr.BH) ||
+  if (!make_tmap_bf16(&p.tq, a.Q, D, pr.n, pr.BH) || !make_tmap_bf16(&p.tk, a.K, D, pr.nk, pr.BH) ||
+      !make_tmap_bf16(&p.tv, a.V, D, pr.nk, pr.BH) ||
       !make_tmap_bf16(&p.tdy, a.dY, D, pr.n, pr.BH))
     return cudaErrorInvalidValue;
   p.n = pr.n;
+  p.nk = pr.nk;
+  p.off = pr.nk - pr.n;
   p.npad = a.npad;
   p.BH = pr.BH;
   p.mask_kind = pr.mask_kind;
@@ -957,13 +966,13 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
     record_error("tc_bwd2: cudaFuncSetAttribute", static_cast<int>(e), cudaGetErrorString(e));
     return e;
   }
-  const int nb = (pr.n + kBN - 1) / kBN;
+  const int nkb = (pr.nk + kBN - 1) / kBN, nqb = (pr.n + kBM - 1) / kBM;
   before_launch(kKernBwd, s);
-  kv<<<dim3(nb, pr.BH), kThreads, KvLayout<D, D>::TOTAL, s>>>(p);
+  kv<<<dim3(nkb, pr.BH), kThreads, KvLayout<D, D>::TOTAL, s>>>(p);
   e = cudaGetLastError();
   if (e == cudaSuccess) {
     before_launch(kKernBwdQ, s);
-    qk<<<dim3(nb, pr.BH), kThreads, QLayout<D, D>::TOTAL, s>>>(p);
+    qk<<<dim3(nqb, pr.BH), kThreads, QLayout<D, D>::TOTAL, s>>>(p);
     e = cudaGetLastError();
   }
   after_launch(kKernBwd, s);
@@ -974,7 +983,8 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
 
 bool tc_bwd_split_supported(const Problem& p) {
   if (p.dtype != kBF16 || p.d != p.v || (p.d != 64 && p.d != 128)) return false;
-  if (p.mask_kind == kMaskBitmask && p.n > kMaxBlocks * kBM) return false;
+  if (p.mask_kind == kMaskBitmask && (p.n > kMaxBlocks * kBM || p.nk > kMaxBlocks * kBN))
+    return false;
   return tmap_encoder_available();
 }
 

@@ -56,6 +56,7 @@ enum : int { kEmpty = 0, kFull = 1, kPartial = 2 };
 struct FwdParams {
   CUtensorMap tq, tk, tv;
   int n, BH, n_qblocks, mask_kind, window, words_per_row;
+  int nk, off;  // keys, and the absolute position of query 0 (nk - n)
   const uint32_t* bits;
   float sl2;  // scale * log2(e), > 0
   __nv_bfloat16* Y;
@@ -113,15 +114,16 @@ __device__ __forceinline__ int classify(const FwdParams& p, const TileRows& t, i
                                         const uint32_t* any, const uint32_t* all) {
   if (!t.valid) return kEmpty;
   const int k0 = kt * kBN;
-  const bool tail = k0 + kBN > p.n;
-  const int k1 = min(k0 + kBN, p.n) - 1;
+  const bool tail = k0 + kBN > p.nk;
+  const int k1 = min(k0 + kBN, p.nk) - 1;
+  const int a0 = t.r0 + p.off, a1 = t.r1 + p.off;  // absolute positions of the rows
   switch (p.mask_kind) {
     case kMaskCausal:
-      if (k0 > t.r1) return kEmpty;
-      return (k0 + kBN - 1 <= t.r0 && !tail) ? kFull : kPartial;
+      if (k0 > a1) return kEmpty;
+      return (k0 + kBN - 1 <= a0 && !tail) ? kFull : kPartial;
     case kMaskWindow:
-      if (k0 > t.r1 || k1 <= t.r0 - p.window) return kEmpty;
-      return (k0 + kBN - 1 <= t.r0 && k0 >= t.r1 - p.window + 1 && !tail) ? kFull : kPartial;
+      if (k0 > a1 || k1 <= a0 - p.window) return kEmpty;
+      return (k0 + kBN - 1 <= a0 && k0 >= a1 - p.window + 1 && !tail) ? kFull : kPartial;
     case kMaskBitmask: {
       const int w = X * (kMaxKT / 32) + (kt >> 5);
       if (!((any[w] >> (kt & 31)) & 1u)) return kEmpty;
@@ -160,13 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     rows[X].r1 = min(q0 + X * kBM + kBM, n) - 1;
     rows[X].valid = rows[X].r0 < n;
   }
-  const int nkt = (n + kBN - 1) / kBN;
+  const int nk = p.nk;
+  const int nkt = (nk + kBN - 1) / kBN;
   int kt_begin = 0, kt_end = nkt;
   {
-    const int rlast = rows[1].valid ? rows[1].r1 : rows[0].r1;
+    const int alast = (rows[1].valid ? rows[1].r1 : rows[0].r1) + p.off;
     if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow)
-      kt_end = min(nkt, rlast / kBN + 1);
-    if (p.mask_kind == kMaskWindow) kt_begin = max(0, rows[0].r0 - p.window + 1) / kBN;
+      kt_end = alast < 0 ? 0 : min(nkt, alast / kBN + 1);
+    if (p.mask_kind == kMaskWindow) kt_begin = max(0, rows[0].r0 + p.off - p.window + 1) / kBN;
   }
 
   if (threadIdx.x == 0) {
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int w = kt * 4 + q;
-          const uint32_t valid = range_bits(0, n - 1 - 32 * w);
+          const uint32_t valid = range_bits(0, nk - 1 - 32 * w);
           const uint32_t word = w < p.words_per_row ? __ldg(row + w) & valid : 0u;
           any |= word != 0u;
           all &= word == valid;
@@ -408,9 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         if (c == kPartial) {
           // Allowed keys of row i in this block as four 32-bit words.
           const int k0 = kt * kBN;
-          int lo = 0, hi = n - 1;
-          if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) hi = min(hi, i);
-          if (p.mask_kind == kMaskWindow) lo = max(lo, i - p.window + 1);
+          int lo = 0, hi = nk - 1;
+          const int ia = i + p.off;  // absolute position of row i
+          if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) hi = min(hi, ia);
+          if (p.mask_kind == kMaskWindow) lo = max(lo, ia - p.window + 1);
           uint32_t mw[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -573,7 +577,7 @@ bool tmap_encoder_available() { return encode_fn() != nullptr; }
 bool tc_fwd_supported(const Problem& p) {
   if (p.dtype != kBF16 || p.d != p.v || (p.d != 64 && p.d != 128)) return false;
   if (!(p.scale > 0.f)) return false;
-  if (p.mask_kind == kMaskBitmask && p.n > kMaxKT * kBN) return false;
+  if (p.mask_kind == kMaskBitmask && p.nk > kMaxKT * kBN) return false;
   return encode_fn() != nullptr;
 }
 
@@ -581,10 +585,12 @@ template <int D>
 cudaError_t launch_tc_fwd_d(const FwdArgs& a, cudaStream_t s) {
   const Problem& pr = a.p;
   FwdParams p;
-  if (!make_tmap_bf16(&p.tq, a.Q, D, pr.n, pr.BH) || !make_tmap_bf16(&p.tk, a.K, D, pr.n, pr.BH) ||
-      !make_tmap_bf16(&p.tv, a.V, D, pr.n, pr.BH))
+  if (!make_tmap_bf16(&p.tq, a.Q, D, pr.n, pr.BH) || !make_tmap_bf16(&p.tk, a.K, D, pr.nk, pr.BH) ||
+      !make_tmap_bf16(&p.tv, a.V, D, pr.nk, pr.BH))
     return cudaErrorInvalidValue;
   p.n = pr.n;
+  p.nk = pr.nk;
+  p.off = pr.nk - pr.n;
   p.BH = pr.BH;
   p.n_qblocks = (pr.n + 2 * kBM - 1) / (2 * kBM);
   p.mask_kind = pr.mask_kind;

@@ -233,6 +233,39 @@ int attn_fwd_splitkv(const exattn_qk_shape* shape, const void* Q, const void* K,
                      int num_splits, void* Y, float* L, void* workspace, size_t workspace_bytes,
                      void* cuda_stream);
 
+/* ---------------------------------------------------------------------------
+ * Cross-attention: nq query rows against nk keys.
+ *
+ * The method of "Exact tiled softmax attention with block-recomputed vector-
+ * Jacobian products" (Inputs: allowed-key sets A_i of keys per query row)
+ * does not need nq == nk; "What Ordinary Autograd Saves" (The implementation
+ * under test) keeps separate query and key lengths.  Here query i sits at
+ * absolute position i + nk - nq (the queries are the last nq positions), so
+ * CAUSAL allows j <= i + nk - nq, WINDOW w the w keys ending there, and
+ * BITMASK reads bit rows [nq][ceil(nk/32)].  With nq > nk the first nq - nk
+ * queries precede every key: under CAUSAL their allowed sets are empty (Y_i =
+ * 0, L_i = -inf, dQ_i = 0, status EXATTN_EMPTY_ROW).
+ *
+ * Shapes: Q, dQ [B][H][nq][d]; K, dK [B][H][nk][d]; V, dV [B][H][nk][v];
+ * Y, dY [B][H][nq][v]; L float32 [B][H][nq].  Limits as for attn_fwd, for nq
+ * and nk alike.  dropout_p and seed as for attn_fwd_dropout (0: none; keep
+ * decisions are indexed by the query row i and key j).  The workspace queries
+ * follow attn_fwd / attn_bwd (the reverse workspace grows with nq).  With nq ==
+ * nk these calls are attn_fwd_dropout / attn_bwd_dropout.  The atomic dQ form
+ * does not take nq != nk: with EXATTN_PATH_ATOMIC_DQ the reverse pass of such
+ * a shape runs on the SIMT kernels.
+ * ------------------------------------------------------------------------- */
+size_t exattn_fwd_qk_workspace_size(const exattn_qk_shape* shape, int mask_kind);
+size_t exattn_bwd_qk_workspace_size(const exattn_qk_shape* shape, int mask_kind);
+int attn_fwd_qk(const exattn_qk_shape* shape, const void* Q, const void* K, const void* V,
+                float scale, int mask_kind, int window, const uint32_t* bitmask, float dropout_p,
+                uint64_t seed, void* Y, float* L, void* workspace, size_t workspace_bytes,
+                void* cuda_stream);
+int attn_bwd_qk(const exattn_qk_shape* shape, const void* Q, const void* K, const void* V,
+                const void* Y, const void* dY, const float* L, float scale, int mask_kind,
+                int window, const uint32_t* bitmask, float dropout_p, uint64_t seed, void* dQ,
+                void* dK, void* dV, void* workspace, size_t workspace_bytes, void* cuda_stream);
+
 /* Waits for `cuda_stream`, then reads the status word of `workspace` (the
  * workspace of the last call queued on it).  Returns EXATTN_OK,
  * EXATTN_EMPTY_ROW, EXATTN_TIMEOUT or EXATTN_CUDA_ERROR. */

@@ -138,11 +138,18 @@ def row_forward(Q, K, V, c, allowed_row, i):
     return (e @ V) / l, m + np.log(l)
 
 
-def forward_rect(Q, K, V, c, mask_kind, window=0, bitmask=None):
+def _rect_keep(h, nq, nk, dropout):
+    from .philox import keep_mask, keep_scale
+    q, seed = dropout
+    return keep_mask(h, nq, nk, q, seed), keep_scale(q)
+
+
+def forward_rect(Q, K, V, c, mask_kind, window=0, bitmask=None, dropout=None):
     """Forward for nq queries against nk keys ([B,H,nq,d], [B,H,nk,d], [B,H,nk,v]),
     queries aligned to the end of the keys (masks.allowed_matrix_rect).
     Rows whose allowed set is empty get Y_i = 0 and L_i = -inf (the library's
-    convention for inputs outside the method's domain)."""
+    convention for inputs outside the method's domain).  ``dropout`` = (q, seed)
+    applies the replayed keep mask of flat head h (philox.keep_mask(h, nq, nk))."""
     from .masks import allowed_matrix_rect
     nq, nk = Q.shape[-2], K.shape[-2]
     allowed = allowed_matrix_rect(nq, nk, mask_kind, window, bitmask)
@@ -152,7 +159,12 @@ def forward_rect(Q, K, V, c, mask_kind, window=0, bitmask=None):
     rows = allowed.any(axis=1)
     for h in range(q.shape[0]):
         if rows.any():
-            y, l = head_forward(q[h][rows], k[h], vv[h], c, allowed[rows])
+            if dropout is None:
+                y, l = head_forward(q[h][rows], k[h], vv[h], c, allowed[rows])
+            else:
+                keep, ks = _rect_keep(h, nq, nk, dropout)
+                y, l = head_forward_dropout(q[h][rows], k[h], vv[h], c, allowed[rows],
+                                            keep[rows], ks)
             Y[h][rows] = y
             L[h][rows] = l
     return Y.reshape(V.shape[:-2] + (nq, V.shape[-1])), L.reshape(Q.shape[:-1])
@@ -258,10 +270,11 @@ def backward_dropout(Q, K, V, G, c, mask_kind, window=0, bitmask=None, q=0.0, se
     return tuple(res)
 
 
-def backward_rect(Q, K, V, G, c, mask_kind, window=0, bitmask=None):
+def backward_rect(Q, K, V, G, c, mask_kind, window=0, bitmask=None, dropout=None):
     """Reverse pass for nq queries against nk keys (``forward_rect``'s alignment):
     -> (dQ [..,nq,d], dK [..,nk,d], dV [..,nk,v], delta [..,nq]).  Rows whose
-    allowed set is empty contribute nothing (dQ_i = 0, delta_i = 0)."""
+    allowed set is empty contribute nothing (dQ_i = 0, delta_i = 0).
+    ``dropout`` as for ``forward_rect``."""
     from .masks import allowed_matrix_rect
     nq, nk = Q.shape[-2], K.shape[-2]
     allowed = allowed_matrix_rect(nq, nk, mask_kind, window, bitmask)
@@ -273,7 +286,13 @@ def backward_rect(Q, K, V, G, c, mask_kind, window=0, bitmask=None):
     delta = np.zeros((q.shape[0], nq))
     for h in range(q.shape[0]):
         if rows.any():
-            a, b, cc, dl = head_backward(q[h][rows], k[h], vv[h], g[h][rows], c, allowed[rows])
+            if dropout is None:
+                a, b, cc, dl = head_backward(q[h][rows], k[h], vv[h], g[h][rows], c,
+                                             allowed[rows])
+            else:
+                keep, ks = _rect_keep(h, nq, nk, dropout)
+                a, b, cc, dl = head_backward_dropout(q[h][rows], k[h], vv[h], g[h][rows], c,
+                                                     allowed[rows], keep[rows], ks)
             dQ[h][rows] = a
             dK[h] = b
             dV[h] = cc

@@ -781,3 +781,20 @@ def test_rect_backward_finite_differences():
             ym = np.sum(G * dense.forward_rect(*args, c, masks.CAUSAL)[0])
             num[idx] = (yp - ym) / 2e-6
         assert _rel(grads[which], num) <= 1e-5
+
+
+def test_rect_dropout_reduces_to_square_dropout_and_to_plain():
+    """nq == nk with dropout is the square dropout oracle; q = 0 is forward_rect."""
+    r = _rng(45)
+    B, H, n, d = 1, 2, 11, 4
+    Q, K, V, G = (r.normal(size=(B, H, n, d)) for _ in range(4))
+    for kind in (masks.NONE, masks.CAUSAL):
+        Y1, L1 = dense.forward_rect(Q, K, V, 0.6, kind, dropout=(0.3, 9))
+        Y2, L2 = dense.forward_dropout(Q, K, V, 0.6, kind, q=0.3, seed=9)
+        assert _rel(Y1, Y2) <= 1e-15 and _rel(L1, L2) <= 1e-15
+        g1 = dense.backward_rect(Q, K, V, G, 0.6, kind, dropout=(0.3, 9))
+        g2 = dense.backward_dropout(Q, K, V, G, 0.6, kind, q=0.3, seed=9)
+        for a, b in zip(g1, g2):
+            assert _rel(a, b) <= 1e-14
+        Y3, _ = dense.forward_rect(Q, K, V, 0.6, kind, dropout=(0.0, 9))
+        assert _rel(Y3, dense.forward_rect(Q, K, V, 0.6, kind)[0]) <= 1e-15

@@ -168,21 +168,28 @@ def make_inputs(w: Workload, heads: int | None = None) -> Inputs:
     return Inputs(Q, K, V, dY, bitmask)
 
 
-def make_decode_inputs(B, H, nq, nk, d, v, dtype, mask="none", seed=1, p_allow=0.3):
+def make_decode_inputs(B, H, nq, nk, d, v, dtype, mask="none", seed=1, p_allow=0.3,
+                       with_dy=False):
     """Q [B,H,nq,d], K [B,H,nk,d], V [B,H,nk,v] (N(0,1), drawn in that order) for
     nq queries at the end of an nk-key sequence, plus bit rows [nq][ceil(nk/32)]
     for the bitmask (each key allowed with p_allow, the query's own position
-    always allowed)."""
+    i + nk - nq always allowed when it is a key).  ``with_dy`` also draws an
+    upstream gradient dY [B,H,nq,v] right after V and returns it fifth."""
     g = torch.Generator().manual_seed(seed)
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
     Q = torch.randn(B, H, nq, d, generator=g).to(tdt)
     K = torch.randn(B, H, nk, d, generator=g).to(tdt)
     V = torch.randn(B, H, nk, v, generator=g).to(tdt)
+    dY = torch.randn(B, H, nq, v, generator=g).to(tdt) if with_dy else None
     bitmask = None
     if mask == "bitmask":
         allowed = (torch.rand(nq, nk, generator=g) < p_allow).numpy()
-        allowed[np.arange(nq), nk - nq + np.arange(nq)] = True
+        rows = np.arange(nq)
+        own = nk - nq + rows
+        allowed[rows[own >= 0], own[own >= 0]] = True
         bitmask = pack_bitmask(allowed)
+    if with_dy:
+        return Q, K, V, dY, bitmask
     return Q, K, V, bitmask
 
 
