@@ -69,7 +69,9 @@ def whole_job_tflops(flops_per_rank_step, steps, world, ms_max):
 def flops(w: workloads.Workload, allowed_pairs=None):
     """(forward, reverse) flop counts of one step of workload ``w``."""
     heads = w.B * w.H
-    if w.mask in ("none", "causal"):
+    if w.n_keys != w.n and w.mask != "bitmask":
+        f = 2.0 * w.allowed_pairs_per_head() * (w.d + w.v) * heads
+    elif w.mask in ("none", "causal"):
         f = 2.0 * w.n * w.n * (w.d + w.v) * heads
         if w.mask == "causal":
             f /= 2.0
@@ -152,6 +154,15 @@ def oracle_sample_step(w, Q, K, V, G, rows, dropout=None):
     from oracle import dense, masks
     n = w.n
     r0 = n - rows
+    if w.n_keys != w.n:  # the last rows of a cross-attention problem are one too
+        dense.forward_rect(Q[None, None, r0:], K[None, None], V[None, None], w.scale,
+                           w.mask_kind, w.window)
+        dense.backward_rect(Q[None, None, r0:], K[None, None], V[None, None],
+                            G[None, None, r0:], w.scale, w.mask_kind, w.window)
+        off = w.n_keys - n
+        pairs = sum(max(0, min(w.n_keys, i + off + 1)) if w.mask == "causal" else w.n_keys
+                    for i in range(r0, n))
+        return 3.5 * 2.0 * pairs * (w.d + w.v)
     allowed = masks.allowed_matrix(n, w.mask_kind, w.window, None)[r0:]
     if dropout is None:
         dense.head_forward(Q[r0:], K, V, w.scale, allowed)
@@ -285,9 +296,18 @@ def run_gpu(args, w):
     x = workloads.make_inputs(w)
     q, k, v, dy = (t.to(dev) for t in (x.Q, x.K, x.V, x.dY))
     bm = None if x.bitmask is None else torch.from_numpy(x.bitmask.view(np.int32)).to(dev)
-    shape = ex.Shape(w.B, w.H, w.n, w.d, w.v, 0 if w.dtype == "f32" else 1)
-    ws_f = ex.workspace(ex.fwd_workspace_size(shape, w.mask), dev)
-    ws_b = ex.workspace(ex.bwd_workspace_size(shape, w.mask), dev)
+    if w.n_keys != w.n:
+        import ctypes
+        shape = ex.QKShape(w.B, w.H, w.n, w.n_keys, w.d, w.v, 0 if w.dtype == "f32" else 1)
+        lib = ex.load_library()
+        ws_f = ex.workspace(lib.exattn_fwd_qk_workspace_size(ctypes.byref(shape),
+                                                             w.mask_kind), dev)
+        ws_b = ex.workspace(lib.exattn_bwd_qk_workspace_size(ctypes.byref(shape),
+                                                             w.mask_kind), dev)
+    else:
+        shape = ex.Shape(w.B, w.H, w.n, w.d, w.v, 0 if w.dtype == "f32" else 1)
+        ws_f = ex.workspace(ex.fwd_workspace_size(shape, w.mask), dev)
+        ws_b = ex.workspace(ex.bwd_workspace_size(shape, w.mask), dev)
     y = torch.empty(q.shape[:-1] + (w.v,), dtype=q.dtype, device=dev)
     L = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -411,8 +431,8 @@ def run_gpu(args, w):
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d, "v": w.v,
-                   "mask": w.mask, "window": w.window, "scale": w.scale,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "nk": w.n_keys, "d": w.d,
+                   "v": w.v, "mask": w.mask, "window": w.window, "scale": w.scale,
                    "kernel_path": args.path, "dropout_p": args.dropout,
                    "l2": ("inputs larger than L2 (%d MB of Q, K, V, dY vs 129 MB), no flush"
                           % (sum(t.numel() * t.element_size() for t in (q, k, v, dy)) >> 20)),
@@ -637,6 +657,8 @@ def main():
     ap.add_argument("--batch", type=int, default=None,
                     help="override the batch size (a smaller case of the same workload)")
     ap.add_argument("--heads", type=int, default=None, help="override the head count")
+    ap.add_argument("--nk", type=int, default=0,
+                    help="keys per slice (cross-attention: the n queries sit at the end)")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="drop probability (dropout with a replayed mask), default none")
     ap.add_argument("--seed", type=int, default=1234, help="dropout seed")
@@ -658,6 +680,9 @@ def main():
         (run_reference_decode if args.impl == "reference" else run_gpu_decode)(args, dw)
         return
     w = workloads.workload(args.workload, args.variant)
+    if args.nk and args.nk != w.n:
+        import dataclasses
+        w = dataclasses.replace(w, nk=args.nk, name=f"{w.name}-nk{args.nk}")
     if args.batch is not None or args.heads is not None:
         import dataclasses
         B = args.batch if args.batch is not None else w.B

@@ -51,6 +51,11 @@ class Workload:
     self_attention: bool = False
     seed: int = SEED_BASE
     extra: dict = field(default_factory=dict)
+    nk: int = 0                # keys (0: n, self-attention shapes); queries sit at the end
+
+    @property
+    def n_keys(self) -> int:
+        return self.nk or self.n
 
     @property
     def torch_dtype(self):
@@ -61,15 +66,17 @@ class Workload:
         return MASK_KINDS[self.mask]
 
     def allowed_pairs_per_head(self) -> int:
-        """|A| = sum_i |A_i| for the arithmetic masks (bitmask: unknown here)."""
-        n = self.n
+        """|A| = sum_i |A_i| for the arithmetic masks (bitmask: unknown here); query
+        i sits at position i + nk - n, so it sees min(nk, i + nk - n + 1) keys
+        under the causal mask and at most ``window`` of them under the window."""
+        n, nk = self.n, self.n_keys
         if self.mask == "none":
-            return n * n
+            return n * nk
+        off = nk - n
         if self.mask == "causal":
-            return n * (n + 1) // 2
+            return sum(max(0, min(nk, i + off + 1)) for i in range(n))
         if self.mask == "window":
-            w = min(self.window, n)
-            return sum(min(i + 1, w) for i in range(n))
+            return sum(max(0, min(nk, i + off + 1, self.window)) for i in range(n))
         raise ValueError("bitmask pair count depends on the drawn mask")
 
 
@@ -145,8 +152,12 @@ def make_inputs(w: Workload, heads: int | None = None) -> Inputs:
     the same numbers as the full draw sliced, so callers that compare against a
     full-size run must draw the full size and slice instead.
     """
-    g = torch.Generator().manual_seed(w.seed)
     B, H = (w.B, w.H) if heads is None else (1, heads)
+    if w.n_keys != w.n:  # cross-attention: the decode-shape generator with dY
+        Q, K, V, dY, bm = make_decode_inputs(B, H, w.n, w.n_keys, w.d, w.v, w.dtype, w.mask,
+                                             seed=w.seed, p_allow=w.p_allow, with_dy=True)
+        return Inputs(Q, K, V, dY, bm)
+    g = torch.Generator().manual_seed(w.seed)
     n, d, v = w.n, w.d, w.v
     if w.self_attention:
         X = 0.5 * torch.randn(B, H, n, d, generator=g)
