@@ -318,7 +318,7 @@ def bwd_noalloc(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, d
 
 
 KERNEL_FWD, KERNEL_DELTA, KERNEL_BWD, KERNEL_DQ_CONVERT, KERNEL_BWD_Q = 0, 1, 2, 3, 4
-KERNEL_SPLIT_PARTIAL, KERNEL_SPLIT_MERGE = 5, 6
+KERNEL_SPLIT_PARTIAL, KERNEL_SPLIT_MERGE, KERNEL_SPLIT32 = 5, 6, 7
 
 
 def record_kernel_events(which: int, start, stop) -> None:

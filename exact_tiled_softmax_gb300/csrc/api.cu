@@ -155,10 +155,18 @@ int exattn_set_path(int path) {
   return g_path.exchange(path);
 }
 
+// Forward workspace: the status word, plus for fp32 shapes that the 3xTF32
+// tensor-core forward takes (d = v in {64, 128}) the split copies of K and V.
+static size_t fwd_ws_bytes(const Dims& s) {
+  if (s.dtype != EXATTN_F32 || s.d != s.v || (s.d != 64 && s.d != 128)) return kStatusBytes;
+  Problem p = make_problem(s, 1.f, EXATTN_MASK_NONE, 0, nullptr);
+  return kStatusBytes + split32_bytes(p);
+}
+
 size_t exattn_fwd_workspace_size(const exattn_shape* shape, int mask_kind) {
   if (check_shape(shape) != EXATTN_OK) return 0;
   (void)mask_kind;
-  return kStatusBytes;
+  return fwd_ws_bytes(dims_of(shape));
 }
 
 size_t exattn_bwd_workspace_size(const exattn_shape* shape, int mask_kind) {
@@ -170,7 +178,7 @@ size_t exattn_bwd_workspace_size(const exattn_shape* shape, int mask_kind) {
 size_t exattn_fwd_qk_workspace_size(const exattn_qk_shape* shape, int mask_kind) {
   if (!shape || check_dims(dims_of(shape)) != EXATTN_OK) return 0;
   (void)mask_kind;
-  return kStatusBytes;
+  return fwd_ws_bytes(dims_of(shape));
 }
 
 size_t exattn_bwd_qk_workspace_size(const exattn_qk_shape* shape, int mask_kind) {
@@ -193,7 +201,7 @@ int fwd_impl(const Dims& dims, const void* Q, const void* K, const void* V, floa
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Y) || !aligned16(L))
     return EXATTN_MISALIGNED;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return EXATTN_MISALIGNED;
-  if (workspace_bytes < kStatusBytes) return EXATTN_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < fwd_ws_bytes(dims)) return EXATTN_WORKSPACE_TOO_SMALL;
 
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   exattn::g_last_error[0] = 0;
@@ -210,6 +218,10 @@ int fwd_impl(const Dims& dims, const void* Q, const void* K, const void* V, floa
   if (e != cudaSuccess) return cuda_status(e, "attn_fwd: clearing the status word");
   if (g_path.load() != EXATTN_PATH_SIMT && tc_fwd_supported(a.p))
     return cuda_status(launch_tc_fwd(a, s), "attn_fwd: tensor-core forward launch");
+  if (g_path.load() != EXATTN_PATH_SIMT && tc_fwd32_supported(a.p))
+    return cuda_status(
+        launch_tc_fwd32(a, split32_layout(a.p, static_cast<char*>(workspace) + kStatusBytes), s),
+        "attn_fwd: 3xTF32 forward launch");
   return cuda_status(launch_simt_fwd(a, s), "attn_fwd: SIMT forward launch");
 }
 

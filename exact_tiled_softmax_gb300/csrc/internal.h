@@ -66,7 +66,8 @@ enum KernelRole {
   kKernBwdQ = 4,
   kKernSplitPartial = 5,
   kKernSplitMerge = 6,
-  kKernRoles = 7
+  kKernSplit32 = 7,
+  kKernRoles = 8
 };
 void before_launch(int role, cudaStream_t s);
 // Remember the last failing step of this host thread (exattn_last_error).
@@ -93,6 +94,20 @@ bool tc_fwd_supported(const Problem& p);
 cudaError_t launch_tc_fwd(const FwdArgs& a, cudaStream_t s);
 bool tc_bwd_supported(const Problem& p);
 cudaError_t launch_tc_bwd(const BwdArgs& a, cudaStream_t s);
+
+// 3xTF32 tensor-core forward for fp32 inputs (d = v in {64, 128}).  K and V
+// are first split into tf32 hi / lo parts (V transposed) in the workspace.
+struct Split32 {
+  float* kh;   // [BH][nk][d]
+  float* kl;
+  float* vth;  // [BH][v][ldt], keys contiguous
+  float* vtl;
+  int ldt;     // nk rounded up to 32
+};
+bool tc_fwd32_supported(const Problem& p);
+size_t split32_bytes(const Problem& p);
+Split32 split32_layout(const Problem& p, void* base);
+cudaError_t launch_tc_fwd32(const FwdArgs& a, const Split32& ws, cudaStream_t s);
 
 // Split-KV forward (nq queries aligned to the end of nk keys).
 struct SplitArgs {

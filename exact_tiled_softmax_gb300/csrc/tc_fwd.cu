@@ -573,6 +573,7 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, int width, int n, int BH) 
 }
 
 bool tmap_encoder_available() { return encode_fn() != nullptr; }
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() { return encode_fn(); }
 
 bool tc_fwd_supported(const Problem& p) {
   if (p.dtype != kBF16 || p.d != p.v || (p.d != 64 && p.d != 128)) return false;

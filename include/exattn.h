@@ -94,8 +94,11 @@ typedef struct exattn_shape {
 
 /* Kernel path selection, process-wide (default EXATTN_PATH_AUTO).
  * AUTO uses the tcgen05/TMA/TMEM kernels where the shape allows (bf16 with
- * d = v in {64, 128}) and the SIMT fp32 kernels otherwise; its reverse pass is
- * a key-major dK/dV kernel plus a query-major dQ kernel.  SIMT forces the SIMT
+ * d = v in {64, 128}; for fp32 with d = v in {64, 128} and a positive scale
+ * the forward runs 3xTF32 on the tensor cores: each operand split into two
+ * tf32 parts, three products per product, partial sums promoted to fp32 every
+ * key block) and the SIMT fp32 kernels otherwise; its reverse pass is a
+ * key-major dK/dV kernel plus a query-major dQ kernel.  SIMT forces the SIMT
  * kernels for every shape.  ATOMIC_DQ is AUTO with the other reverse form on
  * the tensor cores: one key-major kernel that adds dQ into an fp32 accumulator
  * with vector reductions (kept for measurement).  Returns the previous
@@ -104,9 +107,12 @@ enum exattn_path { EXATTN_PATH_AUTO = 0, EXATTN_PATH_SIMT = 1, EXATTN_PATH_ATOMI
 int exattn_set_path(int path);
 
 /* Workspace bytes that attn_fwd / attn_bwd need for this shape and mask kind.
- * The workspace holds the device status word (first 256 bytes) and, for the
- * reverse pass, delta [B][H][n] and the fp32 dQ accumulator [B][H][n][d].
- * Returns 0 when the shape is invalid. */
+ * The workspace holds the device status word (first 256 bytes); for an fp32
+ * forward with d = v in {64, 128} (the 3xTF32 tensor-core forward) also the
+ * tf32 hi / lo split of K and V (4 copies of K's and V's size, V transposed
+ * with rows padded to 32 keys); for the reverse pass delta [B][H][n], L log2(e)
+ * [B][H][n] and the fp32 dQ accumulator [B][H][n][d].  Every size is linear in
+ * n.  Returns 0 when the shape is invalid. */
 size_t exattn_fwd_workspace_size(const exattn_shape* shape, int mask_kind);
 size_t exattn_bwd_workspace_size(const exattn_shape* shape, int mask_kind);
 
@@ -280,7 +286,8 @@ enum exattn_kernel {
   EXATTN_KERNEL_DQ_CONVERT = 3, /* fp32 dQ accumulator -> dQ (SIMT and ATOMIC_DQ paths) */
   EXATTN_KERNEL_BWD_Q = 4,      /* the query-major dQ kernel alone (AUTO path) */
   EXATTN_KERNEL_SPLIT_PARTIAL = 5, /* per-chunk summaries of attn_fwd_splitkv */
-  EXATTN_KERNEL_SPLIT_MERGE = 6    /* the merge kernel of attn_fwd_splitkv (nq > 4) */
+  EXATTN_KERNEL_SPLIT_MERGE = 6,   /* the merge kernel of attn_fwd_splitkv (nq > 4) */
+  EXATTN_KERNEL_SPLIT32 = 7        /* the tf32 hi / lo split of K and V (fp32 forward) */
 };
 
 /* One-shot: on the next launch of kernel `which` (an exattn_kernel), record
