@@ -278,6 +278,39 @@ def read_traffic(kernel_tag):
     return float(e["bytes_per_launch"])
 
 
+# Peaks beyond the measured bf16 figure (derived, stated in the roofline):
+# tf32 dense = measured bf16 burst x 1.1 / 2.25 (nominal per-GPU ratio); fp32
+# FMA = 152 SMs x 128 lanes x 2 flop x the maximum SM clock.
+TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def kernel_roofline(args, w, which, achieved, peaks, peak_kind):
+    """Roofline object for the forward ("fwd") or reverse ("bwd") kernel(s)."""
+    eligible = args.path != "simt" and w.d == w.v and w.d in (64, 128)
+    bf16_peak = float(peaks["bf16_tflops"])
+    if w.dtype == "bf16" and eligible:
+        tag = f"tc_{which}"
+        if which == "bwd":
+            tag += "_atomic" if args.path == "atomic_dq" else "_split"
+        return {"kernel": tag, "bound": "tensor", "achieved": achieved, "peak": bf16_peak,
+                "unit": "TFLOP/s", "frac": achieved / bf16_peak,
+                "peak_kind": f"bf16 dense burst, of {peak_kind}", "traffic": read_traffic(tag)}
+    if w.dtype == "f32" and eligible and which == "fwd" and not args.dropout:
+        peak = bf16_peak * TF32_OVER_BF16
+        return {"kernel": "tc32_fwd", "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_kind": f"tf32 dense = bf16 burst of {peak_kind} x 1.1/2.25 (nominal ratio)",
+                "tensor_work_frac": 3 * achieved / peak,
+                "note": "3xTF32: the tensor pipe runs three tf32 products per product",
+                "traffic": read_traffic("tc32_fwd")}
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    peak = 152 * 128 * 2 * mhz * 1e6 / 1e12
+    return {"kernel": f"simt_{which}", "bound": "alu", "achieved": achieved, "peak": peak,
+            "unit": "TFLOP/s", "frac": achieved / peak,
+            "peak_kind": f"fp32 FMA: 152 SMs x 128 lanes x 2 flop x {mhz:.0f} MHz",
+            "traffic": read_traffic(f"simt_{which}")}
+
+
 def run_gpu(args, w):
     import exact_tiled_softmax_gb300 as ex
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -418,15 +451,10 @@ def run_gpu(args, w):
     dom_flops = f_fwd if dom == ex.KERNEL_FWD else f_bwd
     dom_name = "fwd" if dom == ex.KERNEL_FWD else "bwd"
     achieved = dom_flops / (kern_ms[dom] * 1e-3) / 1e12
-    tc = args.path != "simt" and w.dtype == "bf16" and w.d == w.v and w.d in (64, 128)
-    tag = f"{'tc' if tc else 'simt'}_{dom_name}"
-    if tc and dom_name == "bwd":
-        tag += "_atomic" if args.path == "atomic_dq" else "_split"
-    roofline = {"kernel": tag,
-                "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_kind": f"bf16 dense burst, of {peak_kind}",
-                "traffic": read_traffic(tag),
-                "kernel_ms": {"fwd": kern_ms[ex.KERNEL_FWD], "bwd": kern_ms[ex.KERNEL_BWD]}}
+    roofline = kernel_roofline(args, w, dom_name, achieved, peaks, peak_kind)
+    roofline["kernel_ms"] = {"fwd": kern_ms[ex.KERNEL_FWD], "bwd": kern_ms[ex.KERNEL_BWD]}
+    roofline_fwd = kernel_roofline(args, w, "fwd", f_fwd / (kern_ms[ex.KERNEL_FWD] * 1e-3) / 1e12,
+                                   peaks, peak_kind)
     line = {
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
@@ -441,6 +469,7 @@ def run_gpu(args, w):
         "fwd_bwd_frac_of_peak": tflops / peak, "ms_fwd": ms_fwd / K,
         "gpu_launches": launches,
         "roofline": roofline,
+        "roofline_fwd": roofline_fwd,
         "e2e": e2e,
         "clocks": clocks.summary(),
     }
@@ -657,6 +686,8 @@ def main():
     ap.add_argument("--batch", type=int, default=None,
                     help="override the batch size (a smaller case of the same workload)")
     ap.add_argument("--heads", type=int, default=None, help="override the head count")
+    ap.add_argument("--dtype", choices=["bf16", "f32"], default=None,
+                    help="override the workload's input dtype")
     ap.add_argument("--nk", type=int, default=0,
                     help="keys per slice (cross-attention: the n queries sit at the end)")
     ap.add_argument("--dropout", type=float, default=0.0,
@@ -680,6 +711,9 @@ def main():
         (run_reference_decode if args.impl == "reference" else run_gpu_decode)(args, dw)
         return
     w = workloads.workload(args.workload, args.variant)
+    if args.dtype and args.dtype != w.dtype:
+        import dataclasses
+        w = dataclasses.replace(w, dtype=args.dtype, name=f"{w.name}-as-{args.dtype}")
     if args.nk and args.nk != w.n:
         import dataclasses
         w = dataclasses.replace(w, nk=args.nk, name=f"{w.name}-nk{args.nk}")
