@@ -634,7 +634,8 @@ def run_gpu_decode(args, w):
     e = 4 if w.dtype == "f32" else 2
     partial_bytes = w.B * w.H * (w.nq * w.d * e + w.nk * (w.d + w.v) * e)
     achieved = partial_bytes / (kern_ms[ex.KERNEL_SPLIT_PARTIAL] * 1e-3) / 1e9
-    kind = "reg" if w.nq <= 4 else "smem"
+    kind = "reg" if w.nq <= 4 else ("tc" if w.dtype == "bf16" and w.d == w.v and w.d in (64, 128)
+                                     else "smem")
     roofline = {"kernel": f"splitkv_partial_{kind}", "bound": "hbm", "achieved": achieved,
                 "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": f"copy bandwidth, of {peak_kind}",

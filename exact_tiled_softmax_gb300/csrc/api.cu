@@ -358,27 +358,37 @@ int check_qk_shape(const exattn_qk_shape* s) {
   return EXATTN_OK;
 }
 
-// num_splits == 0: enough chunks for about 32 CTAs per SM of the 152-SM part
-// (8 waves of the decode kernel's 4 resident CTAs per SM, so the last wave is
-// a small part of the run) over all batch*head slices, with at least 256 keys
-// per chunk.
-constexpr int kAutoSplitCtas = 32 * 152;
+// Shapes whose chunks can run on the tensor-core forward in summary mode
+// (bf16, d = v in {64, 128}, more queries than the register kernel takes).
+// The plan depends on the shape alone, so the workspace query and the call
+// agree whatever the kernel path setting.
+bool splitkv_tc_shape(const exattn_qk_shape* s) {
+  return s->dtype == EXATTN_BF16 && s->d == s->v && (s->d == 64 || s->d == 128) &&
+         s->nq > splitkv_reg_max_queries();
+}
+
+// num_splits == 0: enough chunks for about 8 waves of resident CTAs over all
+// batch*head slices (the register kernel keeps 4 CTAs per SM of the 152-SM
+// part, the tensor-core kernel 1), with at least 256 keys per chunk.
 constexpr int kAutoMinChunk = 256;
 
 int resolve_splits(const exattn_qk_shape* s, int num_splits) {
   if (num_splits != 0) return num_splits;
+  const int target = (splitkv_tc_shape(s) ? 8 : 32) * 152;
   const int bh = s->batch * s->heads;
-  const int want = (kAutoSplitCtas + bh - 1) / bh;
+  const int want = (target + bh - 1) / bh;
   const int most = (s->nk + kAutoMinChunk - 1) / kAutoMinChunk;
   return want < 1 ? 1 : (want > most ? most : want);
 }
 
-// Keys per chunk (a multiple of 32) and the number of chunks actually used.
-void split_plan(int nk, int num_splits, int* chunk, int* splits) {
-  int c = (nk + num_splits - 1) / num_splits;
-  c = (c + 31) / 32 * 32;
+// Keys per chunk (a multiple of 32, of 128 for tensor-core shapes) and the
+// number of chunks actually used.
+void split_plan(const exattn_qk_shape* s, int num_splits, int* chunk, int* splits) {
+  const int gran = splitkv_tc_shape(s) ? 128 : 32;
+  int c = (s->nk + num_splits - 1) / num_splits;
+  c = (c + gran - 1) / gran * gran;
   *chunk = c;
-  *splits = (nk + c - 1) / c;
+  *splits = (s->nk + c - 1) / c;
 }
 
 }  // namespace
@@ -387,7 +397,7 @@ size_t exattn_splitkv_workspace_size(const exattn_qk_shape* shape, int num_split
   if (check_qk_shape(shape) != EXATTN_OK || num_splits < 0 || num_splits > 4096) return 0;
   num_splits = resolve_splits(shape, num_splits);
   int chunk, splits;
-  split_plan(shape->nk, num_splits, &chunk, &splits);
+  split_plan(shape, num_splits, &chunk, &splits);
   const size_t bh = (size_t)shape->batch * shape->heads;
   const size_t rows = bh * splits * shape->nq;
   return kStatusBytes + align_up(sizeof(unsigned) * bh, 256) +
@@ -425,7 +435,7 @@ int attn_fwd_splitkv(const exattn_qk_shape* shape, const void* Q, const void* K,
   a.words_per_row = (shape->nk + 31) / 32;
   a.bits = mask_kind == EXATTN_MASK_BITMASK ? bitmask : nullptr;
   a.sl2 = scale * 1.4426950408889634f;
-  split_plan(shape->nk, resolve_splits(shape, num_splits), &a.chunk, &a.splits);
+  split_plan(shape, resolve_splits(shape, num_splits), &a.chunk, &a.splits);
   // Workspace: status word | chunk counters [BH] | m | l | z (each 256-byte aligned).
   const size_t rows = (size_t)a.BH * a.splits * a.nq;
   const size_t cnt_bytes = align_up(sizeof(unsigned) * a.BH, 256);
@@ -440,6 +450,23 @@ int attn_fwd_splitkv(const exattn_qk_shape* shape, const void* Q, const void* K,
   a.status = static_cast<unsigned*>(workspace);
   cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes + cnt_bytes, s);
   if (e != cudaSuccess) return cuda_status(e, "attn_fwd_splitkv: clearing the status word");
+  if (g_path.load() != EXATTN_PATH_SIMT && splitkv_tc_shape(shape)) {
+    // Chunks on the tensor-core forward in summary mode, then the merge.
+    FwdArgs f;
+    f.p = make_problem(dims_of(shape), scale, mask_kind, window, bitmask);
+    if (tc_fwd_supported(f.p)) {
+      f.Q = Q;
+      f.K = K;
+      f.V = V;
+      f.Y = Y;
+      f.L = L;
+      f.status = a.status;
+      e = launch_tc_fwd_chunks(f, a.chunk, a.splits, a.pm, a.pl, a.pz, s);
+      if (e != cudaSuccess) return cuda_status(e, "attn_fwd_splitkv: tensor-core chunks");
+      return cuda_status(launch_splitkv_merge(a, shape->dtype, Y, L, a.status, s),
+                         "attn_fwd_splitkv: merge launch");
+    }
+  }
   return cuda_status(launch_splitkv(a, shape->dtype, Y, L, static_cast<unsigned*>(workspace), s),
                      "attn_fwd_splitkv: launch");
 }

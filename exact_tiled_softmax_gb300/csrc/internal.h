@@ -92,6 +92,10 @@ bool tc_bwd_split_supported(const Problem& p);
 cudaError_t launch_tc_bwd_split(const BwdArgs& a, cudaStream_t s);
 bool tc_fwd_supported(const Problem& p);
 cudaError_t launch_tc_fwd(const FwdArgs& a, cudaStream_t s);
+// The same kernel in split-KV summary mode: chunks of chunk_keys (a multiple
+// of 128) keys, summaries to pm / pl / pz [BH][splits][n] (see SplitArgs).
+cudaError_t launch_tc_fwd_chunks(const FwdArgs& a, int chunk_keys, int splits, float* pm,
+                                 float* pl, float* pz, cudaStream_t s);
 bool tc_bwd_supported(const Problem& p);
 cudaError_t launch_tc_bwd(const BwdArgs& a, cudaStream_t s);
 
@@ -127,7 +131,11 @@ struct SplitArgs {
 };
 size_t splitkv_smem_bytes(int nq, int d, int v, int elem_bytes);
 int splitkv_max_queries();
+int splitkv_reg_max_queries();  // nq up to this runs the register-resident chunk kernel
 cudaError_t launch_splitkv(const SplitArgs& a, int dtype, void* Y, float* L, unsigned* status,
                            cudaStream_t s);
+// The star merge of the chunk summaries alone (after launch_tc_fwd_chunks).
+cudaError_t launch_splitkv_merge(const SplitArgs& a, int dtype, void* Y, float* L,
+                                 unsigned* status, cudaStream_t s);
 
 }  // namespace exattn

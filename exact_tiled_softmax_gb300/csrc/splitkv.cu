@@ -580,6 +580,22 @@ size_t splitkv_smem_bytes(int nq, int d, int v, int elem_bytes) {
 }
 
 int splitkv_max_queries() { return kMaxNq; }
+int splitkv_reg_max_queries() { return kRegMaxNq; }
+
+cudaError_t launch_splitkv_merge(const SplitArgs& a, int dtype, void* Y, float* L,
+                                 unsigned* status, cudaStream_t s) {
+  const int rows = a.BH * a.nq;
+  const unsigned blocks = (rows * 32 + kMergeThreads - 1) / kMergeThreads;
+  before_launch(kKernSplitMerge, s);
+  if (dtype == kF32)
+    splitkv_merge_kernel<float><<<blocks, kMergeThreads, 0, s>>>(a, static_cast<float*>(Y), L,
+                                                                 status);
+  else
+    splitkv_merge_kernel<__nv_bfloat16><<<blocks, kMergeThreads, 0, s>>>(
+        a, static_cast<__nv_bfloat16*>(Y), L, status);
+  after_launch(kKernSplitMerge, s);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_splitkv(const SplitArgs& a, int dtype, void* Y, float* L, unsigned* status,
                            cudaStream_t s) {

@@ -64,6 +64,13 @@ struct FwdParams {
   unsigned* status;
   uint32_t drop_t, seed_lo, seed_hi;  // dropout (kernel variant kDrop only)
   float drop_scale;
+  // Split-KV summary mode (chunk_kt > 0): CTA z covers key blocks
+  // [z * chunk_kt, (z + 1) * chunk_kt) and writes its rows' summaries (m in the
+  // exp2 domain, l, z unnormalised) to pm / pl / pz [BH][splits][n] instead of Y, L.
+  int chunk_kt, splits;
+  float* pm;
+  float* pl;
+  float* pz;
 };
 
 template <int D, int V>
@@ -170,6 +177,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow)
       kt_end = alast < 0 ? 0 : min(nkt, alast / kBN + 1);
     if (p.mask_kind == kMaskWindow) kt_begin = max(0, rows[0].r0 + p.off - p.window + 1) / kBN;
+  }
+  const int split = blockIdx.z;
+  if (p.chunk_kt > 0) {
+    kt_begin = max(kt_begin, split * p.chunk_kt);
+    kt_end = max(kt_begin, min(kt_end, (split + 1) * p.chunk_kt));
   }
 
   if (threadIdx.x == 0) {
@@ -498,6 +510,34 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         tc_fence_after();
       }
       const bool valid = i < n;
+      if (p.chunk_kt > 0) {
+        // Split-KV summary of this key chunk for row i ("Exact tiled softmax
+        // attention ...", Forward procedure: the summary of a block of keys).
+        const size_t row = (static_cast<size_t>(bh) * p.splits + split) * n + (valid ? i : 0);
+#pragma unroll
+        for (int ch = 0; ch < V / 32; ++ch) {
+          uint32_t o[32];
+          if (have_o) {
+            tmem_ld32(t_o + ch * 32, o);
+            tmem_ld_wait();
+            reg_fence(o);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+          }
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(p.pz + row * V + ch * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                   __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+          }
+        }
+        if (valid) {
+          p.pm[row] = l > 0.f ? m_ref : -INFINITY;
+          p.pl[row] = l;
+        }
+      } else {
       const float inv = l > 0.f ? (kDrop ? p.drop_scale : 1.f) / l : 0.f;
       __nv_bfloat16* yrow = p.Y + (static_cast<size_t>(bh) * n + (valid ? i : 0)) * V;
 #pragma unroll
@@ -526,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         p.L[static_cast<size_t>(bh) * n + i] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
         if (!(l > 0.f)) raise_status(p.status, kStatusEmptyRow);
       }
+      }  // plain epilogue
     }
   }
 
@@ -583,7 +624,8 @@ bool tc_fwd_supported(const Problem& p) {
 }
 
 template <int D>
-cudaError_t launch_tc_fwd_d(const FwdArgs& a, cudaStream_t s) {
+cudaError_t launch_tc_fwd_d(const FwdArgs& a, cudaStream_t s, int chunk_kt = 0, int splits = 1,
+                            float* pm = nullptr, float* pl = nullptr, float* pz = nullptr) {
   const Problem& pr = a.p;
   FwdParams p;
   if (!make_tmap_bf16(&p.tq, a.Q, D, pr.n, pr.BH) || !make_tmap_bf16(&p.tk, a.K, D, pr.nk, pr.BH) ||
@@ -606,6 +648,11 @@ cudaError_t launch_tc_fwd_d(const FwdArgs& a, cudaStream_t s) {
   p.seed_lo = pr.seed_lo;
   p.seed_hi = pr.seed_hi;
   p.drop_scale = pr.drop_scale;
+  p.chunk_kt = chunk_kt;
+  p.splits = splits;
+  p.pm = pm;
+  p.pl = pl;
+  p.pz = pz;
   using Lay = Layout<D, D>;
   auto kern = pr.drop_t != 0 ? tc_fwd_kernel<D, D, true> : tc_fwd_kernel<D, D, false>;
   cudaError_t e =
@@ -614,15 +661,23 @@ cudaError_t launch_tc_fwd_d(const FwdArgs& a, cudaStream_t s) {
     record_error("tc_fwd: cudaFuncSetAttribute", static_cast<int>(e), cudaGetErrorString(e));
     return e;
   }
-  dim3 grid(p.n_qblocks, pr.BH);
-  before_launch(kKernFwd, s);
+  dim3 grid(p.n_qblocks, pr.BH, chunk_kt > 0 ? splits : 1);
+  const int role = chunk_kt > 0 ? kKernSplitPartial : kKernFwd;
+  before_launch(role, s);
   kern<<<grid, kThreads, Lay::ALLOC, s>>>(p);
-  after_launch(kKernFwd, s);
+  after_launch(role, s);
   return cudaGetLastError();
 }
 
 cudaError_t launch_tc_fwd(const FwdArgs& a, cudaStream_t s) {
   return a.p.d == 128 ? launch_tc_fwd_d<128>(a, s) : launch_tc_fwd_d<64>(a, s);
+}
+
+cudaError_t launch_tc_fwd_chunks(const FwdArgs& a, int chunk_keys, int splits, float* pm,
+                                 float* pl, float* pz, cudaStream_t s) {
+  const int chunk_kt = chunk_keys / kBN;
+  return a.p.d == 128 ? launch_tc_fwd_d<128>(a, s, chunk_kt, splits, pm, pl, pz)
+                      : launch_tc_fwd_d<64>(a, s, chunk_kt, splits, pm, pl, pz);
 }
 
 }  // namespace exattn

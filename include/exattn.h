@@ -213,10 +213,15 @@ int attn_bwd_noalloc(const exattn_shape* shape, const void* Q, const void* K, co
  * j <= i + nk - nq, WINDOW w the w keys ending there, BITMASK reads bit rows
  * [nq][ceil(nk/32)].  Limits: 1 <= nq <= 64, nk >= 1, d, v <= 256 and rows of
  * whole 16-byte pieces (d, v multiples of 8 for bf16, of 4 for fp32),
- * 0 <= num_splits <= 4096 (chunks are whole multiples of 32 keys, so fewer
- * chunks may be used than asked for; 0 picks enough chunks for about 4864
- * CTAs over all batch*head slices, at least 256 keys each, from the shape
- * alone, so the workspace query and the call agree).  Rows with an empty
+ * 0 <= num_splits <= 4096 (chunks are whole multiples of 32 keys, of 128 for
+ * the tensor-core shapes below, so fewer chunks may be used than asked for;
+ * 0 picks enough chunks for about 8 waves of resident CTAs over all
+ * batch*head slices, at least 256 keys each, from the shape alone, so the
+ * workspace query and the call agree).  Kernels: nq <= 4 runs a register-
+ * resident chunk kernel that merges in its last CTA per slice; bf16 with
+ * d = v in {64, 128}, nq > 4 and a positive scale runs the tensor-core
+ * forward in summary mode per chunk, then a merge kernel; other shapes a
+ * shared-memory chunk kernel, then the merge kernel.  Rows with an empty
  * allowed set get Y_i = 0, L_i = -inf and the EXATTN_EMPTY_ROW status.
  * Ownership, streams and errors as for attn_fwd.
  * ------------------------------------------------------------------------- */

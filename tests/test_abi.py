@@ -128,6 +128,12 @@ def test_splitkv_workspace_and_split_plan(lib):
     assert chunks(_qk(B=1, H=1, nk=1000), 0) == 4
     assert chunks(_qk(B=64, H=64, nk=1000), 0) == 2
     assert chunks(_qk(B=128, H=64, nk=1000), 0) == 1
+    # bf16, d = v = 128, nq > 4 (tensor-core chunks): chunks are multiples of 128
+    # keys, and auto aims at 8 waves of one CTA per SM (1216 CTAs).
+    assert chunks(_qk(nq=8, nk=1000), 4) == 4        # 250 -> 256 keys
+    assert chunks(_qk(nq=8, nk=1000), 16) == 8       # 63 -> 128 keys
+    assert chunks(_qk(B=8, H=32, nq=8, nk=16384), 0) == 5
+    assert chunks(_qk(nq=8, nk=1000, d=80, v=80), 16) == 16   # not a tensor-core shape
     assert size(_qk(nq=65), 1) == 0            # more than 64 queries
     assert size(_qk(d=20, dtype=1), 1) == 0    # bf16 rows need 8-element pieces
     assert size(_qk(d=20, dtype=0), 1) != 0    # fp32: 4-element pieces

@@ -60,6 +60,13 @@ CASES = [
     (1, 3, 4, 2500, 16, 32, "bf16", "causal", 0),
     (1, 1, 1, 2049, 128, 128, "f32", "causal", 0),
     (1, 2, 3, 1500, 64, 64, "f32", "window", 64),
+    # bf16, d = v in {64, 128}, nq > 4: chunks on the tensor-core forward (summary
+    # mode, 128-key chunks), then the merge kernel.
+    (1, 2, 8, 1000, 128, 128, "bf16", "causal", 0),
+    (2, 2, 64, 3000, 64, 64, "bf16", "bitmask", 0),
+    (1, 1, 5, 129, 128, 128, "bf16", "none", 0),
+    (1, 2, 40, 5000, 128, 128, "bf16", "window", 1000),
+    (1, 1, 17, 300, 64, 64, "bf16", "causal", 0),
 ]
 
 
@@ -79,7 +86,7 @@ def test_splitkv_matches_oracle_for_every_split_count(ex, case):
         _check(dtype, Y, L, Yr, Lr)
 
 
-@pytest.mark.parametrize("nq,nk", [(8, 5), (4, 2)])
+@pytest.mark.parametrize("nq,nk", [(8, 5), (4, 2), (20, 7)])
 def test_more_queries_than_keys_gives_empty_rows(ex, nq, nk):
     """With nq > nk under the causal mask the first nq - nk queries precede every
     key: their allowed sets are empty (Y = 0, L = -inf, status EMPTY_ROW)."""
