@@ -380,7 +380,7 @@ def run_gpu(args, w):
     # are also bracketed by events recorded on this stream by the library.
     K = args.steps
     ev = {role: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(K)] for role in (ex.KERNEL_FWD, ex.KERNEL_BWD)}
+                 for _ in range(K)] for role in (ex.KERNEL_FWD, ex.KERNEL_BWD, ex.KERNEL_DELTA)}
     for pairs_ in ev.values():
         for a, b in pairs_:
             a.record(stream)
@@ -399,6 +399,7 @@ def run_gpu(args, w):
     launches = ex.launch_count() - launches0
     ms = rank_max(start.elapsed_time(stop))
     kern_ms = {role: sum(a.elapsed_time(b) for a, b in ev[role]) / K for role in ev}
+    delta_ms = kern_ms.pop(ex.KERNEL_DELTA)
 
     # Forward alone.
     for _ in range(args.warmup):
@@ -455,6 +456,16 @@ def run_gpu(args, w):
     roofline["kernel_ms"] = {"fwd": kern_ms[ex.KERNEL_FWD], "bwd": kern_ms[ex.KERNEL_BWD]}
     roofline_fwd = kernel_roofline(args, w, "fwd", f_fwd / (kern_ms[ex.KERNEL_FWD] * 1e-3) / 1e12,
                                    peaks, peak_kind)
+    # delta_i = dY_i . Y_i: reads Y and dY, writes delta and L log2(e) (both padded to 128 rows).
+    e = 4 if w.dtype == "f32" else 2
+    npad = (w.n + 127) // 128 * 128
+    delta_bytes = w.B * w.H * (2 * w.n * w.v * e + 4 * w.n + 8 * npad)
+    hbm = float(peaks["hbm_gbs"])
+    roofline_delta = {"kernel": "delta", "bound": "hbm",
+                      "achieved": delta_bytes / (delta_ms * 1e-3) / 1e9, "peak": hbm,
+                      "unit": "GB/s", "frac": delta_bytes / (delta_ms * 1e-3) / 1e9 / hbm,
+                      "peak_kind": f"copy bandwidth, of {peak_kind}", "bytes": delta_bytes,
+                      "ms": delta_ms}
     line = {
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
@@ -470,6 +481,7 @@ def run_gpu(args, w):
         "gpu_launches": launches,
         "roofline": roofline,
         "roofline_fwd": roofline_fwd,
+        "roofline_delta": roofline_delta,
         "e2e": e2e,
         "clocks": clocks.summary(),
     }

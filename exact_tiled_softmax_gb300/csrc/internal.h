@@ -74,9 +74,13 @@ void before_launch(int role, cudaStream_t s);
 void record_error(const char* where, int code, const char* detail);
 void after_launch(int role, cudaStream_t s);
 
-// SIMT fp32 kernels (any dtype, d, v <= 256).
+// SIMT fp32 kernels (any dtype, d, v <= 256).  launch_simt_bwd uses the
+// register-tiled reverse kernel for d, v in {64, 128} and the general one
+// otherwise.
 cudaError_t launch_simt_fwd(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_simt_bwd(const BwdArgs& a, cudaStream_t s);
+bool simt_bwd_rt_supported(const Problem& p);
+cudaError_t launch_simt_bwd_rt(const BwdArgs& a, cudaStream_t s);
 
 // delta_i = dY_i . Y_i and the log2-scaled row statistic (memory-bound
 // preprocessing of the reverse pass), written to padded [BH][npad] vectors.

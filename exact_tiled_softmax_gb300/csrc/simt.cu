@@ -462,6 +462,7 @@ cudaError_t launch_simt_fwd(const FwdArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_simt_bwd(const BwdArgs& a, cudaStream_t s) {
+  if (simt_bwd_rt_supported(a.p)) return launch_simt_bwd_rt(a, s);
   return a.p.dtype == kF32 ? bwd_dispatch<float>(a, s) : bwd_dispatch<__nv_bfloat16>(a, s);
 }
 
