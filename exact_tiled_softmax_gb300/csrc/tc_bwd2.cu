@@ -487,18 +487,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float da[4] = {d4.x, d4.y, d4.z, d4.w};
           float pv[4], gv[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float pp = ex2(fmaf(__uint_as_float(s[e + u]), sl2, -la[u]));
-            if (!((allow >> (16 * c + e + u)) & 1u)) pp = 0.f;
+          for (int u = 0; u < 4; u += 2) {  // query pairs: packed fp32 arithmetic
+            float x0, x1;
+            ffma2(x0, x1, __uint_as_float(s[e + u]), __uint_as_float(s[e + u + 1]), sl2, sl2,
+                  -la[u], -la[u + 1]);
+            float pp[2] = {ex2(x0), ex2(x1)};
+#pragma unroll
+            for (int w = 0; w < 2; ++w)
+              if (!((allow >> (16 * c + e + u + w)) & 1u)) pp[w] = 0.f;
+            float dq0 = __uint_as_float(dp[e + u]), dq1 = __uint_as_float(dp[e + u + 1]);
             if constexpr (kDrop) {
               // Replayed mask: dV takes p xi s; dP = xi s (G_i . V_j).
-              const float xs = ((keep >> (16 * c + e + u)) & 1u) ? p.drop_scale : 0.f;
-              pv[u] = pp * xs;
-              gv[u] = pp * (__uint_as_float(dp[e + u]) * xs - da[u]);
+              const float xs0 = ((keep >> (16 * c + e + u)) & 1u) ? p.drop_scale : 0.f;
+              const float xs1 = ((keep >> (16 * c + e + u + 1)) & 1u) ? p.drop_scale : 0.f;
+              fmul2(dq0, dq1, dq0, dq1, xs0, xs1);
+              fmul2(pv[u], pv[u + 1], pp[0], pp[1], xs0, xs1);
             } else {
-              pv[u] = pp;
-              gv[u] = pp * (__uint_as_float(dp[e + u]) - da[u]);
+              pv[u] = pp[0];
+              pv[u + 1] = pp[1];
             }
+            float t0, t1;
+            fadd2(t0, t1, dq0, dq1, -da[u], -da[u + 1]);
+            fmul2(gv[u], gv[u + 1], pp[0], pp[1], t0, t1);
           }
           pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
           pk[e / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
@@ -858,8 +868,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint4 rw;  // dropout: Philox words of keys kc + 16c + 8*(e/8) .. of row i
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
-          float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, -lse2));
-          float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -lse2));
+          float x0, x1;  // packed fp32 arithmetic over the key pair
+          ffma2(x0, x1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]), sl2, sl2, -lse2, -lse2);
+          float p0 = ex2(x0);
+          float p1 = ex2(x1);
           if (!((allow >> (16 * c + e)) & 1u)) p0 = 0.f;
           if (!((allow >> (16 * c + e + 1)) & 1u)) p1 = 0.f;
           float dp0 = __uint_as_float(dp[e]), dp1 = __uint_as_float(dp[e + 1]);
@@ -871,7 +883,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             dp0 *= (w & 0xFFFFu) >= p.drop_t ? p.drop_scale : 0.f;
             dp1 *= w >= (p.drop_t << 16) ? p.drop_scale : 0.f;
           }
-          dk[e / 2] = pack_bf16x2(p0 * (dp0 - dl), p1 * (dp1 - dl));
+          float t0, t1, g0, g1;
+          fadd2(t0, t1, dp0, dp1, -dl, -dl);
+          fmul2(g0, g1, p0, p1, t0, t1);
+          dk[e / 2] = pack_bf16x2(g0, g1);
         }
         tmem_st8(tD + 32 * g + 8 * c, dk);
       }

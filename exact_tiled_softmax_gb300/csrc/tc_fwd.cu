@@ -441,14 +441,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           for (int cc = 0; cc < 128; ++cc)
             if (!((mw[cc >> 5] >> (cc & 31)) & 1u)) s[cc] = __float_as_uint(-INFINITY);
         }
-        // Row maximum as 8 independent chains, then a short tree.
+        // Row maximum as 8 independent chains of three-input maxima, then a short tree.
         float mx8[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(s[k]);
 #pragma unroll
-        for (int cc = 8; cc < 128; ++cc) mx8[cc & 7] = fmaxf(mx8[cc & 7], __uint_as_float(s[cc]));
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int cc = 8; cc + 16 <= 128; cc += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mx8[k] = fmax3(mx8[k], __uint_as_float(s[cc + k]), __uint_as_float(s[cc + 8 + k]));
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], __uint_as_float(s[120 + k]));
+        const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
+                               fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
         const float tmax = mx * sl2;  // -inf stays -inf (sl2 > 0)
         const float m_new = fmaxf(m_ref, tmax);
         const bool need = (m_ref != -INFINITY) && (m_new > m_ref + kRescaleThreshold);
@@ -469,16 +474,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           }
         }
         const float neg = m_ref == -INFINITY ? 0.f : -m_ref;
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
+        float sum2[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // partial sums
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t pk[32];
           uint4 rw;  // dropout: Philox words of keys kt*128 + 64*half + 8*(e/4) ..
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float p0 = ex2(fmaf(__uint_as_float(s[64 * half + 2 * e]), sl2, neg));
-            const float p1 = ex2(fmaf(__uint_as_float(s[64 * half + 2 * e + 1]), sl2, neg));
-            sum4[e & 3] += p0 + p1;  // the row sum is of the undropped p
+            float x0, x1;  // s * c log2(e) - m for the key pair, one packed FMA
+            ffma2(x0, x1, __uint_as_float(s[64 * half + 2 * e]),
+                  __uint_as_float(s[64 * half + 2 * e + 1]), sl2, sl2, neg, neg);
+            const float p0 = ex2(x0);
+            const float p1 = ex2(x1);
+            // the row sum is of the undropped p (packed adds into 4 pairs of partials)
+            fadd2(sum2[e & 3][0], sum2[e & 3][1], sum2[e & 3][0], sum2[e & 3][1], p0, p1);
             if constexpr (kDrop) {
               // Keys 2e and 2e+1 of this half are the low and high halves of one word.
               if ((e & 3) == 0)
@@ -492,7 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           }
           tmem_st32(t_s + 32 * half, pk);
         }
-        const float rowsum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        const float rowsum = ((sum2[0][0] + sum2[0][1]) + (sum2[1][0] + sum2[1][1])) +
+                             ((sum2[2][0] + sum2[2][1]) + (sum2[3][0] + sum2[3][1]));
         tmem_st_wait();
         l += rowsum;
         tc_fence_before();
