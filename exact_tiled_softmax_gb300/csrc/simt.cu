@@ -318,33 +318,50 @@ __device__ __forceinline__ void delta_store(const DeltaArgs& a, size_t row, floa
   }
 }
 
+// One row per group of G lanes (G = v / elements per 16-byte vector, so each
+// lane reads one vector of Y and one of dY per row); a grid-stride loop over
+// rows with kRows rows in flight per group.  The trip count is the same for
+// every lane, so the group reductions run converged.
+constexpr int kDeltaRows = 4;
+
 template <typename T, int G>
 __global__ void __launch_bounds__(256) delta_vec_kernel(DeltaArgs a) {
   constexpr int E = 16 / sizeof(T);  // elements per 16-byte vector
-  const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const size_t row = gtid / G;
-  const int lane = (int)(gtid % G);
-  const int vecs = a.v / E;
-  float acc = 0.f;
-  if (row < a.rows) {
-    const size_t bh = row / a.npad;
-    const int i = static_cast<int>(row - bh * a.npad);
-    if (i < a.n) {
-      const size_t src = (bh * a.n + i) * a.v;
-      const uint4* y = reinterpret_cast<const uint4*>(static_cast<const T*>(a.Y) + src);
-      const uint4* g = reinterpret_cast<const uint4*>(static_cast<const T*>(a.dY) + src);
-      for (int k = lane; k < vecs; k += G) {
-        uint4 va = __ldcs(y + k), vb = __ldcs(g + k);
-        const T* ea = reinterpret_cast<const T*>(&va);
-        const T* eb = reinterpret_cast<const T*>(&vb);
+  constexpr int R = kDeltaRows;
+  const int lane = static_cast<int>(threadIdx.x % G);
+  const size_t groups = static_cast<size_t>(gridDim.x) * (256 / G);
+  const size_t group = static_cast<size_t>(blockIdx.x) * (256 / G) + threadIdx.x / G;
+  const size_t iters = (a.rows + groups * R - 1) / (groups * R);
+  for (size_t it = 0; it < iters; ++it) {
+    const size_t r0 = (it * groups + group) * R;
+    uint4 va[R], vb[R];
+    bool live[R];
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+      const size_t row = r0 + u;
+      const size_t bh = row / a.npad;
+      const int i = static_cast<int>(row - bh * a.npad);
+      live[u] = row < a.rows && i < a.n;
+      if (live[u]) {
+        const size_t src = (bh * a.n + i) * a.v;
+        va[u] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const T*>(a.Y) + src) + lane);
+        vb[u] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const T*>(a.dY) + src) + lane);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+      float acc = 0.f;
+      if (live[u]) {
+        const T* ea = reinterpret_cast<const T*>(&va[u]);
+        const T* eb = reinterpret_cast<const T*>(&vb[u]);
 #pragma unroll
         for (int e = 0; e < E; ++e) acc = fmaf(Elem<T>::cvt(ea[e]), Elem<T>::cvt(eb[e]), acc);
       }
+#pragma unroll
+      for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (r0 + u < a.rows && lane == 0) delta_store(a, r0 + u, acc);
     }
   }
-#pragma unroll
-  for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < a.rows && lane == 0) delta_store(a, row, acc);
 }
 
 template <typename T>
@@ -435,10 +452,11 @@ cudaError_t delta_dispatch(const BwdArgs& a, cudaStream_t s) {
   const int vecs = p.v / E;
   before_launch(kKernDelta, s);
   if (p.v % E == 0 && (vecs & (vecs - 1)) == 0 && vecs <= 32) {
-    // G lanes per row, one 16-byte vector per lane per step.
+    // G lanes per row, one 16-byte vector per lane per row; one wave of 8 CTAs
+    // per SM (fewer when there are fewer rows).
     const int G = vecs;
-    const size_t threads = d.rows * G;
-    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    const size_t need = (d.rows * G + 255) / 256;
+    const unsigned blocks = (unsigned)(need < 152 * 8 ? need : 152 * 8);
     switch (G) {
       case 1: delta_vec_kernel<T, 1><<<blocks, 256, 0, s>>>(d); break;
       case 2: delta_vec_kernel<T, 2><<<blocks, 256, 0, s>>>(d); break;
