@@ -119,3 +119,23 @@ def test_equal_lengths_match_the_square_call(ex):
     torch.cuda.synchronize()
     for a, b in ((y, y2), (L, L2), (dq, dq2), (dk, dk2), (dv, dv2)):
         assert torch.equal(a, b)
+
+
+def test_cross_benchmark_size_sampled_heads(ex):
+    """bench.py --nk 8192: the benchmark workload's 4096 queries against 8192 keys,
+    forward and reverse, sampled heads against the oracle."""
+    import dataclasses
+    from sampling import head_slices
+    w = dataclasses.replace(workloads.workload(3), nk=8192)
+    x = workloads.make_inputs(w)
+    dev = torch.device("cuda:0")
+    q, k, v, g = (t.to(dev) for t in (x.Q, x.K, x.V, x.dY))
+    y, L = ex.fwd(q, k, v, w.scale, w.mask)
+    dq, dk, dv = ex.bwd(q, k, v, y, g, L, w.scale, w.mask)
+    torch.cuda.synchronize()
+    heads = [0, w.B * w.H - 1]
+    Q, K, V, G = (head_slices(t, heads)[:, None] for t in (x.Q, x.K, x.V, x.dY))
+    Yr, Lr = dense.forward_rect(Q, K, V, w.scale, w.mask_kind)
+    dQ, dK, dV, _ = dense.backward_rect(Q, K, V, G, w.scale, w.mask_kind)
+    ref = dict(Y=Yr[:, 0], L=Lr[:, 0], dQ=dQ[:, 0], dK=dK[:, 0], dV=dV[:, 0])
+    compare("bf16", dict(Y=y, L=L, dQ=dq, dK=dk, dV=dv), ref, heads=heads)

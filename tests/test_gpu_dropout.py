@@ -143,3 +143,27 @@ def test_bad_probability_is_rejected(ex):
     for q in (1.0, -0.5, float("nan")):
         with pytest.raises(ex.ExattnError):
             _run(ex, w, x, q, 1)
+
+
+def test_dropout_benchmark_size_sampled_heads(ex):
+    """The benchmark workload with dropout 0.1 (bench.py --dropout 0.1, seed 1234),
+    compared with the oracle on sampled heads."""
+    from oracle import masks
+    from sampling import head_slices
+    w = workloads.workload(3)
+    x = workloads.make_inputs(w)
+    q, seed = 0.1, 1234
+    got = _run(ex, w, x, q, seed)
+    heads = [0, 77, w.B * w.H - 1]
+    Q, K, V, G = (head_slices(t, heads) for t in (x.Q, x.K, x.V, x.dY))
+    allowed = masks.allowed_matrix(w.n, w.mask_kind)
+    ks = philox.keep_scale(q)
+    ref = {key: [] for key in ("Y", "L", "dQ", "dK", "dV")}
+    for idx, h in enumerate(heads):
+        keep = philox.keep_mask(h, w.n, w.n, q, seed)
+        yy, ll = dense.head_forward_dropout(Q[idx], K[idx], V[idx], w.scale, allowed, keep, ks)
+        a, b, c, _ = dense.head_backward_dropout(Q[idx], K[idx], V[idx], G[idx], w.scale,
+                                                 allowed, keep, ks)
+        for key, val in zip(("Y", "L", "dQ", "dK", "dV"), (yy, ll, a, b, c)):
+            ref[key].append(val)
+    compare("bf16", got, {key: np.stack(val) for key, val in ref.items()}, heads=heads)

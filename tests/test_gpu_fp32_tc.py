@@ -95,3 +95,29 @@ def test_fp32_large_magnitudes_keep_the_fp32_bar(ex):
     Yr, Lr = dense.forward(Q.double().numpy(), K.double().numpy(), V.double().numpy(),
                            1 / math.sqrt(128), workloads.MASK_CAUSAL)
     compare("f32", dict(Y=y, L=L), dict(Y=Yr, L=Lr))
+
+
+def test_fp32_benchmark_step_full_size_sampled_heads(ex):
+    """The benchmark workload in fp32 (bench.py --dtype f32): the 3xTF32 forward and
+    the register-tiled reverse pass, compared with the oracle on sampled heads."""
+    import dataclasses
+    from oracle import masks
+    from sampling import head_slices
+    w = dataclasses.replace(workloads.workload(3), dtype="f32")
+    x = workloads.make_inputs(w)
+    dev = torch.device("cuda:0")
+    q, k, v, g = (t.to(dev) for t in (x.Q, x.K, x.V, x.dY))
+    y, L = ex.fwd(q, k, v, w.scale, w.mask)
+    dq, dk, dv = ex.bwd(q, k, v, y, g, L, w.scale, w.mask)
+    torch.cuda.synchronize()
+    heads = [0, 77, w.B * w.H - 1]
+    Q, K, V, G = (head_slices(t, heads) for t in (x.Q, x.K, x.V, x.dY))
+    allowed = masks.allowed_matrix(w.n, w.mask_kind)
+    ref = {key: [] for key in ("Y", "L", "dQ", "dK", "dV")}
+    for h in range(len(heads)):
+        yy, ll = dense.head_forward(Q[h], K[h], V[h], w.scale, allowed)
+        a, b, cc, _ = dense.head_backward(Q[h], K[h], V[h], G[h], w.scale, allowed)
+        for key, val in zip(("Y", "L", "dQ", "dK", "dV"), (yy, ll, a, b, cc)):
+            ref[key].append(val)
+    compare("f32", dict(Y=y, L=L, dQ=dq, dK=dk, dV=dv),
+            {key: np.stack(val) for key, val in ref.items()}, heads=heads)

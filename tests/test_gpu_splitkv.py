@@ -117,3 +117,24 @@ def test_splitkv_agrees_with_last_rows_of_full_forward(ex, nq):
     torch.cuda.synchronize()
     assert (y_dec.float() - y_full[:, :, -nq:].float()).abs().max() <= 2e-2
     assert (L_dec - L_full[:, :, -nq:]).abs().max() <= 1e-4
+
+
+@pytest.mark.parametrize("nq", [1, 16])
+def test_decode_benchmark_size_sampled_heads(ex, nq):
+    """bench.py --decode (B=8, H=32, nk=16384, d=v=128, bf16, causal, automatic
+    chunk count): the register kernel for nq = 1, the tensor-core chunks for 16;
+    sampled heads against the oracle."""
+    from sampling import head_slices
+    w = workloads.decode_workload(nq)
+    Q, K, V, _ = workloads.make_decode_inputs(w.B, w.H, w.nq, w.nk, w.d, w.v, w.dtype, w.mask,
+                                              seed=w.seed)
+    dev = torch.device("cuda:0")
+    Y, L = ex.fwd_splitkv(Q.to(dev), K.to(dev), V.to(dev), w.scale, w.mask, num_splits=0)
+    torch.cuda.synchronize()
+    heads = [0, 100, w.B * w.H - 1]
+    Qh, Kh, Vh = (head_slices(t, heads) for t in (Q, K, V))
+    Yr, Lr = dense.forward_rect(Qh[:, None], Kh[:, None], Vh[:, None], w.scale,
+                                workloads.MASK_KINDS[w.mask])
+    Yg = Y.reshape(-1, nq, w.v)[heads]
+    Lg = L.reshape(-1, nq)[heads]
+    _check("bf16", Yg, Lg, Yr[:, 0], Lr[:, 0])
