@@ -18,7 +18,6 @@ std::atomic<unsigned long long> g_launches{0};
 std::atomic<void*> g_hook_start[kKernRoles];
 std::atomic<void*> g_hook_stop[kKernRoles];
 
-constexpr size_t kStatusBytes = 256;
 constexpr int kMaxWidth = 256;
 constexpr int kMaxN = 1 << 20;
 

@@ -11,6 +11,12 @@ namespace exattn {
 enum { kMaskNone = 0, kMaskCausal = 1, kMaskWindow = 2, kMaskBitmask = 3 };
 enum { kF32 = 0, kBF16 = 1 };
 
+// The workspace of every entry point starts with a 256-byte area that the
+// host clears before the first launch: word 0 is the status word; word
+// kSchedWord counts the items the persistent dK/dV kernel has handed out.
+constexpr size_t kStatusBytes = 256;
+constexpr int kSchedWord = 16;
+
 // One attention problem: BH = batch*heads independent slices; n query rows
 // against nk keys (nk == n for self-attention shapes).  Query i sits at
 // absolute position i + nk - n: the causal and window masks compare keys with

@@ -64,6 +64,7 @@ struct Bwd2Params {
   __nv_bfloat16* dK;
   __nv_bfloat16* dV;
   unsigned* status;
+  unsigned* sched;  // item counter of the persistent dK/dV kernel (zero at launch)
   uint32_t drop_t, seed_lo, seed_hi;  // dropout (kernel variants kDrop only)
   float drop_scale;
 };
@@ -205,12 +206,29 @@ struct KvLayout {
   static constexpr int VEC_OFF = STAGE_OFF + NST * STAGE;  // per stage: delta[128], lse2[128]
   static constexpr int BAR_OFF = VEC_OFF + NST * 1024;
   static constexpr int B_KV = 0, B_QF = 1, B_QE = B_QF + NST, B_SDP = B_QE + NST, B_DS = B_SDP + 2,
-                       B_DONE = B_DS + 2, B_DRAIN = B_DONE + 1, NBAR = B_DRAIN + 1;
+                       B_DONE = B_DS + 2, B_DRAIN = B_DONE + 1, B_KVFREE = B_DRAIN + 1,
+                       B_ACCFREE = B_KVFREE + 1, B_ITEMF = B_ACCFREE + 1, B_ITEME = B_ITEMF + 2,
+                       NBAR = B_ITEME + 2;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int CLS_OFF = MISC_OFF + 16;
   static constexpr int TOTAL = CLS_OFF + 2 * (kMaxBlocks / 32) * 4;
   static_assert(TOTAL <= 232448, "shared memory");
 };
+
+// Item t of the persistent dK/dV kernel -> (key block kb, slice bh).  Items
+// come in groups of kHeadGroup slices; inside a group the key blocks ascend
+// (under the causal mask the low ones reach the most query blocks), so the
+// CTAs at work at one time share the Q and dY rows of a few slices in L2.
+constexpr int kHeadGroup = 16;
+__device__ __forceinline__ void kv_item(int t, int nkb, int BH, int& kb, int& bh) {
+  const int per = kHeadGroup * nkb;
+  const int grp = t / per;
+  const int base = grp * kHeadGroup;
+  const int hg = min(kHeadGroup, BH - base);
+  const int r = t - grp * per;
+  kb = r / hg;
+  bh = base + (r - kb * hg);
+}
 
 template <int D, int V, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -223,23 +241,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int k) { return bar0 + 8u * k; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(misc + 2);  // two entries
   uint32_t* anyb = reinterpret_cast<uint32_t*>(smem + Lay::CLS_OFF);
   uint32_t* notallb = anyb + kMaxBlocks / 32;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kb = blockIdx.x;  // causal: low key blocks have the most query blocks
-  const int bh = blockIdx.y;
   const int n = p.n, nk = p.nk, off = p.off;
-  const int k0 = kb * kBN;
-  const int nqb = (n + kBM - 1) / kBM;
-  int qb_begin = 0, qb_end = nqb;
-  // Query rows that can reach this key block (row i sits at i + off).
-  if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow)
-    qb_begin = min(nqb, max(0, k0 - off) / kBM);
-  if (p.mask_kind == kMaskWindow) {
-    const int last = min(k0 + kBN, nk) - 1 - off + p.window - 1;
-    qb_end = last < 0 ? 0 : min(nqb, last / kBM + 1);
-  }
+  const int nqb = (n + kBM - 1) / kBM, nkb = (nk + kBN - 1) / kBN;
+  const int items = nkb * p.BH;
+  // Persistent: the TMA warp takes items from a counter (CTA c starts with
+  // item c, then item gridDim.x + the counter's old value) and hands each
+  // to the other roles through a two-entry ring in shared memory (-1 ends).
+  // Ring and barrier phases run on across items.
+  // Query blocks that can reach key block kb (row i sits at i + off).
+  auto q_range = [&](int kb, int& qb_begin, int& qb_end) {
+    const int k0 = kb * kBN;
+    qb_begin = 0;
+    qb_end = nqb;
+    if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow)
+      qb_begin = min(nqb, max(0, k0 - off) / kBM);
+    if (p.mask_kind == kMaskWindow) {
+      const int last = min(k0 + kBN, nk) - 1 - off + p.window - 1;
+      qb_end = last < 0 ? 0 : min(nqb, last / kBM + 1);
+    }
+  };
 
   if ((sbase & 1023u) != 0u) {
     if (threadIdx.x == 0) raise_status(p.status, kStatusTimeout);
@@ -254,9 +279,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int h = 0; h < 2; ++h) {
       mbar_init(bar(Lay::B_SDP + h), 1);
       mbar_init(bar(Lay::B_DS + h), 8 * 32);
+      mbar_init(bar(Lay::B_ITEMF + h), 1);
+      mbar_init(bar(Lay::B_ITEME + h), 1 + kEwWarps);  // MMA warp + elementwise warps
     }
     mbar_init(bar(Lay::B_DONE), 1);
     mbar_init(bar(Lay::B_DRAIN), 1);
+    mbar_init(bar(Lay::B_KVFREE), 1);
+    mbar_init(bar(Lay::B_ACCFREE), kEwWarps * 32);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -267,15 +296,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x < 2 * (kMaxBlocks / 32)) anyb[threadIdx.x] = 0u;
   __syncthreads();
-  if (p.mask_kind == kMaskBitmask)
-    build_bitmask_table(p, true, kb, qb_begin, qb_end, anyb, notallb);
+  if (p.mask_kind == kMaskBitmask) {
+    // The bitmask tile table is per key block: the launcher gives every CTA
+    // exactly one item for this mask kind (item blockIdx.x).
+    int kb0, bh0, qb_begin, qb_end;
+    kv_item(blockIdx.x, nkb, p.BH, kb0, bh0);
+    q_range(kb0, qb_begin, qb_end);
+    build_bitmask_table(p, true, kb0, qb_begin, qb_end, anyb, notallb);
+  }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
   const uint32_t tA = tmem, tB = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + V;
-  auto cls_of = [&](int qb) {
+  auto cls_of = [&](int qb, int kb) {
     return classify_tile(p, qb, kb, (anyb[qb >> 5] >> (qb & 31)) & 1u,
                          (notallb[qb >> 5] >> (qb & 31)) & 1u);
+  };
+  // Consumers: item nitem from the ring (waits for it, then frees the entry).
+  auto take_item = [&](int nitem, int& t) {
+    const int e = nitem & 1;
+    if (!mbar_wait(bar(Lay::B_ITEMF + e), (nitem >> 1) & 1, abort_flag)) return false;
+    t = item_ring[e];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(Lay::B_ITEME + e));
+    return true;
   };
 
   if (warp == kWarpTMA) {
@@ -287,45 +331,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&p.tdy);
     }
     const uint64_t keep = policy_evict_last();
-    if (leader) {
-      mbar_arrive_expect_tx(bar(Lay::B_KV), Lay::KBYTES + Lay::VBYTES);
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(sbase + Lay::K_OFF + c * 16384, &p.tk, bar(Lay::B_KV), 64 * c, k0, bh, keep);
-      for (int c = 0; c < V / 64; ++c)
-        tma_load_3d(sbase + Lay::V_OFF + c * 16384, &p.tv, bar(Lay::B_KV), 64 * c, k0, bh, keep);
-    }
-    int it = 0;
-    int last_phase[NST];
-    for (int s = 0; s < NST; ++s) last_phase[s] = -1;
+    int it = 0, kv_loads = 0;
     bool ok = true;
-    for (int qb = qb_begin; qb < qb_end; ++qb) {
-      if (cls_of(qb) == kEmpty) continue;
-      const int slot = it % NST, phase = (it / NST) & 1;
-      ++it;
-      if (!(ok = mbar_wait(bar(Lay::B_QE + slot), phase ^ 1, abort_flag))) break;
-      const uint32_t st = sbase + Lay::STAGE_OFF + slot * Lay::STAGE;
-      const uint32_t fb = bar(Lay::B_QF + slot);
+    int t = blockIdx.x;
+    for (int nitem = 0;; ++nitem) {
+      const int e = nitem & 1;
+      if (nitem >= 2 && !(ok = mbar_wait(bar(Lay::B_ITEME + e), ((nitem >> 1) - 1) & 1, abort_flag)))
+        break;
       if (leader) {
-        mbar_arrive_expect_tx(fb, Lay::QBYTES + Lay::YBYTES + 1024);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(st + c * 16384, &p.tq, fb, 64 * c, qb * kBM, bh, keep);
-        for (int c = 0; c < V / 64; ++c)
-          tma_load_3d(st + Lay::QBYTES + c * 16384, &p.tdy, fb, 64 * c, qb * kBM, bh, keep);
-        const size_t vo = static_cast<size_t>(bh) * p.npad + qb * kBM;
-        const uint32_t vec = sbase + Lay::VEC_OFF + slot * 1024;
-        bulk_load(vec, p.delta + vo, 512, fb);
-        bulk_load(vec + 512, p.lse2 + vo, 512, fb);
+        item_ring[e] = t < items ? t : -1;
+        mbar_arrive(bar(Lay::B_ITEMF + e));
       }
-      last_phase[slot] = phase;
+      if (t >= items) break;
+      // Claim the next item now; its value is first needed after this one.
+      unsigned claimed = 0u;
+      if (lane == 0) claimed = atomicAdd(p.sched, 1u);
+      int kb, bh;
+      kv_item(t, nkb, p.BH, kb, bh);
+      const int k0 = kb * kBN;
+      int qb_begin, qb_end;
+      q_range(kb, qb_begin, qb_end);
+      // K and V of the item once the previous item's S^T, dP^T products no longer read them.
+      if (nitem > 0 && !(ok = mbar_wait(bar(Lay::B_KVFREE), (nitem - 1) & 1, abort_flag))) break;
+      if (leader) {
+        mbar_arrive_expect_tx(bar(Lay::B_KV), Lay::KBYTES + Lay::VBYTES);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sbase + Lay::K_OFF + c * 16384, &p.tk, bar(Lay::B_KV), 64 * c, k0, bh, keep);
+        for (int c = 0; c < V / 64; ++c)
+          tma_load_3d(sbase + Lay::V_OFF + c * 16384, &p.tv, bar(Lay::B_KV), 64 * c, k0, bh, keep);
+      }
+      ++kv_loads;
+      for (int qb = qb_begin; qb < qb_end; ++qb) {
+        if (cls_of(qb, kb) == kEmpty) continue;
+        const int slot = it % NST, phase = (it / NST) & 1;
+        ++it;
+        if (!(ok = mbar_wait(bar(Lay::B_QE + slot), phase ^ 1, abort_flag))) break;
+        const uint32_t st = sbase + Lay::STAGE_OFF + slot * Lay::STAGE;
+        const uint32_t fb = bar(Lay::B_QF + slot);
+        if (leader) {
+          mbar_arrive_expect_tx(fb, Lay::QBYTES + Lay::YBYTES + 1024);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(st + c * 16384, &p.tq, fb, 64 * c, qb * kBM, bh, keep);
+          for (int c = 0; c < V / 64; ++c)
+            tma_load_3d(st + Lay::QBYTES + c * 16384, &p.tdy, fb, 64 * c, qb * kBM, bh, keep);
+          const size_t vo = static_cast<size_t>(bh) * p.npad + qb * kBM;
+          const uint32_t vec = sbase + Lay::VEC_OFF + slot * 1024;
+          bulk_load(vec, p.delta + vo, 512, fb);
+          bulk_load(vec + 512, p.lse2 + vo, 512, fb);
+        }
+      }
+      if (!ok) break;
+      const unsigned next = __shfl_sync(0xFFFFFFFFu, claimed, 0);
+      t = static_cast<int>(min(next + gridDim.x, static_cast<unsigned>(items)));
     }
     __syncwarp();
     if (!ok && leader) {
       raise_status(p.status, kStatusTimeout);
       *abort_flag = 1;
     }
-    for (int s = 0; s < NST; ++s)
-      if (last_phase[s] >= 0) mbar_wait(bar(Lay::B_QF + s), last_phase[s], abort_flag);
-    mbar_wait(bar(Lay::B_KV), 0, abort_flag);
+    // The last fill of each stage (iteration i = it - 1 - u fills stage i % NST).
+    for (int u = 0; u < NST && u < it; ++u) {
+      const int i = it - 1 - u;
+      mbar_wait(bar(Lay::B_QF + i % NST), (i / NST) & 1, abort_flag);
+    }
+    if (kv_loads > 0) mbar_wait(bar(Lay::B_KV), (kv_loads - 1) & 1, abort_flag);
   } else if (warp == kWarpMMA) {
     const bool leader = elect_one();
     constexpr uint32_t kIdHalf = idesc_bf16(kBN, 64, false, false);
@@ -336,8 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dSt = sdesc_sw128(sbase + Lay::STAGE_OFF, 16, 1024);     // K-major view
     const uint64_t dSm = sdesc_sw128(sbase + Lay::STAGE_OFF, 16384, 1024);  // MN-major view
     constexpr uint32_t kStage16 = Lay::STAGE >> 4, kQ16 = Lay::QBYTES >> 4;
-    bool ok = mbar_wait(bar(Lay::B_KV), 0, abort_flag);
-    tc_fence_after();
+    bool ok = true;
     // Per query block i and half h: A_h(i) = dP^T_h, S^T_h (N = 64) and
     // B_h(i) = dV, dK updates from that half (K = 64).  Issue order
     //   A0(0) A1(0) | B0(0) A0(1) B1(0) A1(1) | B0(1) A0(2) B1(1) A1(2) | ...
@@ -374,42 +442,76 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
-    auto next_qb = [&](int qb) {
-      for (++qb; qb < qb_end; ++qb)
-        if (cls_of(qb) != kEmpty) return qb;
-      return qb_end;
+    // K and V are read by the A products only: once the item's last ones are
+    // issued, the commit lets the TMA warp load the next item's K and V while
+    // this item's last block is still in the elementwise warps and B products.
+    auto free_kv = [&]() {
+      if (leader) tc_commit(bar(Lay::B_KVFREE));
     };
-    int qb = next_qb(qb_begin - 1);
     int it = 0;
-    if (ok && qb < qb_end) {
-      if ((ok = mbar_wait(bar(Lay::B_QF + 0), 0, abort_flag))) {
-        tc_fence_after();
-        issue_a(0, 0);
-        issue_a(1, 0);
-      }
-    }
-    while (ok && qb < qb_end) {
-      const int slot = it % NST;
-      const int qb_n = next_qb(qb);
-      const bool more = qb_n < qb_end;
-      const int slot_n = (it + 1) % NST, phase_n = ((it + 1) / NST) & 1;
-      if (!(ok = mbar_wait(bar(Lay::B_DS + 0), it & 1, abort_flag))) break;
+    for (int nitem = 0; ok; ++nitem) {
+      int t;
+      if (!(ok = take_item(nitem, t))) break;
+      if (t < 0) break;
+      int kb, bh;
+      kv_item(t, nkb, p.BH, kb, bh);
+      int qb_begin, qb_end;
+      q_range(kb, qb_begin, qb_end);
+      auto next_qb = [&](int qb) {
+        for (++qb; qb < qb_end; ++qb)
+          if (cls_of(qb, kb) != kEmpty) return qb;
+        return qb_end;
+      };
+      if (!(ok = mbar_wait(bar(Lay::B_KV), nitem & 1, abort_flag))) break;
       tc_fence_after();
-      issue_b(0, slot, it == 0);
-      if (more) {
-        if (!(ok = mbar_wait(bar(Lay::B_QF + slot_n), phase_n, abort_flag))) break;
+      int qb = next_qb(qb_begin - 1);
+      int qb_n = qb < qb_end ? next_qb(qb) : qb_end;
+      const int it0 = it;  // first query block of this item
+      if (qb < qb_end) {
+        if (!(ok = mbar_wait(bar(Lay::B_QF + it % NST), (it / NST) & 1, abort_flag))) break;
         tc_fence_after();
-        issue_a(0, slot_n);
+        issue_a(0, it % NST);
+        issue_a(1, it % NST);
       }
-      if (!(ok = mbar_wait(bar(Lay::B_DS + 1), it & 1, abort_flag))) break;
-      tc_fence_after();
-      issue_b(1, slot, false);
-      if (leader) tc_commit(bar(Lay::B_QE + slot));  // Q_i, dY_i no longer read
-      if (more) issue_a(1, slot_n);
-      qb = qb_n;
-      ++it;
+      if (qb_n >= qb_end) free_kv();
+      while (qb < qb_end) {
+        const int slot = it % NST;
+        const bool more = qb_n < qb_end;
+        const int qb_nn = more ? next_qb(qb_n) : qb_end;
+        const int slot_n = (it + 1) % NST, phase_n = ((it + 1) / NST) & 1;
+        if (!(ok = mbar_wait(bar(Lay::B_DS + 0), it & 1, abort_flag))) break;
+        tc_fence_after();
+        if (it == it0 && nitem > 0) {
+          // dV, dK restart from zero: the previous item's epilogue has read them.
+          if (!(ok = mbar_wait(bar(Lay::B_ACCFREE), (nitem - 1) & 1, abort_flag))) break;
+          tc_fence_after();
+        }
+        issue_b(0, slot, it == it0);
+        if (more) {
+          if (!(ok = mbar_wait(bar(Lay::B_QF + slot_n), phase_n, abort_flag))) break;
+          tc_fence_after();
+          issue_a(0, slot_n);
+        }
+        if (!(ok = mbar_wait(bar(Lay::B_DS + 1), it & 1, abort_flag))) break;
+        tc_fence_after();
+        issue_b(1, slot, false);
+        if (leader) tc_commit(bar(Lay::B_QE + slot));  // Q_i, dY_i no longer read
+        if (more) {
+          issue_a(1, slot_n);
+          if (qb_nn >= qb_end) free_kv();
+        }
+        qb = qb_n;
+        qb_n = qb_nn;
+        ++it;
+      }
+      if (!ok) break;
+      if (it == it0 && nitem > 0) {
+        // An item without query blocks: keep "done" at most one phase ahead.
+        if (!(ok = mbar_wait(bar(Lay::B_ACCFREE), (nitem - 1) & 1, abort_flag))) break;
+      }
+      if (leader) tc_commit(bar(Lay::B_DONE));  // dV, dK of the item complete
+      __syncwarp();
     }
-    if (leader) tc_commit(bar(Lay::B_DONE));
     __syncwarp();
     if (!ok && leader) {
       raise_status(p.status, kStatusTimeout);
@@ -422,125 +524,131 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 32g..32g+31 (half h = g / 2).
     const int g = warp >> 2, wl = warp & 3, h = g >> 1;
     const int r = wl * 32 + lane;
-    const int j = k0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(wl * 32) << 16;
     const float sl2 = p.sl2;
     int it = 0;
     bool ok = true;
-    for (int qb = qb_begin; qb < qb_end; ++qb) {
-      const int cls = cls_of(qb);
-      if (cls == kEmpty) continue;
-      const int slot = it % NST;
-      // Dropout: lane e draws the keep bits of query q0 + 32g + e for this warp's
-      // 32 keys; the transpose gives each lane (key) its bits over the 32 queries.
-      uint32_t keep = 0xFFFFFFFFu;
-      if constexpr (kDrop)
-        keep = transpose_bits32(keep_word32(p, bh, qb * kBM + 32 * g + lane, k0 + wl * 32), lane);
-      if (!(ok = mbar_wait(bar(Lay::B_SDP + h), it & 1, abort_flag))) break;
-      tc_fence_after();
-      const float* dvec = reinterpret_cast<const float*>(smem + Lay::VEC_OFF + slot * 1024);
-      const float* lvec = dvec + 128;
-      const int q0 = qb * kBM;
-      const int cb = 32 * g;
-      uint32_t allow = 0xFFFFFFFFu;
-      if (cls == kPartial) {
-        if (j >= nk) {
-          allow = 0u;
-        } else if (p.mask_kind == kMaskCausal) {
-          allow = range_bits(j - off - q0 - cb, 31);
-        } else if (p.mask_kind == kMaskWindow) {
-          allow = range_bits(j - off - q0 - cb, j - off + p.window - 1 - q0 - cb);
-        } else if (p.mask_kind == kMaskBitmask) {
-          allow = 0u;
-          const uint32_t* col = p.bits + (j >> 5);
-#pragma unroll 4
-          for (int e = 0; e < 32; ++e) {
-            const int i = q0 + cb + e;
-            if (i < n)
-              allow |= ((__ldg(col + static_cast<size_t>(i) * p.words_per_row) >> (j & 31)) & 1u)
-                       << e;
-          }
-        }
-      }
-      uint32_t sv[2][16], dpv[2][16];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        tmem_ld16(tA + lane_off + cb + 16 * c, sv[c]);
-        tmem_ld16(tB + lane_off + cb + 16 * c, dpv[c]);
-      }
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        reg_fence(sv[c]);
-        reg_fence(dpv[c]);
-      }
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {  // two chunks of 16 queries
-        const uint32_t (&s)[16] = sv[c];
-        const uint32_t (&dp)[16] = dpv[c];
-        uint32_t pk[8], dk[8];
-#pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lvec + cb + 16 * c + e);
-          const float4 d4 = *reinterpret_cast<const float4*>(dvec + cb + 16 * c + e);
-          const float la[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float da[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4], gv[4];
-#pragma unroll
-          for (int u = 0; u < 4; u += 2) {  // query pairs: packed fp32 arithmetic
-            float x0, x1;
-            ffma2(x0, x1, __uint_as_float(s[e + u]), __uint_as_float(s[e + u + 1]), sl2, sl2,
-                  -la[u], -la[u + 1]);
-            float pp[2] = {ex2(x0), ex2(x1)};
-#pragma unroll
-            for (int w = 0; w < 2; ++w)
-              if (!((allow >> (16 * c + e + u + w)) & 1u)) pp[w] = 0.f;
-            float dq0 = __uint_as_float(dp[e + u]), dq1 = __uint_as_float(dp[e + u + 1]);
-            if constexpr (kDrop) {
-              // Replayed mask: dV takes p xi s; dP = xi s (G_i . V_j).
-              const float xs0 = ((keep >> (16 * c + e + u)) & 1u) ? p.drop_scale : 0.f;
-              const float xs1 = ((keep >> (16 * c + e + u + 1)) & 1u) ? p.drop_scale : 0.f;
-              fmul2(dq0, dq1, dq0, dq1, xs0, xs1);
-              fmul2(pv[u], pv[u + 1], pp[0], pp[1], xs0, xs1);
-            } else {
-              pv[u] = pp[0];
-              pv[u + 1] = pp[1];
-            }
-            float t0, t1;
-            fadd2(t0, t1, dq0, dq1, -da[u], -da[u + 1]);
-            fmul2(gv[u], gv[u + 1], pp[0], pp[1], t0, t1);
-          }
-          pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
-          pk[e / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-          dk[e / 2] = pack_bf16x2(gv[0], gv[1]);
-          dk[e / 2 + 1] = pack_bf16x2(gv[2], gv[3]);
-        }
-        // P^T / dS^T (bf16 pairs) over the first 16 columns of this group's range.
-        tmem_st8(tA + lane_off + cb + 8 * c, pk);
-        tmem_st8(tB + lane_off + cb + 8 * c, dk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(Lay::B_DS + h));
-      ++it;
-    }
-    if (!ok) {
-      raise_status(p.status, kStatusTimeout);
-      *abort_flag = 1;
-    }
-    // Epilogue: group 0 writes dV rows, group 1 dK rows (scaled by c).
-    if (g < 2) {
-      bool have = ok && it > 0;
-      if (have) {
-        have = mbar_wait(bar(Lay::B_DONE), 0, abort_flag);
+    for (int nitem = 0; ok; ++nitem) {
+      int t;
+      if (!(ok = take_item(nitem, t))) break;
+      if (t < 0) break;
+      int kb, bh;
+      kv_item(t, nkb, p.BH, kb, bh);
+      const int k0 = kb * kBN, j = k0 + r;
+      int qb_begin, qb_end;
+      q_range(kb, qb_begin, qb_end);
+      const int it0 = it;
+      for (int qb = qb_begin; qb < qb_end; ++qb) {
+        const int cls = cls_of(qb, kb);
+        if (cls == kEmpty) continue;
+        const int slot = it % NST;
+        // Dropout: lane e draws the keep bits of query q0 + 32g + e for this warp's
+        // 32 keys; the transpose gives each lane (key) its bits over the 32 queries.
+        uint32_t keep = 0xFFFFFFFFu;
+        if constexpr (kDrop)
+          keep = transpose_bits32(keep_word32(p, bh, qb * kBM + 32 * g + lane, k0 + wl * 32), lane);
+        if (!(ok = mbar_wait(bar(Lay::B_SDP + h), it & 1, abort_flag))) break;
         tc_fence_after();
+        const float* dvec = reinterpret_cast<const float*>(smem + Lay::VEC_OFF + slot * 1024);
+        const float* lvec = dvec + 128;
+        const int q0 = qb * kBM;
+        const int cb = 32 * g;
+        uint32_t allow = 0xFFFFFFFFu;
+        if (cls == kPartial) {
+          if (j >= nk) {
+            allow = 0u;
+          } else if (p.mask_kind == kMaskCausal) {
+            allow = range_bits(j - off - q0 - cb, 31);
+          } else if (p.mask_kind == kMaskWindow) {
+            allow = range_bits(j - off - q0 - cb, j - off + p.window - 1 - q0 - cb);
+          } else if (p.mask_kind == kMaskBitmask) {
+            allow = 0u;
+            const uint32_t* col = p.bits + (j >> 5);
+#pragma unroll 4
+            for (int e = 0; e < 32; ++e) {
+              const int i = q0 + cb + e;
+              if (i < n)
+                allow |= ((__ldg(col + static_cast<size_t>(i) * p.words_per_row) >> (j & 31)) & 1u)
+                         << e;
+            }
+          }
+        }
+        uint32_t sv[2][16], dpv[2][16];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld16(tA + lane_off + cb + 16 * c, sv[c]);
+          tmem_ld16(tB + lane_off + cb + 16 * c, dpv[c]);
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          reg_fence(sv[c]);
+          reg_fence(dpv[c]);
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {  // two chunks of 16 queries
+          const uint32_t (&s)[16] = sv[c];
+          const uint32_t (&dp)[16] = dpv[c];
+          uint32_t pk[8], dk[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lvec + cb + 16 * c + e);
+            const float4 d4 = *reinterpret_cast<const float4*>(dvec + cb + 16 * c + e);
+            const float la[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float da[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], gv[4];
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {  // query pairs: packed fp32 arithmetic
+              float x0, x1;
+              ffma2(x0, x1, __uint_as_float(s[e + u]), __uint_as_float(s[e + u + 1]), sl2, sl2,
+                    -la[u], -la[u + 1]);
+              float pp[2] = {ex2(x0), ex2(x1)};
+#pragma unroll
+              for (int w = 0; w < 2; ++w)
+                if (!((allow >> (16 * c + e + u + w)) & 1u)) pp[w] = 0.f;
+              float dq0 = __uint_as_float(dp[e + u]), dq1 = __uint_as_float(dp[e + u + 1]);
+              if constexpr (kDrop) {
+                // Replayed mask: dV takes p xi s; dP = xi s (G_i . V_j).
+                const float xs0 = ((keep >> (16 * c + e + u)) & 1u) ? p.drop_scale : 0.f;
+                const float xs1 = ((keep >> (16 * c + e + u + 1)) & 1u) ? p.drop_scale : 0.f;
+                fmul2(dq0, dq1, dq0, dq1, xs0, xs1);
+                fmul2(pv[u], pv[u + 1], pp[0], pp[1], xs0, xs1);
+              } else {
+                pv[u] = pp[0];
+                pv[u + 1] = pp[1];
+              }
+              float t0, t1;
+              fadd2(t0, t1, dq0, dq1, -da[u], -da[u + 1]);
+              fmul2(gv[u], gv[u + 1], pp[0], pp[1], t0, t1);
+            }
+            pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
+            pk[e / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+            dk[e / 2] = pack_bf16x2(gv[0], gv[1]);
+            dk[e / 2 + 1] = pack_bf16x2(gv[2], gv[3]);
+          }
+          // P^T / dS^T (bf16 pairs) over the first 16 columns of this group's range.
+          tmem_st8(tA + lane_off + cb + 8 * c, pk);
+          tmem_st8(tB + lane_off + cb + 8 * c, dk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(Lay::B_DS + h));
+        ++it;
       }
-      const int W = g == 0 ? V : D;
-      const uint32_t tsrc = (g == 0 ? tdV : tdK) + lane_off;
-      const float mul = g == 0 ? 1.f : p.scale;
-      __nv_bfloat16* dst =
-          (g == 0 ? p.dV : p.dK) + (static_cast<size_t>(bh) * nk + (j < nk ? j : 0)) * W;
-      for (int ch = 0; ch < W / 16; ++ch) {
+      if (!ok) break;
+      // Epilogue, all four groups: g = 0, 1 write the two column halves of the
+      // dV rows, g = 2, 3 those of the dK rows (scaled by c).
+      if (!(ok = mbar_wait(bar(Lay::B_DONE), nitem & 1, abort_flag))) break;
+      tc_fence_after();
+      const bool have = it > it0;
+      const bool is_dv = g < 2;
+      const int W = is_dv ? V : D;
+      const int c0 = (g & 1) * (W / 2);
+      const uint32_t tsrc = (is_dv ? tdV : tdK) + lane_off + c0;
+      const float mul = is_dv ? 1.f : p.scale;
+      __nv_bfloat16* dst = (is_dv ? p.dV : p.dK) +
+                           (static_cast<size_t>(bh) * nk + (j < nk ? j : 0)) * W + c0;
+      for (int ch = 0; ch < W / 32; ++ch) {
         uint32_t o[16];
         if (have) {
           tmem_ld16(tsrc + ch * 16, o);
@@ -560,6 +668,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           d4[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
         }
       }
+      tc_fence_before();
+      mbar_arrive(bar(Lay::B_ACCFREE));  // dV, dK read: the next item may restart them
+    }
+    if (!ok) {
+      raise_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
     }
   }
 
@@ -966,6 +1080,7 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
   p.dK = static_cast<__nv_bfloat16*>(a.dK);
   p.dV = static_cast<__nv_bfloat16*>(a.dV);
   p.status = a.status;
+  p.sched = a.status + kSchedWord;
   p.drop_t = pr.drop_t;
   p.seed_lo = pr.seed_lo;
   p.seed_hi = pr.seed_hi;
@@ -983,7 +1098,17 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
   }
   const int nkb = (pr.nk + kBN - 1) / kBN, nqb = (pr.n + kBM - 1) / kBM;
   before_launch(kKernBwd, s);
-  kv<<<dim3(nkb, pr.BH), kThreads, KvLayout<D, D>::TOTAL, s>>>(p);
+  // Persistent dK/dV kernel: one CTA per SM, items handed out by a counter;
+  // one item per CTA for the bitmask, whose tile table the kernel builds once.
+  const int kv_items = nkb * pr.BH;
+  int kv_grid = kv_items;
+  if (pr.mask_kind != kMaskBitmask) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    kv_grid = kv_items < sms ? kv_items : sms;
+  }
+  kv<<<kv_grid, kThreads, KvLayout<D, D>::TOTAL, s>>>(p);
   e = cudaGetLastError();
   if (e == cudaSuccess) {
     before_launch(kKernBwdQ, s);
