@@ -379,8 +379,15 @@ def run_gpu(args, w):
     # Timed region: K full steps; the forward and reverse kernels of every step
     # are also bracketed by events recorded on this stream by the library.
     K = args.steps
+    # The split tensor-core reverse pass (bf16, d = v in {64, 128}) also brackets
+    # its dQ kernel, so the dK/dV kernel's time is the difference.
+    split_bwd = (w.dtype == "bf16" and w.d == w.v and w.d in (64, 128)
+                 and args.path == "auto"
+                 and (w.mask != "bitmask" or max(w.n, w.n_keys) <= 256 * 128))
+    roles = (ex.KERNEL_FWD, ex.KERNEL_BWD, ex.KERNEL_DELTA) + ((ex.KERNEL_BWD_Q,) if split_bwd
+                                                              else ())
     ev = {role: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(K)] for role in (ex.KERNEL_FWD, ex.KERNEL_BWD, ex.KERNEL_DELTA)}
+                 for _ in range(K)] for role in roles}
     for pairs_ in ev.values():
         for a, b in pairs_:
             a.record(stream)
@@ -400,6 +407,7 @@ def run_gpu(args, w):
     ms = rank_max(start.elapsed_time(stop))
     kern_ms = {role: sum(a.elapsed_time(b) for a, b in ev[role]) / K for role in ev}
     delta_ms = kern_ms.pop(ex.KERNEL_DELTA)
+    bwd_q_ms = kern_ms.pop(ex.KERNEL_BWD_Q, None)
 
     # Forward alone.
     for _ in range(args.warmup):
@@ -454,6 +462,9 @@ def run_gpu(args, w):
     achieved = dom_flops / (kern_ms[dom] * 1e-3) / 1e12
     roofline = kernel_roofline(args, w, dom_name, achieved, peaks, peak_kind)
     roofline["kernel_ms"] = {"fwd": kern_ms[ex.KERNEL_FWD], "bwd": kern_ms[ex.KERNEL_BWD]}
+    if bwd_q_ms is not None:
+        roofline["kernel_ms"]["bwd_kv"] = kern_ms[ex.KERNEL_BWD] - bwd_q_ms
+        roofline["kernel_ms"]["bwd_q"] = bwd_q_ms
     roofline_fwd = kernel_roofline(args, w, "fwd", f_fwd / (kern_ms[ex.KERNEL_FWD] * 1e-3) / 1e12,
                                    peaks, peak_kind)
     # delta_i = dY_i . Y_i: reads Y and dY, writes delta and L log2(e) (both padded to 128 rows).

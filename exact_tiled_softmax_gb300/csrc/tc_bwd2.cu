@@ -53,6 +53,7 @@ enum : int { kEmpty = 0, kFull = 1, kPartial = 2 };
 
 struct Bwd2Params {
   CUtensorMap tq, tk, tv, tdy;
+  CUtensorMap tdk, tdv;  // dK, dV as store targets (dK/dV kernel)
   int n, npad, BH, mask_kind, window, words_per_row;
   int nk, off;  // keys, and the absolute position of query 0 (nk - n)
   const uint32_t* bits;
@@ -204,11 +205,15 @@ struct KvLayout {
   static constexpr int STAGE = QBYTES + YBYTES;
   static constexpr int NST = 2;
   static constexpr int VEC_OFF = STAGE_OFF + NST * STAGE;  // per stage: delta[128], lse2[128]
-  static constexpr int BAR_OFF = VEC_OFF + NST * 1024;
+  // Epilogue tile: kBN rows of dV, then of dK, as 64-column boxes (128-byte swizzle).
+  static constexpr int EPI_OFF = VEC_OFF + NST * 1024;
+  static constexpr int EPI = kBN * (D > V ? D : V) * 2;
+  static constexpr int BAR_OFF = EPI_OFF + EPI;
   static constexpr int B_KV = 0, B_QF = 1, B_QE = B_QF + NST, B_SDP = B_QE + NST, B_DS = B_SDP + 2,
                        B_DONE = B_DS + 2, B_DRAIN = B_DONE + 1, B_KVFREE = B_DRAIN + 1,
                        B_ACCFREE = B_KVFREE + 1, B_ITEMF = B_ACCFREE + 1, B_ITEME = B_ITEMF + 2,
-                       NBAR = B_ITEME + 2;
+                       B_EPIFV = B_ITEME + 2, B_EPIV = B_EPIFV + 1, B_EPIFK = B_EPIV + 1,
+                       B_EPIK = B_EPIFK + 1, NBAR = B_EPIK + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int CLS_OFF = MISC_OFF + 16;
   static constexpr int TOTAL = CLS_OFF + 2 * (kMaxBlocks / 32) * 4;
@@ -286,6 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(Lay::B_DRAIN), 1);
     mbar_init(bar(Lay::B_KVFREE), 1);
     mbar_init(bar(Lay::B_ACCFREE), kEwWarps * 32);
+    mbar_init(bar(Lay::B_EPIFV), 1);   // the dK store of the previous item has read the tile
+    mbar_init(bar(Lay::B_EPIV), 8 * 32);
+    mbar_init(bar(Lay::B_EPIFK), 1);   // the dV store has read the tile
+    mbar_init(bar(Lay::B_EPIK), 8 * 32);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -329,8 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&p.tk);
       prefetch_tmap(&p.tv);
       prefetch_tmap(&p.tdy);
+      prefetch_tmap(&p.tdk);
+      prefetch_tmap(&p.tdv);
     }
-    const uint64_t keep = policy_evict_last();
+    const uint64_t keep = policy_evict_last();   // Q, dY: read by every key block of the slice
+    const uint64_t once = policy_evict_first();  // K, V: read by one item
     int it = 0, kv_loads = 0;
     bool ok = true;
     int t = blockIdx.x;
@@ -356,11 +368,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) {
         mbar_arrive_expect_tx(bar(Lay::B_KV), Lay::KBYTES + Lay::VBYTES);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sbase + Lay::K_OFF + c * 16384, &p.tk, bar(Lay::B_KV), 64 * c, k0, bh, keep);
+          tma_load_3d(sbase + Lay::K_OFF + c * 16384, &p.tk, bar(Lay::B_KV), 64 * c, k0, bh, once);
         for (int c = 0; c < V / 64; ++c)
-          tma_load_3d(sbase + Lay::V_OFF + c * 16384, &p.tv, bar(Lay::B_KV), 64 * c, k0, bh, keep);
+          tma_load_3d(sbase + Lay::V_OFF + c * 16384, &p.tv, bar(Lay::B_KV), 64 * c, k0, bh, once);
       }
       ++kv_loads;
+      // The next item's K and V go into L2 after this item's first stage load,
+      // so that their load (issued once this item's last A products are done)
+      // does not wait on HBM.
+      int t_next = -1;
+      auto prefetch_next = [&]() {
+        t_next = static_cast<int>(
+            min(__shfl_sync(0xFFFFFFFFu, claimed, 0) + gridDim.x, static_cast<unsigned>(items)));
+        if (t_next < items && leader) {
+          int kbn, bhn;
+          kv_item(t_next, nkb, p.BH, kbn, bhn);
+          for (int c = 0; c < D / 64; ++c) tma_prefetch_3d(&p.tk, 64 * c, kbn * kBN, bhn);
+          for (int c = 0; c < V / 64; ++c) tma_prefetch_3d(&p.tv, 64 * c, kbn * kBN, bhn);
+        }
+      };
       for (int qb = qb_begin; qb < qb_end; ++qb) {
         if (cls_of(qb, kb) == kEmpty) continue;
         const int slot = it % NST, phase = (it / NST) & 1;
@@ -379,10 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_load(vec, p.delta + vo, 512, fb);
           bulk_load(vec + 512, p.lse2 + vo, 512, fb);
         }
+        if (t_next < 0) prefetch_next();
       }
       if (!ok) break;
-      const unsigned next = __shfl_sync(0xFFFFFFFFu, claimed, 0);
-      t = static_cast<int>(min(next + gridDim.x, static_cast<unsigned>(items)));
+      if (t_next < 0) prefetch_next();
+      t = t_next;
     }
     __syncwarp();
     if (!ok && leader) {
@@ -636,45 +663,81 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++it;
       }
       if (!ok) break;
-      // Epilogue, all four groups: g = 0, 1 write the two column halves of the
-      // dV rows, g = 2, 3 those of the dK rows (scaled by c).
+      // Epilogue.  Every group reads its D/2 columns of dV (g = 0, 1) or dK
+      // (g = 2, 3; scaled by c) and releases the accumulators at once.  The
+      // rows then leave through one shared-memory tile in the TMA layout
+      // (64-column boxes, 128-byte swizzle) and TMA stores, which write whole
+      // lines and clip rows past nk: dV first, then dK in the same tile.
       if (!(ok = mbar_wait(bar(Lay::B_DONE), nitem & 1, abort_flag))) break;
       tc_fence_after();
-      const bool have = it > it0;
+      constexpr int HC = D / 2;  // columns per group (D == V)
       const bool is_dv = g < 2;
-      const int W = is_dv ? V : D;
-      const int c0 = (g & 1) * (W / 2);
-      const uint32_t tsrc = (is_dv ? tdV : tdK) + lane_off + c0;
-      const float mul = is_dv ? 1.f : p.scale;
-      __nv_bfloat16* dst = (is_dv ? p.dV : p.dK) +
-                           (static_cast<size_t>(bh) * nk + (j < nk ? j : 0)) * W + c0;
-      for (int ch = 0; ch < W / 32; ++ch) {
-        uint32_t o[16];
-        if (have) {
-          tmem_ld16(tsrc + ch * 16, o);
+      const int c0 = (g & 1) * HC;
+      uint32_t pk[HC / 2];
+      {
+        uint32_t o[HC / 16][16];
+        if (it > it0) {
+#pragma unroll
+          for (int c = 0; c < HC / 16; ++c)
+            tmem_ld16((is_dv ? tdV : tdK) + lane_off + c0 + 16 * c, o[c]);
           tmem_ld_wait();
-          reg_fence(o);
+#pragma unroll
+          for (int c = 0; c < HC / 16; ++c) reg_fence(o[c]);
         } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = 0u;
-        }
-        if (j < nk) {
-          uint32_t ov[8];
+          for (int c = 0; c < HC / 16; ++c)
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            ov[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
-          uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 16);
-          d4[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
-          d4[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
+            for (int e = 0; e < 16; ++e) o[c][e] = 0u;
         }
+        const float mul = is_dv ? 1.f : p.scale;
+#pragma unroll
+        for (int e = 0; e < HC / 2; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(o[e >> 3][(2 * e) & 15]) * mul,
+                              __uint_as_float(o[e >> 3][(2 * e + 1) & 15]) * mul);
       }
       tc_fence_before();
       mbar_arrive(bar(Lay::B_ACCFREE));  // dV, dK read: the next item may restart them
+      if (warp == kEwWarps / 2) {
+        // Issuer of the dK stores (thread 256): the previous item's have read the tile.
+        if (lane == 0) {
+          bulk_wait_read_all();
+          mbar_arrive(bar(Lay::B_EPIFV));
+        }
+        __syncwarp();
+      }
+      if (!(ok = mbar_wait(bar(is_dv ? Lay::B_EPIFV : Lay::B_EPIFK), nitem & 1, abort_flag))) break;
+      const uint32_t tile = sbase + Lay::EPI_OFF;
+#pragma unroll
+      for (int u = 0; u < HC / 8; ++u) {
+        const int col = c0 + 8 * u;
+        const uint32_t addr = tile + (col >> 6) * (kBN * 128) + r * 128 +
+                              ((((col & 63) >> 3) ^ (r & 7)) << 4);
+        st_shared_v4(addr, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(is_dv ? Lay::B_EPIV : Lay::B_EPIK));
+      if (threadIdx.x == (is_dv ? 0 : 32 * (kEwWarps / 2))) {
+        if (mbar_wait(bar(is_dv ? Lay::B_EPIV : Lay::B_EPIK), nitem & 1, abort_flag)) {
+          const CUtensorMap* map = is_dv ? &p.tdv : &p.tdk;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) tma_store_3d(map, tile + c * (kBN * 128), 64 * c, k0, bh);
+          bulk_commit();
+          if (is_dv) {
+            bulk_wait_read_all();
+            mbar_arrive(bar(Lay::B_EPIFK));
+          }
+        } else {
+          ok = false;
+        }
+      }
+      ok = __all_sync(0xFFFFFFFFu, ok);
     }
     if (!ok) {
       raise_status(p.status, kStatusTimeout);
       *abort_flag = 1;
     }
+    // The stores' issuers: all of their stores complete before the CTA ends.
+    if (threadIdx.x == 0 || threadIdx.x == 32 * (kEwWarps / 2)) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -1061,7 +1124,9 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
   Bwd2Params p;
   if (!make_tmap_bf16(&p.tq, a.Q, D, pr.n, pr.BH) || !make_tmap_bf16(&p.tk, a.K, D, pr.nk, pr.BH) ||
       !make_tmap_bf16(&p.tv, a.V, D, pr.nk, pr.BH) ||
-      !make_tmap_bf16(&p.tdy, a.dY, D, pr.n, pr.BH))
+      !make_tmap_bf16(&p.tdy, a.dY, D, pr.n, pr.BH) ||
+      !make_tmap_bf16(&p.tdk, a.dK, D, pr.nk, pr.BH) ||
+      !make_tmap_bf16(&p.tdv, a.dV, D, pr.nk, pr.BH))
     return cudaErrorInvalidValue;
   p.n = pr.n;
   p.nk = pr.nk;
@@ -1114,6 +1179,7 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
     before_launch(kKernBwdQ, s);
     qk<<<dim3(nqb, pr.BH), kThreads, QLayout<D, D>::TOTAL, s>>>(p);
     e = cudaGetLastError();
+    after_launch(kKernBwdQ, s);
   }
   after_launch(kKernBwd, s);
   return e;
