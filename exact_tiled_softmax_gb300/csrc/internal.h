@@ -12,8 +12,9 @@ enum { kMaskNone = 0, kMaskCausal = 1, kMaskWindow = 2, kMaskBitmask = 3 };
 enum { kF32 = 0, kBF16 = 1 };
 
 // The workspace of every entry point starts with a 256-byte area that the
-// host clears before the first launch: word 0 is the status word; word
-// kSchedWord counts the items the persistent dK/dV kernel has handed out.
+// host clears before the first launch: word 0 is the status word; words
+// kSchedWord and kSchedWord + 1 count the items that the persistent kernels
+// of one call (forward; or dK/dV, then dQ) have handed out.
 constexpr size_t kStatusBytes = 256;
 constexpr int kSchedWord = 16;
 

@@ -54,6 +54,7 @@ enum : int { kEmpty = 0, kFull = 1, kPartial = 2 };
 struct Bwd2Params {
   CUtensorMap tq, tk, tv, tdy;
   CUtensorMap tdk, tdv;  // dK, dV as store targets (dK/dV kernel)
+  CUtensorMap tdq;       // dQ as a store target (dQ kernel)
   int n, npad, BH, mask_kind, window, words_per_row;
   int nk, off;  // keys, and the absolute position of query 0 (nk - n)
   const uint32_t* bits;
@@ -65,7 +66,7 @@ struct Bwd2Params {
   __nv_bfloat16* dK;
   __nv_bfloat16* dV;
   unsigned* status;
-  unsigned* sched;  // item counter of the persistent dK/dV kernel (zero at launch)
+  unsigned* sched;  // item counters of the dK/dV ([0]) and dQ ([1]) kernels (zero at launch)
   uint32_t drop_t, seed_lo, seed_hi;  // dropout (kernel variants kDrop only)
   float drop_scale;
 };
@@ -759,14 +760,18 @@ struct QLayout {
   static constexpr int KBYTES = kBN * D * 2;
   static constexpr int VBYTES = kBN * V * 2;
   static constexpr int SLOT = KBYTES > VBYTES ? KBYTES : VBYTES;
-  static constexpr int NS = D == 128 ? 5 : 8;  // K and V tiles alternate in one ring
+  static constexpr int NS = D == 128 ? 4 : 8;  // K and V tiles alternate in one ring
   static constexpr int Q_OFF = 0;
   static constexpr int Y_OFF = QBYTES;
   static constexpr int SLOT_OFF = Y_OFF + YBYTES;
-  static constexpr int BAR_OFF = SLOT_OFF + NS * SLOT;
-  static constexpr int B_Q = 0, B_KVF = 1, B_KVE = B_KVF + NS, B_SDP = B_KVE + NS,
+  // Epilogue tile: kBM rows of dQ as 64-column boxes (128-byte swizzle).
+  static constexpr int EPI_OFF = SLOT_OFF + NS * SLOT;
+  static constexpr int BAR_OFF = EPI_OFF + kBM * D * 2;
+  static constexpr int B_Q = 0, B_QFREE = 1, B_KVF = 2, B_KVE = B_KVF + NS, B_SDP = B_KVE + NS,
                        B_DS = B_SDP + 1, B_SFREE = B_DS + 1, B_DONE = B_SFREE + 1,
-                       B_DRAIN = B_DONE + 1, NBAR = B_DRAIN + 1;
+                       B_DREAD = B_DONE + 1, B_ITEMF = B_DREAD + 1, B_ITEME = B_ITEMF + 2,
+                       B_EPIF = B_ITEME + 2, B_EPI = B_EPIF + 1, B_DRAIN = B_EPI + 1,
+                       NBAR = B_DRAIN + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int CLS_OFF = MISC_OFF + 16;
   static constexpr int TOTAL = CLS_OFF + 2 * (kMaxBlocks / 32) * 4;
@@ -784,23 +789,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int k) { return bar0 + 8u * k; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(misc + 2);  // two entries
   uint32_t* anyb = reinterpret_cast<uint32_t*>(smem + Lay::CLS_OFF);
   uint32_t* notallb = anyb + kMaxBlocks / 32;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nqb = (p.n + kBM - 1) / kBM;
-  const int qb = nqb - 1 - blockIdx.x;  // causal: high query blocks have the most key blocks
-  const int bh = blockIdx.y;
-  const int n = p.n;
-  const int q0 = qb * kBM;
-  const int q1 = min(q0 + kBM, n) - 1;
-  const int nk = p.nk, off = p.off;
-  const int nkb = (nk + kBN - 1) / kBN;
-  int kb_begin = 0, kb_end = nkb;
+  const int n = p.n, nk = p.nk, off = p.off;
+  const int nqb = (n + kBM - 1) / kBM, nkb = (nk + kBN - 1) / kBN;
+  const int items = nqb * p.BH;
+  // Persistent: as in the dK/dV kernel, the TMA warp takes items from a
+  // counter and hands them out through a two-entry ring; item t is
+  // (query block nqb - 1 - x, slice bh) with (x, bh) = kv_item(t): heaviest
+  // (causal) query blocks first inside each group of slices.
+  auto item_of = [&](int t, int& qb, int& bh) {
+    int x;
+    kv_item(t, nqb, p.BH, x, bh);
+    qb = nqb - 1 - x;
+  };
   // Key blocks that rows q0..q1 (at absolute positions q0 + off ..) can reach.
-  if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow)
-    kb_end = q1 + off < 0 ? 0 : min(nkb, (q1 + off) / kBN + 1);
-  if (p.mask_kind == kMaskWindow) kb_begin = min(kb_end, max(0, q0 + off - p.window + 1) / kBN);
+  auto kb_range = [&](int qb, int& kb_begin, int& kb_end) {
+    const int q0 = qb * kBM, q1 = min(q0 + kBM, n) - 1;
+    kb_begin = 0;
+    kb_end = nkb;
+    if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow)
+      kb_end = q1 + off < 0 ? 0 : min(nkb, (q1 + off) / kBN + 1);
+    if (p.mask_kind == kMaskWindow) kb_begin = min(kb_end, max(0, q0 + off - p.window + 1) / kBN);
+  };
 
   if ((sbase & 1023u) != 0u) {
     if (threadIdx.x == 0) raise_status(p.status, kStatusTimeout);
@@ -808,6 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     mbar_init(bar(Lay::B_Q), 1);
+    mbar_init(bar(Lay::B_QFREE), 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar(Lay::B_KVF + s), 1);
       mbar_init(bar(Lay::B_KVE + s), 1);
@@ -816,6 +831,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(Lay::B_DS), kEwWarps * 32);
     mbar_init(bar(Lay::B_SFREE), kEwWarps * 32);
     mbar_init(bar(Lay::B_DONE), 1);
+    mbar_init(bar(Lay::B_DREAD), kEwWarps * 32);  // the epilogue has read dQ
+    for (int e = 0; e < 2; ++e) {
+      mbar_init(bar(Lay::B_ITEMF + e), 1);
+      mbar_init(bar(Lay::B_ITEME + e), 1 + kEwWarps);  // MMA warp + elementwise warps
+    }
+    mbar_init(bar(Lay::B_EPIF), 1);  // the previous item's dQ stores have read the tile
+    mbar_init(bar(Lay::B_EPI), kEwWarps * 32);
     mbar_init(bar(Lay::B_DRAIN), 1);
     misc[1] = 0;
     fence_mbar_init();
@@ -827,15 +849,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x < 2 * (kMaxBlocks / 32)) anyb[threadIdx.x] = 0u;
   __syncthreads();
-  if (p.mask_kind == kMaskBitmask)
-    build_bitmask_table(p, false, qb, kb_begin, kb_end, anyb, notallb);
+  if (p.mask_kind == kMaskBitmask) {
+    // The tile table is per query block: the launcher gives every CTA exactly
+    // one item for this mask kind (item blockIdx.x).
+    int qb0, bh0, kb_begin, kb_end;
+    item_of(blockIdx.x, qb0, bh0);
+    kb_range(qb0, kb_begin, kb_end);
+    build_bitmask_table(p, false, qb0, kb_begin, kb_end, anyb, notallb);
+  }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
   const uint32_t tS = tmem, tD0 = tmem + 128, tQ = tmem + 384;
-  auto cls_of = [&](int kb) {
+  auto cls_of = [&](int qb, int kb) {
     return classify_tile(p, qb, kb, (anyb[kb >> 5] >> (kb & 31)) & 1u,
                          (notallb[kb >> 5] >> (kb & 31)) & 1u);
+  };
+  // Consumers: item nitem from the ring (waits for it, then frees the entry).
+  auto take_item = [&](int nitem, int& t) {
+    const int e = nitem & 1;
+    if (!mbar_wait(bar(Lay::B_ITEMF + e), (nitem >> 1) & 1, abort_flag)) return false;
+    t = item_ring[e];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(Lay::B_ITEME + e));
+    return true;
   };
 
   if (warp == kWarpTMA) {
@@ -845,56 +882,96 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&p.tk);
       prefetch_tmap(&p.tv);
       prefetch_tmap(&p.tdy);
+      prefetch_tmap(&p.tdq);
     }
     const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
-    if (leader) {
-      mbar_arrive_expect_tx(bar(Lay::B_Q), Lay::QBYTES + Lay::YBYTES);
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(sbase + Lay::Q_OFF + c * 16384, &p.tq, bar(Lay::B_Q), 64 * c, q0, bh, stream);
-      for (int c = 0; c < V / 64; ++c)
-        tma_load_3d(sbase + Lay::Y_OFF + c * 16384, &p.tdy, bar(Lay::B_Q), 64 * c, q0, bh, stream);
-    }
-    int it = 0;
-    int last_phase[NS];
-    for (int s = 0; s < NS; ++s) last_phase[s] = -1;
+    int it = 0, q_loads = 0;
     bool ok = true;
-    for (int kb = kb_begin; kb < kb_end && ok; ++kb) {
-      if (cls_of(kb) == kEmpty) continue;
-#pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
-        const int slot = it % NS, phase = (it / NS) & 1;
-        ++it;
-        if (!mbar_wait(bar(Lay::B_KVE + slot), phase ^ 1, abort_flag)) {
-          ok = false;
-          break;
+    int t = blockIdx.x;
+    for (int nitem = 0;; ++nitem) {
+      const int e = nitem & 1;
+      if (nitem >= 2 &&
+          !(ok = mbar_wait(bar(Lay::B_ITEME + e), ((nitem >> 1) - 1) & 1, abort_flag)))
+        break;
+      if (leader) {
+        item_ring[e] = t < items ? t : -1;
+        mbar_arrive(bar(Lay::B_ITEMF + e));
+      }
+      if (t >= items) break;
+      // Claim the next item now; its value is first needed after this one's first block.
+      unsigned claimed = 0u;
+      if (lane == 0) claimed = atomicAdd(p.sched + 1, 1u);
+      int qb, bh, kb_begin, kb_end;
+      item_of(t, qb, bh);
+      kb_range(qb, kb_begin, kb_end);
+      const int q0 = qb * kBM;
+      // Q and dY of the item once the previous item's S, dP products no longer read them.
+      if (nitem > 0 && !(ok = mbar_wait(bar(Lay::B_QFREE), (nitem - 1) & 1, abort_flag))) break;
+      if (leader) {
+        mbar_arrive_expect_tx(bar(Lay::B_Q), Lay::QBYTES + Lay::YBYTES);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sbase + Lay::Q_OFF + c * 16384, &p.tq, bar(Lay::B_Q), 64 * c, q0, bh, stream);
+        for (int c = 0; c < V / 64; ++c)
+          tma_load_3d(sbase + Lay::Y_OFF + c * 16384, &p.tdy, bar(Lay::B_Q), 64 * c, q0, bh, stream);
+      }
+      ++q_loads;
+      // The next item's Q and dY go into L2 after this item's first block.
+      int t_next = -1;
+      auto prefetch_next = [&]() {
+        t_next = static_cast<int>(
+            min(__shfl_sync(0xFFFFFFFFu, claimed, 0) + gridDim.x, static_cast<unsigned>(items)));
+        if (t_next < items && leader) {
+          int qbn, bhn;
+          item_of(t_next, qbn, bhn);
+          for (int c = 0; c < D / 64; ++c) tma_prefetch_3d(&p.tq, 64 * c, qbn * kBM, bhn);
+          for (int c = 0; c < V / 64; ++c) tma_prefetch_3d(&p.tdy, 64 * c, qbn * kBM, bhn);
         }
-        const uint32_t dst = sbase + Lay::SLOT_OFF + slot * Lay::SLOT;
-        if (leader) {
-          // V(t) first, then K(t): V(t) is needed one step earlier (for dP(t))
-          // and each slot is then reused two steps after its last reader.
-          if (kv == 1) {
-            mbar_arrive_expect_tx(bar(Lay::B_KVF + slot), Lay::KBYTES);
-            for (int c = 0; c < D / 64; ++c)
-              tma_load_3d(dst + c * 16384, &p.tk, bar(Lay::B_KVF + slot), 64 * c, kb * kBN, bh,
-                          keep);
-          } else {
-            mbar_arrive_expect_tx(bar(Lay::B_KVF + slot), Lay::VBYTES);
-            for (int c = 0; c < V / 64; ++c)
-              tma_load_3d(dst + c * 16384, &p.tv, bar(Lay::B_KVF + slot), 64 * c, kb * kBN, bh,
-                          keep);
+      };
+      for (int kb = kb_begin; kb < kb_end && ok; ++kb) {
+        if (cls_of(qb, kb) == kEmpty) continue;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+          const int slot = it % NS, phase = (it / NS) & 1;
+          ++it;
+          if (!mbar_wait(bar(Lay::B_KVE + slot), phase ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = sbase + Lay::SLOT_OFF + slot * Lay::SLOT;
+          if (leader) {
+            // V(t) first, then K(t): V(t) is needed one step earlier (for dP(t))
+            // and each slot is then reused two steps after its last reader.
+            if (kv == 1) {
+              mbar_arrive_expect_tx(bar(Lay::B_KVF + slot), Lay::KBYTES);
+              for (int c = 0; c < D / 64; ++c)
+                tma_load_3d(dst + c * 16384, &p.tk, bar(Lay::B_KVF + slot), 64 * c, kb * kBN, bh,
+                            keep);
+            } else {
+              mbar_arrive_expect_tx(bar(Lay::B_KVF + slot), Lay::VBYTES);
+              for (int c = 0; c < V / 64; ++c)
+                tma_load_3d(dst + c * 16384, &p.tv, bar(Lay::B_KVF + slot), 64 * c, kb * kBN, bh,
+                            keep);
+            }
           }
         }
-        last_phase[slot] = phase;
+        if (ok && t_next < 0) prefetch_next();
       }
+      if (!ok) break;
+      if (t_next < 0) prefetch_next();
+      t = t_next;
     }
     __syncwarp();
     if (!ok && leader) {
       raise_status(p.status, kStatusTimeout);
       *abort_flag = 1;
     }
-    for (int s = 0; s < NS; ++s)
-      if (last_phase[s] >= 0) mbar_wait(bar(Lay::B_KVF + s), last_phase[s], abort_flag);
-    mbar_wait(bar(Lay::B_Q), 0, abort_flag);
+    // Never leave with copies in flight: the last fill of every slot (fill
+    // i = it - 1 - u went to slot i % NS) and the last Q, dY.
+    for (int u = 0; u < NS && u < it; ++u) {
+      const int i = it - 1 - u;
+      mbar_wait(bar(Lay::B_KVF + i % NS), (i / NS) & 1, abort_flag);
+    }
+    if (q_loads > 0) mbar_wait(bar(Lay::B_Q), (q_loads - 1) & 1, abort_flag);
   } else if (warp == kWarpMMA) {
     const bool leader = elect_one();
     constexpr uint32_t kIdSS = idesc_bf16(kBM, kBN, false, false);
@@ -904,85 +981,105 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dSk = sdesc_sw128(sbase + Lay::SLOT_OFF, 16, 1024);
     const uint64_t dSm = sdesc_sw128(sbase + Lay::SLOT_OFF, 16384, 1024);
     constexpr uint32_t kSlot16 = Lay::SLOT >> 4;
-    bool ok = mbar_wait(bar(Lay::B_Q), 0, abort_flag);
-    tc_fence_after();
-    // Compact list of the key blocks to visit: recomputed on the fly.
-    auto next_kb = [&](int kb) {
-      for (++kb; kb < kb_end; ++kb)
-        if (cls_of(kb) != kEmpty) return kb;
-      return kb_end;
-    };
-    int kb = next_kb(kb_begin - 1);
-    int t = 0;
-    // Prologue: dP(0) -> D0, S(0) -> S.
-    if (ok && kb < kb_end) {
-      const int vs = 0, ks = 1;
-      if ((ok = mbar_wait(bar(Lay::B_KVF + ks), 0, abort_flag)) &&
-          (ok = mbar_wait(bar(Lay::B_KVF + vs), 0, abort_flag))) {
-        tc_fence_after();
-        if (leader) {
-#pragma unroll
-          for (int kk = 0; kk < V / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-            mma_ss(tD0, dYk + off, dSk + vs * kSlot16 + off, kIdSS, kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-            mma_ss(tS, dQk + off, dSk + ks * kSlot16 + off, kIdSS, kk > 0 ? 1u : 0u);
-          }
-          tc_commit(bar(Lay::B_SDP));
-          tc_commit(bar(Lay::B_KVE + vs));  // V(0) is no longer needed once dP(0) is done
-        }
-      }
-    }
-    while (ok && kb < kb_end) {
-      const int kb_next = next_kb(kb);
-      const int ks = (2 * t + 1) % NS;
-      if (kb_next < kb_end) {
-        // dP(t+1) -> the other buffer (its dS(t-1) was read by dQ(t-1), issued earlier).
-        const int it1 = 2 * (t + 1);
-        const int vs1 = it1 % NS, vp1 = (it1 / NS) & 1;
-        const int ks1 = (it1 + 1) % NS, kp1 = ((it1 + 1) / NS) & 1;
-        if (!(ok = mbar_wait(bar(Lay::B_KVF + vs1), vp1, abort_flag))) break;
-        tc_fence_after();
-        const uint32_t tD = tD0 + 128 * ((t + 1) & 1);
-        if (leader) {
-#pragma unroll
-          for (int kk = 0; kk < V / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-            mma_ss(tD, dYk + off, dSk + vs1 * kSlot16 + off, kIdSS, kk > 0 ? 1u : 0u);
-          }
-          tc_commit(bar(Lay::B_KVE + vs1));
-        }
-        // S(t+1) as soon as the elementwise warps hold S(t) in registers.
-        if (!(ok = mbar_wait(bar(Lay::B_SFREE), t & 1, abort_flag))) break;
-        if (!(ok = mbar_wait(bar(Lay::B_KVF + ks1), kp1, abort_flag))) break;
-        tc_fence_after();
-        if (leader) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-            mma_ss(tS, dQk + off, dSk + ks1 * kSlot16 + off, kIdSS, kk > 0 ? 1u : 0u);
-          }
-          tc_commit(bar(Lay::B_SDP));
-        }
-      }
-      if (!(ok = mbar_wait(bar(Lay::B_DS), t & 1, abort_flag))) break;
-      tc_fence_after();
-      // dQ += dS(t) K_t  (A = dS bf16 in TMEM over dP(t), keys packed; B = K_t MN-major)
-      const uint32_t tD = tD0 + 128 * (t & 1);
+    bool ok = true;
+    // Block t (counted across items) uses ring fills 2t (V) and 2t + 1 (K).
+    auto issue_dp = [&](int tt) {
+      const int vs = (2 * tt) % NS;
+      const uint32_t tD = tD0 + 128 * (tt & 1);
       if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tQ, tD + 32 * (kk >> 1) + 8 * (kk & 1), dSm + ks * kSlot16 + kk * 128, kIdDQ,
-                 (t > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar(Lay::B_KVE + ks));
+        for (int kk = 0; kk < V / 16; ++kk) {
+          const uint32_t o16 = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_ss(tD, dYk + o16, dSk + vs * kSlot16 + o16, kIdSS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(Lay::B_KVE + vs));  // V(t) is no longer needed once dP(t) is done
       }
-      kb = kb_next;
-      ++t;
+    };
+    auto issue_s = [&](int tt) {
+      const int ks = (2 * tt + 1) % NS;
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o16 = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_ss(tS, dQk + o16, dSk + ks * kSlot16 + o16, kIdSS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(Lay::B_SDP));
+      }
+    };
+    auto kv_full = [&](int fill) {
+      return mbar_wait(bar(Lay::B_KVF + fill % NS), (fill / NS) & 1, abort_flag);
+    };
+    int t = 0;
+    for (int nitem = 0; ok; ++nitem) {
+      int ti;
+      if (!(ok = take_item(nitem, ti))) break;
+      if (ti < 0) break;
+      int qb, bh, kb_begin, kb_end;
+      item_of(ti, qb, bh);
+      kb_range(qb, kb_begin, kb_end);
+      (void)bh;
+      // Compact list of the key blocks to visit: recomputed on the fly.
+      auto next_kb = [&](int kb) {
+        for (++kb; kb < kb_end; ++kb)
+          if (cls_of(qb, kb) != kEmpty) return kb;
+        return kb_end;
+      };
+      if (!(ok = mbar_wait(bar(Lay::B_Q), nitem & 1, abort_flag))) break;
+      tc_fence_after();
+      int kb = next_kb(kb_begin - 1);
+      int kb_n = kb < kb_end ? next_kb(kb) : kb_end;
+      const int t0 = t;
+      // Prologue: dP(t0) -> its buffer, S(t0) -> S once the previous item's
+      // last S is in the elementwise warps' registers.
+      if (kb < kb_end) {
+        if (!(ok = kv_full(2 * t))) break;
+        tc_fence_after();
+        issue_dp(t);
+        if (t > 0 && !(ok = mbar_wait(bar(Lay::B_SFREE), (t - 1) & 1, abort_flag))) break;
+        if (!(ok = kv_full(2 * t + 1))) break;
+        tc_fence_after();
+        issue_s(t);
+      }
+      // Q and dY are read by the S and dP products only.
+      if (kb_n >= kb_end && leader) tc_commit(bar(Lay::B_QFREE));
+      while (kb < kb_end) {
+        const bool more = kb_n < kb_end;
+        const int kb_nn = more ? next_kb(kb_n) : kb_end;
+        if (more) {
+          // dP(t+1) -> the other buffer (its dS(t-1) was read by dQ(t-1), issued earlier).
+          if (!(ok = kv_full(2 * (t + 1)))) break;
+          tc_fence_after();
+          issue_dp(t + 1);
+          // S(t+1) as soon as the elementwise warps hold S(t) in registers.
+          if (!(ok = mbar_wait(bar(Lay::B_SFREE), t & 1, abort_flag))) break;
+          if (!(ok = kv_full(2 * (t + 1) + 1))) break;
+          tc_fence_after();
+          issue_s(t + 1);
+          if (kb_nn >= kb_end && leader) tc_commit(bar(Lay::B_QFREE));
+        }
+        if (!(ok = mbar_wait(bar(Lay::B_DS), t & 1, abort_flag))) break;
+        tc_fence_after();
+        // dQ += dS(t) K_t  (A = dS bf16 in TMEM over dP(t), keys packed; B = K_t MN-major)
+        const int ks = (2 * t + 1) % NS;
+        const uint32_t tD = tD0 + 128 * (t & 1);
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts(tQ, tD + 32 * (kk >> 1) + 8 * (kk & 1), dSm + ks * kSlot16 + kk * 128, kIdDQ,
+                   (t > t0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(Lay::B_KVE + ks));
+        }
+        kb = kb_n;
+        kb_n = kb_nn;
+        ++t;
+      }
+      if (!ok) break;
+      // "dQ done" stays at most one phase ahead of the epilogue, also through
+      // items without key blocks.
+      if (nitem > 0 && !(ok = mbar_wait(bar(Lay::B_DREAD), (nitem - 1) & 1, abort_flag))) break;
+      if (leader) tc_commit(bar(Lay::B_DONE));
+      __syncwarp();
     }
-    if (leader) tc_commit(bar(Lay::B_DONE));
     __syncwarp();
     if (!ok && leader) {
       raise_status(p.status, kStatusTimeout);
@@ -994,119 +1091,158 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Elementwise: thread = query row r; group g covers keys 32g..32g+31.
     const int g = warp >> 2, wl = warp & 3;
     const int r = wl * 32 + lane;
-    const int i = q0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(wl * 32) << 16;
     const float sl2 = p.sl2;
-    const size_t vo = static_cast<size_t>(bh) * p.npad + q0 + r;
-    const float lse2 = p.lse2[vo];   // +inf on padding rows and empty rows: p = 0
-    const float dl = p.delta[vo];
     int t = 0;
     bool ok = true;
-    for (int kb = kb_begin; kb < kb_end; ++kb) {
-      const int cls = cls_of(kb);
-      if (cls == kEmpty) continue;
-      const int kc = kb * kBN + 32 * g;  // first key of this group
-      if (!(ok = mbar_wait(bar(Lay::B_SDP), t & 1, abort_flag))) break;
-      tc_fence_after();
-      uint32_t allow = 0xFFFFFFFFu;
-      if (cls == kPartial) {
-        int lo = 0, hi = nk - 1;
-        if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) hi = min(hi, i + off);
-        if (p.mask_kind == kMaskWindow) lo = max(lo, i + off - p.window + 1);
-        allow = range_bits(lo - kc, hi - kc);
-        if (p.mask_kind == kMaskBitmask) {
-          const int w = kb * 4 + g;
-          allow &= (i < n && w < p.words_per_row)
-                       ? __ldg(p.bits + static_cast<size_t>(i) * p.words_per_row + w)
-                       : 0u;
-        }
-      }
-      const uint32_t tD = tD0 + 128 * (t & 1) + lane_off;
-      uint32_t sv[2][16], dpv[2][16];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        tmem_ld16(tS + lane_off + 32 * g + 16 * c, sv[c]);
-        tmem_ld16(tD + 32 * g + 16 * c, dpv[c]);
-      }
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        reg_fence(sv[c]);
-        reg_fence(dpv[c]);
-      }
-      // S(t) is in registers: the MMA warp may overwrite it with S(t+1).
-      tc_fence_before();
-      mbar_arrive(bar(Lay::B_SFREE));
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const uint32_t (&s)[16] = sv[c];
-        const uint32_t (&dp)[16] = dpv[c];
-        uint32_t dk[8];
-        uint4 rw;  // dropout: Philox words of keys kc + 16c + 8*(e/8) .. of row i
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          float x0, x1;  // packed fp32 arithmetic over the key pair
-          ffma2(x0, x1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]), sl2, sl2, -lse2, -lse2);
-          float p0 = ex2(x0);
-          float p1 = ex2(x1);
-          if (!((allow >> (16 * c + e)) & 1u)) p0 = 0.f;
-          if (!((allow >> (16 * c + e + 1)) & 1u)) p1 = 0.f;
-          float dp0 = __uint_as_float(dp[e]), dp1 = __uint_as_float(dp[e + 1]);
-          if constexpr (kDrop) {
-            // Replayed mask: dP = xi s (G_i . V_j); keys e, e+1 share one word.
-            if ((e & 7) == 0) rw = keep_words(p.seed_lo, p.seed_hi, bh, i, (kc + 16 * c + e) >> 3);
-            const int wi = (e & 7) >> 1;
-            const uint32_t w = wi == 0 ? rw.x : wi == 1 ? rw.y : wi == 2 ? rw.z : rw.w;
-            dp0 *= (w & 0xFFFFu) >= p.drop_t ? p.drop_scale : 0.f;
-            dp1 *= w >= (p.drop_t << 16) ? p.drop_scale : 0.f;
+    for (int nitem = 0; ok; ++nitem) {
+      int ti;
+      if (!(ok = take_item(nitem, ti))) break;
+      if (ti < 0) break;
+      int qb, bh, kb_begin, kb_end;
+      item_of(ti, qb, bh);
+      kb_range(qb, kb_begin, kb_end);
+      const int q0 = qb * kBM;
+      const int i = q0 + r;
+      const size_t vo = static_cast<size_t>(bh) * p.npad + q0 + r;
+      const float lse2 = p.lse2[vo];   // +inf on padding rows and empty rows: p = 0
+      const float dl = p.delta[vo];
+      const int t0 = t;
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
+        const int cls = cls_of(qb, kb);
+        if (cls == kEmpty) continue;
+        const int kc = kb * kBN + 32 * g;  // first key of this group
+        if (!(ok = mbar_wait(bar(Lay::B_SDP), t & 1, abort_flag))) break;
+        tc_fence_after();
+        uint32_t allow = 0xFFFFFFFFu;
+        if (cls == kPartial) {
+          int lo = 0, hi = nk - 1;
+          if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) hi = min(hi, i + off);
+          if (p.mask_kind == kMaskWindow) lo = max(lo, i + off - p.window + 1);
+          allow = range_bits(lo - kc, hi - kc);
+          if (p.mask_kind == kMaskBitmask) {
+            const int w = kb * 4 + g;
+            allow &= (i < n && w < p.words_per_row)
+                         ? __ldg(p.bits + static_cast<size_t>(i) * p.words_per_row + w)
+                         : 0u;
           }
-          float t0, t1, g0, g1;
-          fadd2(t0, t1, dp0, dp1, -dl, -dl);
-          fmul2(g0, g1, p0, p1, t0, t1);
-          dk[e / 2] = pack_bf16x2(g0, g1);
         }
-        tmem_st8(tD + 32 * g + 8 * c, dk);
+        const uint32_t tD = tD0 + 128 * (t & 1) + lane_off;
+        uint32_t sv[2][16], dpv[2][16];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld16(tS + lane_off + 32 * g + 16 * c, sv[c]);
+          tmem_ld16(tD + 32 * g + 16 * c, dpv[c]);
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          reg_fence(sv[c]);
+          reg_fence(dpv[c]);
+        }
+        // S(t) is in registers: the MMA warp may overwrite it with S(t+1).
+        tc_fence_before();
+        mbar_arrive(bar(Lay::B_SFREE));
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t (&s)[16] = sv[c];
+          const uint32_t (&dp)[16] = dpv[c];
+          uint32_t dk[8];
+          uint4 rw;  // dropout: Philox words of keys kc + 16c + 8*(e/8) .. of row i
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            float x0, x1;  // packed fp32 arithmetic over the key pair
+            ffma2(x0, x1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]), sl2, sl2, -lse2,
+                  -lse2);
+            float p0 = ex2(x0);
+            float p1 = ex2(x1);
+            if (!((allow >> (16 * c + e)) & 1u)) p0 = 0.f;
+            if (!((allow >> (16 * c + e + 1)) & 1u)) p1 = 0.f;
+            float dp0 = __uint_as_float(dp[e]), dp1 = __uint_as_float(dp[e + 1]);
+            if constexpr (kDrop) {
+              // Replayed mask: dP = xi s (G_i . V_j); keys e, e+1 share one word.
+              if ((e & 7) == 0)
+                rw = keep_words(p.seed_lo, p.seed_hi, bh, i, (kc + 16 * c + e) >> 3);
+              const int wi = (e & 7) >> 1;
+              const uint32_t w = wi == 0 ? rw.x : wi == 1 ? rw.y : wi == 2 ? rw.z : rw.w;
+              dp0 *= (w & 0xFFFFu) >= p.drop_t ? p.drop_scale : 0.f;
+              dp1 *= w >= (p.drop_t << 16) ? p.drop_scale : 0.f;
+            }
+            float t0f, t1f, g0, g1;
+            fadd2(t0f, t1f, dp0, dp1, -dl, -dl);
+            fmul2(g0, g1, p0, p1, t0f, t1f);
+            dk[e / 2] = pack_bf16x2(g0, g1);
+          }
+          tmem_st8(tD + 32 * g + 8 * c, dk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(Lay::B_DS));
+        ++t;
       }
-      tmem_st_wait();
+      if (!ok) break;
+      // Epilogue: dQ_i = c * acc, bf16; group g reads columns CW g .. CW g + CW - 1,
+      // releases the accumulator, and the rows leave through one shared-memory
+      // tile in the TMA layout (64-column boxes, 128-byte swizzle) and TMA
+      // stores, which write whole lines and clip rows past n.
+      if (!(ok = mbar_wait(bar(Lay::B_DONE), nitem & 1, abort_flag))) break;
+      tc_fence_after();
+      constexpr int CW = D / 4;  // columns per group
+      uint32_t pk[CW / 2];
+      {
+        uint32_t o[CW / 16][16];
+        if (t > t0) {
+#pragma unroll
+          for (int ch = 0; ch < CW / 16; ++ch) tmem_ld16(tQ + lane_off + CW * g + 16 * ch, o[ch]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int ch = 0; ch < CW / 16; ++ch) reg_fence(o[ch]);
+        } else {
+#pragma unroll
+          for (int ch = 0; ch < CW / 16; ++ch)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[ch][e] = 0u;
+        }
+#pragma unroll
+        for (int e = 0; e < CW / 2; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(o[e >> 3][(2 * e) & 15]) * p.scale,
+                              __uint_as_float(o[e >> 3][(2 * e + 1) & 15]) * p.scale);
+      }
       tc_fence_before();
-      mbar_arrive(bar(Lay::B_DS));
-      ++t;
+      mbar_arrive(bar(Lay::B_DREAD));  // the next item's first dQ product may overwrite it
+      if (threadIdx.x == 0) {
+        bulk_wait_read_all();
+        mbar_arrive(bar(Lay::B_EPIF));
+      }
+      if (!(ok = mbar_wait(bar(Lay::B_EPIF), nitem & 1, abort_flag))) break;
+      const uint32_t tile = sbase + Lay::EPI_OFF;
+#pragma unroll
+      for (int u = 0; u < CW / 8; ++u) {
+        const int col = CW * g + 8 * u;
+        const uint32_t addr = tile + (col >> 6) * (kBM * 128) + r * 128 +
+                              ((((col & 63) >> 3) ^ (r & 7)) << 4);
+        st_shared_v4(addr, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(Lay::B_EPI));
+      if (threadIdx.x == 0) {
+        if (mbar_wait(bar(Lay::B_EPI), nitem & 1, abort_flag)) {
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_store_3d(&p.tdq, tile + c * (kBM * 128), 64 * c, q0, bh);
+          bulk_commit();
+        } else {
+          ok = false;
+        }
+      }
+      ok = __all_sync(0xFFFFFFFFu, ok);
     }
     if (!ok) {
       raise_status(p.status, kStatusTimeout);
       *abort_flag = 1;
     }
-    // Epilogue: dQ_i = c * acc, bf16; group g writes columns 32g.. (D = 128) or
-    // 16g.. (D = 64).
-    bool have = ok && t > 0;
-    if (have) {
-      have = mbar_wait(bar(Lay::B_DONE), 0, abort_flag);
-      tc_fence_after();
-    }
-    constexpr int CW = D / 4;  // columns per group
-    __nv_bfloat16* dst = p.dQ + (static_cast<size_t>(bh) * n + (i < n ? i : 0)) * D + CW * g;
-#pragma unroll
-    for (int ch = 0; ch < CW / 16; ++ch) {
-      uint32_t o[16];
-      if (have) {
-        tmem_ld16(tQ + lane_off + CW * g + 16 * ch, o);
-        tmem_ld_wait();
-        reg_fence(o);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) o[e] = 0u;
-      }
-      if (i < n) {
-        uint32_t ov[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          ov[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * p.scale,
-                              __uint_as_float(o[2 * e + 1]) * p.scale);
-        uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * ch);
-        d4[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
-        d4[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
-      }
-    }
+    // The stores' issuer: all of its stores complete before the CTA ends.
+    if (threadIdx.x == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -1126,7 +1262,8 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
       !make_tmap_bf16(&p.tv, a.V, D, pr.nk, pr.BH) ||
       !make_tmap_bf16(&p.tdy, a.dY, D, pr.n, pr.BH) ||
       !make_tmap_bf16(&p.tdk, a.dK, D, pr.nk, pr.BH) ||
-      !make_tmap_bf16(&p.tdv, a.dV, D, pr.nk, pr.BH))
+      !make_tmap_bf16(&p.tdv, a.dV, D, pr.nk, pr.BH) ||
+      !make_tmap_bf16(&p.tdq, a.dQ, D, pr.n, pr.BH))
     return cudaErrorInvalidValue;
   p.n = pr.n;
   p.nk = pr.nk;
@@ -1163,21 +1300,22 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
   }
   const int nkb = (pr.nk + kBN - 1) / kBN, nqb = (pr.n + kBM - 1) / kBM;
   before_launch(kKernBwd, s);
-  // Persistent dK/dV kernel: one CTA per SM, items handed out by a counter;
-  // one item per CTA for the bitmask, whose tile table the kernel builds once.
-  const int kv_items = nkb * pr.BH;
-  int kv_grid = kv_items;
-  if (pr.mask_kind != kMaskBitmask) {
-    int dev = 0, sms = 148;
+  // Persistent kernels: one CTA per SM, items handed out by a counter; one
+  // item per CTA for the bitmask, whose tile table each CTA builds once.
+  int sms = 148;
+  {
+    int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess)
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    kv_grid = kv_items < sms ? kv_items : sms;
   }
-  kv<<<kv_grid, kThreads, KvLayout<D, D>::TOTAL, s>>>(p);
+  auto grid_of = [&](int items) {
+    return pr.mask_kind == kMaskBitmask || items < sms ? items : sms;
+  };
+  kv<<<grid_of(nkb * pr.BH), kThreads, KvLayout<D, D>::TOTAL, s>>>(p);
   e = cudaGetLastError();
   if (e == cudaSuccess) {
     before_launch(kKernBwdQ, s);
-    qk<<<dim3(nqb, pr.BH), kThreads, QLayout<D, D>::TOTAL, s>>>(p);
+    qk<<<grid_of(nqb * pr.BH), kThreads, QLayout<D, D>::TOTAL, s>>>(p);
     e = cudaGetLastError();
     after_launch(kKernBwdQ, s);
   }
