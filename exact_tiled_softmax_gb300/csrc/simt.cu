@@ -325,7 +325,7 @@ __device__ __forceinline__ void delta_store(const DeltaArgs& a, size_t row, floa
 constexpr int kDeltaRows = 4;
 
 template <typename T, int G>
-__global__ void __launch_bounds__(256) delta_vec_kernel(DeltaArgs a) {
+__global__ void __launch_bounds__(256, 4) delta_vec_kernel(DeltaArgs a) {
   constexpr int E = 16 / sizeof(T);  // elements per 16-byte vector
   constexpr int R = kDeltaRows;
   const int lane = static_cast<int>(threadIdx.x % G);
@@ -336,16 +336,19 @@ __global__ void __launch_bounds__(256) delta_vec_kernel(DeltaArgs a) {
     const size_t r0 = (it * groups + group) * R;
     uint4 va[R], vb[R];
     bool live[R];
+    float Lr[R];  // L of row u, loaded (with Y and dY) by the lane that stores row u
 #pragma unroll
     for (int u = 0; u < R; ++u) {
       const size_t row = r0 + u;
       const size_t bh = row / a.npad;
       const int i = static_cast<int>(row - bh * a.npad);
       live[u] = row < a.rows && i < a.n;
+      Lr[u] = -INFINITY;
       if (live[u]) {
         const size_t src = (bh * a.n + i) * a.v;
         va[u] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const T*>(a.Y) + src) + lane);
         vb[u] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const T*>(a.dY) + src) + lane);
+        if (lane == u % G) Lr[u] = __ldcs(a.L + bh * a.n + i);
       }
     }
 #pragma unroll
@@ -359,7 +362,11 @@ __global__ void __launch_bounds__(256) delta_vec_kernel(DeltaArgs a) {
       }
 #pragma unroll
       for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (r0 + u < a.rows && lane == 0) delta_store(a, r0 + u, acc);
+      // Padding rows (i >= n): delta 0, L log2(e) = +inf (p = 0 in the reverse kernels).
+      if (r0 + u < a.rows && lane == u % G) {
+        a.delta[r0 + u] = live[u] ? acc : 0.f;
+        a.lse2[r0 + u] = live[u] && Lr[u] != -INFINITY ? Lr[u] * kLog2e : INFINITY;
+      }
     }
   }
 }
@@ -452,18 +459,27 @@ cudaError_t delta_dispatch(const BwdArgs& a, cudaStream_t s) {
   const int vecs = p.v / E;
   before_launch(kKernDelta, s);
   if (p.v % E == 0 && (vecs & (vecs - 1)) == 0 && vecs <= 32) {
-    // G lanes per row, one 16-byte vector per lane per row; one wave of 8 CTAs
-    // per SM (fewer when there are fewer rows).
+    // G lanes per row, one 16-byte vector per lane per row; one wave of as
+    // many CTAs as fit on every SM (fewer when there are fewer rows).
     const int G = vecs;
-    const size_t need = (d.rows * G + 255) / 256;
-    const unsigned blocks = (unsigned)(need < 152 * 8 ? need : 152 * 8);
+    auto launch = [&](auto kern) {
+      int dev = 0, sms = 148, per_sm = 4;
+      if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess ||
+          per_sm < 1)
+        per_sm = 1;
+      const size_t need = (d.rows * G + 255) / 256;
+      const size_t wave = static_cast<size_t>(sms) * per_sm;
+      kern<<<static_cast<unsigned>(need < wave ? need : wave), 256, 0, s>>>(d);
+    };
     switch (G) {
-      case 1: delta_vec_kernel<T, 1><<<blocks, 256, 0, s>>>(d); break;
-      case 2: delta_vec_kernel<T, 2><<<blocks, 256, 0, s>>>(d); break;
-      case 4: delta_vec_kernel<T, 4><<<blocks, 256, 0, s>>>(d); break;
-      case 8: delta_vec_kernel<T, 8><<<blocks, 256, 0, s>>>(d); break;
-      case 16: delta_vec_kernel<T, 16><<<blocks, 256, 0, s>>>(d); break;
-      default: delta_vec_kernel<T, 32><<<blocks, 256, 0, s>>>(d); break;
+      case 1: launch(delta_vec_kernel<T, 1>); break;
+      case 2: launch(delta_vec_kernel<T, 2>); break;
+      case 4: launch(delta_vec_kernel<T, 4>); break;
+      case 8: launch(delta_vec_kernel<T, 8>); break;
+      case 16: launch(delta_vec_kernel<T, 16>); break;
+      default: launch(delta_vec_kernel<T, 32>); break;
     }
   } else {
     const unsigned blocks = (unsigned)((d.rows * 32 + 255) / 256);
