@@ -380,12 +380,13 @@ def run_gpu(args, w):
     # are also bracketed by events recorded on this stream by the library.
     K = args.steps
     # The split tensor-core reverse pass (bf16, d = v in {64, 128}) also brackets
-    # its dQ kernel, so the dK/dV kernel's time is the difference.
+    # its dQ kernel, so the dK/dV kernel's time is the difference; its dQ kernel
+    # forms delta itself (no delta launch).
     split_bwd = (w.dtype == "bf16" and w.d == w.v and w.d in (64, 128)
                  and args.path == "auto"
                  and (w.mask != "bitmask" or max(w.n, w.n_keys) <= 256 * 128))
-    roles = (ex.KERNEL_FWD, ex.KERNEL_BWD, ex.KERNEL_DELTA) + ((ex.KERNEL_BWD_Q,) if split_bwd
-                                                              else ())
+    roles = ((ex.KERNEL_FWD, ex.KERNEL_BWD, ex.KERNEL_BWD_Q) if split_bwd
+             else (ex.KERNEL_FWD, ex.KERNEL_BWD, ex.KERNEL_DELTA))
     ev = {role: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                  for _ in range(K)] for role in roles}
     for pairs_ in ev.values():
@@ -406,7 +407,7 @@ def run_gpu(args, w):
     launches = ex.launch_count() - launches0
     ms = rank_max(start.elapsed_time(stop))
     kern_ms = {role: sum(a.elapsed_time(b) for a, b in ev[role]) / K for role in ev}
-    delta_ms = kern_ms.pop(ex.KERNEL_DELTA)
+    delta_ms = kern_ms.pop(ex.KERNEL_DELTA, None)
     bwd_q_ms = kern_ms.pop(ex.KERNEL_BWD_Q, None)
 
     # Forward alone.
@@ -472,11 +473,14 @@ def run_gpu(args, w):
     npad = (w.n + 127) // 128 * 128
     delta_bytes = w.B * w.H * (2 * w.n * w.v * e + 4 * w.n + 8 * npad)
     hbm = float(peaks["hbm_gbs"])
-    roofline_delta = {"kernel": "delta", "bound": "hbm",
-                      "achieved": delta_bytes / (delta_ms * 1e-3) / 1e9, "peak": hbm,
-                      "unit": "GB/s", "frac": delta_bytes / (delta_ms * 1e-3) / 1e9 / hbm,
-                      "peak_kind": f"copy bandwidth, of {peak_kind}", "bytes": delta_bytes,
-                      "ms": delta_ms}
+    if delta_ms is None:
+        roofline_delta = {"kernel": "delta", "fused_into": "tc_bwd_q_kernel", "bytes": delta_bytes}
+    else:
+        roofline_delta = {"kernel": "delta", "bound": "hbm",
+                          "achieved": delta_bytes / (delta_ms * 1e-3) / 1e9, "peak": hbm,
+                          "unit": "GB/s", "frac": delta_bytes / (delta_ms * 1e-3) / 1e9 / hbm,
+                          "peak_kind": f"copy bandwidth, of {peak_kind}", "bytes": delta_bytes,
+                          "ms": delta_ms}
     line = {
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,

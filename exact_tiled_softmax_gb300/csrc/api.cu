@@ -266,9 +266,8 @@ int bwd_impl(const Dims& dims, const void* Q, const void* K, const void* V, cons
   if (e != cudaSuccess) return cuda_status(e, "attn_bwd: clearing the status word");
   const int path = g_path.load();
   if (path == EXATTN_PATH_AUTO && tc_bwd_split_supported(a.p)) {
-    // Split form: dQ is written directly, no accumulator.
-    e = launch_delta(a, s);
-    if (e != cudaSuccess) return cuda_status(e, "attn_bwd: delta launch");
+    // Split form: dQ is written directly, no accumulator; the dQ kernel also
+    // forms delta and L log2(e).
     return cuda_status(launch_tc_bwd_split(a, s), "attn_bwd: reverse kernel launch");
   }
   e = cudaMemsetAsync(a.dQacc, 0, acc_bytes, s);

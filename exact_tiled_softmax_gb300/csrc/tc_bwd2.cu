@@ -55,11 +55,14 @@ struct Bwd2Params {
   CUtensorMap tq, tk, tv, tdy;
   CUtensorMap tdk, tdv;  // dK, dV as store targets (dK/dV kernel)
   CUtensorMap tdq;       // dQ as a store target (dQ kernel)
+  CUtensorMap ty;        // Y, for the dQ kernel's L2 prefetch of the next item's rows
   int n, npad, BH, mask_kind, window, words_per_row;
   int nk, off;  // keys, and the absolute position of query 0 (nk - n)
   const uint32_t* bits;
-  const float* delta;  // [BH][npad]
-  const float* lse2;   // [BH][npad]  L log2(e), +inf on padding / empty rows
+  float* delta;  // [BH][npad]: written by the dQ kernel, read by the dK/dV kernel
+  float* lse2;   // [BH][npad]  L log2(e), +inf on padding / empty rows (same)
+  const __nv_bfloat16* Y;  // [BH][n][V], for delta_i = dY_i . Y_i
+  const float* L;          // [BH][n], natural log
   float sl2;           // c log2(e)
   float scale;         // c
   __nv_bfloat16* dQ;
@@ -766,12 +769,14 @@ struct QLayout {
   static constexpr int SLOT_OFF = Y_OFF + YBYTES;
   // Epilogue tile: kBM rows of dQ as 64-column boxes (128-byte swizzle).
   static constexpr int EPI_OFF = SLOT_OFF + NS * SLOT;
-  static constexpr int BAR_OFF = EPI_OFF + kBM * D * 2;
+  // Partial sums of delta_i = dY_i . Y_i, one per elementwise group and row.
+  static constexpr int PART_OFF = EPI_OFF + kBM * D * 2;
+  static constexpr int BAR_OFF = PART_OFF + 4 * kBM * 4;
   static constexpr int B_Q = 0, B_QFREE = 1, B_KVF = 2, B_KVE = B_KVF + NS, B_SDP = B_KVE + NS,
                        B_DS = B_SDP + 1, B_SFREE = B_DS + 1, B_DONE = B_SFREE + 1,
                        B_DREAD = B_DONE + 1, B_ITEMF = B_DREAD + 1, B_ITEME = B_ITEMF + 2,
-                       B_EPIF = B_ITEME + 2, B_EPI = B_EPIF + 1, B_DRAIN = B_EPI + 1,
-                       NBAR = B_DRAIN + 1;
+                       B_EPIF = B_ITEME + 2, B_EPI = B_EPIF + 1, B_DPART = B_EPI + 1,
+                       B_DRAIN = B_DPART + 1, NBAR = B_DRAIN + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int CLS_OFF = MISC_OFF + 16;
   static constexpr int TOTAL = CLS_OFF + 2 * (kMaxBlocks / 32) * 4;
@@ -838,6 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(Lay::B_EPIF), 1);  // the previous item's dQ stores have read the tile
     mbar_init(bar(Lay::B_EPI), kEwWarps * 32);
+    mbar_init(bar(Lay::B_DPART), kEwWarps * 32);  // delta partial sums written (dY read)
     mbar_init(bar(Lay::B_DRAIN), 1);
     misc[1] = 0;
     fence_mbar_init();
@@ -883,6 +889,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&p.tv);
       prefetch_tmap(&p.tdy);
       prefetch_tmap(&p.tdq);
+      prefetch_tmap(&p.ty);
     }
     const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
     int it = 0, q_loads = 0;
@@ -924,7 +931,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           int qbn, bhn;
           item_of(t_next, qbn, bhn);
           for (int c = 0; c < D / 64; ++c) tma_prefetch_3d(&p.tq, 64 * c, qbn * kBM, bhn);
-          for (int c = 0; c < V / 64; ++c) tma_prefetch_3d(&p.tdy, 64 * c, qbn * kBM, bhn);
+          for (int c = 0; c < V / 64; ++c) {
+            tma_prefetch_3d(&p.tdy, 64 * c, qbn * kBM, bhn);
+            tma_prefetch_3d(&p.ty, 64 * c, qbn * kBM, bhn);  // for delta
+          }
         }
       };
       for (int kb = kb_begin; kb < kb_end && ok; ++kb) {
@@ -1009,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto kv_full = [&](int fill) {
       return mbar_wait(bar(Lay::B_KVF + fill % NS), (fill / NS) & 1, abort_flag);
     };
-    int t = 0;
+    int t = 0, ne = 0;  // ne: items with key blocks so far (phases of B_DPART)
     for (int nitem = 0; ok; ++nitem) {
       int ti;
       if (!(ok = take_item(nitem, ti))) break;
@@ -1029,6 +1039,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int kb = next_kb(kb_begin - 1);
       int kb_n = kb < kb_end ? next_kb(kb) : kb_end;
       const int t0 = t;
+      // Q and dY are read by the S and dP products and, for delta, by the
+      // elementwise warps of an item with key blocks.
+      const bool nonempty = kb < kb_end;
+      auto free_q = [&]() {
+        if (nonempty && !mbar_wait(bar(Lay::B_DPART), ne & 1, abort_flag)) return false;
+        if (leader) tc_commit(bar(Lay::B_QFREE));
+        return true;
+      };
       // Prologue: dP(t0) -> its buffer, S(t0) -> S once the previous item's
       // last S is in the elementwise warps' registers.
       if (kb < kb_end) {
@@ -1040,8 +1058,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_s(t);
       }
-      // Q and dY are read by the S and dP products only.
-      if (kb_n >= kb_end && leader) tc_commit(bar(Lay::B_QFREE));
+      if (kb_n >= kb_end && !(ok = free_q())) break;
       while (kb < kb_end) {
         const bool more = kb_n < kb_end;
         const int kb_nn = more ? next_kb(kb_n) : kb_end;
@@ -1055,7 +1072,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = kv_full(2 * (t + 1) + 1))) break;
           tc_fence_after();
           issue_s(t + 1);
-          if (kb_nn >= kb_end && leader) tc_commit(bar(Lay::B_QFREE));
+          if (kb_nn >= kb_end && !(ok = free_q())) break;
         }
         if (!(ok = mbar_wait(bar(Lay::B_DS), t & 1, abort_flag))) break;
         tc_fence_after();
@@ -1074,6 +1091,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++t;
       }
       if (!ok) break;
+      if (nonempty) ++ne;
       // "dQ done" stays at most one phase ahead of the epilogue, also through
       // items without key blocks.
       if (nitem > 0 && !(ok = mbar_wait(bar(Lay::B_DREAD), (nitem - 1) & 1, abort_flag))) break;
@@ -1093,7 +1111,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = wl * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wl * 32) << 16;
     const float sl2 = p.sl2;
-    int t = 0;
+    float* part = reinterpret_cast<float*>(smem + Lay::PART_OFF);  // [4][kBM]
+    int t = 0, ne = 0;  // ne: items with key blocks so far (phases of B_DPART)
     bool ok = true;
     for (int nitem = 0; ok; ++nitem) {
       int ti;
@@ -1105,8 +1124,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = qb * kBM;
       const int i = q0 + r;
       const size_t vo = static_cast<size_t>(bh) * p.npad + q0 + r;
-      const float lse2 = p.lse2[vo];   // +inf on padding rows and empty rows: p = 0
-      const float dl = p.delta[vo];
+      // delta_i = dY_i . Y_i ("Exact tiled softmax attention ...", Reverse
+      // procedure) and L_i log2(e) for this query block: group g sums columns
+      // V/4 g .. of dY (from the staged tile) times Y, the four partial sums
+      // meet in shared memory.  Both go to the workspace for the dK/dV kernel,
+      // which runs after this one.  Padding rows: delta 0, L log2(e) = +inf.
+      int kb_first = kb_begin;
+      while (kb_first < kb_end && cls_of(qb, kb_first) == kEmpty) ++kb_first;
+      float lse2 = INFINITY, dl = 0.f;
+      if (kb_first < kb_end) {
+        // Y and L first: their loads overlap the wait for the staged dY.
+        constexpr int CV = V / 4;  // columns per group
+        uint4 yv[CV / 8];
+        float Li = -INFINITY;
+        if (i < n) {
+          const uint4* yrow =
+              reinterpret_cast<const uint4*>(p.Y + (static_cast<size_t>(bh) * n + i) * V + CV * g);
+#pragma unroll
+          for (int u = 0; u < CV / 8; ++u) yv[u] = __ldg(yrow + u);
+          Li = __ldg(p.L + static_cast<size_t>(bh) * n + i);
+        }
+        if (!(ok = mbar_wait(bar(Lay::B_Q), nitem & 1, abort_flag))) break;
+        float acc = 0.f;
+        if (i < n) {
+#pragma unroll
+          for (int u = 0; u < CV / 8; ++u) {
+            const int col = CV * g + 8 * u;
+            const uint4 gv = ld_shared_v4(sbase + Lay::Y_OFF + (col >> 6) * 16384 + r * 128 +
+                                          ((((col & 63) >> 3) ^ (r & 7)) << 4));
+            const uint32_t ya[4] = {yv[u].x, yv[u].y, yv[u].z, yv[u].w};
+            const uint32_t ga[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc = fmaf(__uint_as_float(ya[e] << 16), __uint_as_float(ga[e] << 16), acc);
+              acc = fmaf(__uint_as_float(ya[e] & 0xFFFF0000u), __uint_as_float(ga[e] & 0xFFFF0000u),
+                         acc);
+            }
+          }
+        }
+        part[g * kBM + r] = acc;
+        mbar_arrive(bar(Lay::B_DPART));
+        if (!(ok = mbar_wait(bar(Lay::B_DPART), ne & 1, abort_flag))) break;
+        ++ne;
+        if (i < n) {
+          dl = (part[r] + part[kBM + r]) + (part[2 * kBM + r] + part[3 * kBM + r]);
+          lse2 = Li == -INFINITY ? INFINITY : Li * kLog2e;  // p = 0 on empty rows
+        }
+      }
+      if (g == 0) {
+        p.delta[vo] = dl;
+        p.lse2[vo] = lse2;
+      }
       const int t0 = t;
       for (int kb = kb_begin; kb < kb_end; ++kb) {
         const int cls = cls_of(qb, kb);
@@ -1263,7 +1331,8 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
       !make_tmap_bf16(&p.tdy, a.dY, D, pr.n, pr.BH) ||
       !make_tmap_bf16(&p.tdk, a.dK, D, pr.nk, pr.BH) ||
       !make_tmap_bf16(&p.tdv, a.dV, D, pr.nk, pr.BH) ||
-      !make_tmap_bf16(&p.tdq, a.dQ, D, pr.n, pr.BH))
+      !make_tmap_bf16(&p.tdq, a.dQ, D, pr.n, pr.BH) ||
+      !make_tmap_bf16(&p.ty, a.Y, D, pr.n, pr.BH))
     return cudaErrorInvalidValue;
   p.n = pr.n;
   p.nk = pr.nk;
@@ -1276,6 +1345,8 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
   p.bits = pr.bitmask;
   p.delta = a.delta;
   p.lse2 = a.lse2;
+  p.Y = static_cast<const __nv_bfloat16*>(a.Y);
+  p.L = a.L;
   p.sl2 = pr.scale * kLog2e;
   p.scale = pr.scale;
   p.dQ = static_cast<__nv_bfloat16*>(a.dQ);
@@ -1311,13 +1382,15 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
   auto grid_of = [&](int items) {
     return pr.mask_kind == kMaskBitmask || items < sms ? items : sms;
   };
-  kv<<<grid_of(nkb * pr.BH), kThreads, KvLayout<D, D>::TOTAL, s>>>(p);
+  // The dQ kernel first: it also forms delta and L log2(e), which the dK/dV
+  // kernel reads.
+  before_launch(kKernBwdQ, s);
+  qk<<<grid_of(nqb * pr.BH), kThreads, QLayout<D, D>::TOTAL, s>>>(p);
   e = cudaGetLastError();
+  after_launch(kKernBwdQ, s);
   if (e == cudaSuccess) {
-    before_launch(kKernBwdQ, s);
-    qk<<<grid_of(nqb * pr.BH), kThreads, QLayout<D, D>::TOTAL, s>>>(p);
+    kv<<<grid_of(nkb * pr.BH), kThreads, KvLayout<D, D>::TOTAL, s>>>(p);
     e = cudaGetLastError();
-    after_launch(kKernBwdQ, s);
   }
   after_launch(kKernBwd, s);
   return e;
