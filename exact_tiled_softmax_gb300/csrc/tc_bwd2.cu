@@ -1114,10 +1114,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* part = reinterpret_cast<float*>(smem + Lay::PART_OFF);  // [4][kBM]
     int t = 0, ne = 0;  // ne: items with key blocks so far (phases of B_DPART)
     bool ok = true;
-    for (int nitem = 0; ok; ++nitem) {
-      int ti;
-      if (!(ok = take_item(nitem, ti))) break;
-      if (ti < 0) break;
+    // Y_i (this group's V/4 columns) and L_i of an item's row r, loaded as soon
+    // as the item is known: for the next item that is before this item's
+    // epilogue, so the loads overlap it.
+    constexpr int CV = V / 4;
+    uint4 yv[CV / 8];
+    float Li = -INFINITY;
+    auto load_row = [&](int tix) {
+      int qbx, bhx;
+      item_of(tix, qbx, bhx);
+      const int ix = qbx * kBM + r;
+      Li = -INFINITY;
+      if (ix < n) {
+        const uint4* yrow =
+            reinterpret_cast<const uint4*>(p.Y + (static_cast<size_t>(bhx) * n + ix) * V + CV * g);
+#pragma unroll
+        for (int u = 0; u < CV / 8; ++u) yv[u] = __ldg(yrow + u);
+        Li = __ldg(p.L + static_cast<size_t>(bhx) * n + ix);
+      }
+    };
+    int ti = -1;
+    if ((ok = take_item(0, ti)) && ti >= 0) load_row(ti);
+    for (int nitem = 0; ok && ti >= 0; ++nitem) {
       int qb, bh, kb_begin, kb_end;
       item_of(ti, qb, bh);
       kb_range(qb, kb_begin, kb_end);
@@ -1133,17 +1151,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (kb_first < kb_end && cls_of(qb, kb_first) == kEmpty) ++kb_first;
       float lse2 = INFINITY, dl = 0.f;
       if (kb_first < kb_end) {
-        // Y and L first: their loads overlap the wait for the staged dY.
-        constexpr int CV = V / 4;  // columns per group
-        uint4 yv[CV / 8];
-        float Li = -INFINITY;
-        if (i < n) {
-          const uint4* yrow =
-              reinterpret_cast<const uint4*>(p.Y + (static_cast<size_t>(bh) * n + i) * V + CV * g);
-#pragma unroll
-          for (int u = 0; u < CV / 8; ++u) yv[u] = __ldg(yrow + u);
-          Li = __ldg(p.L + static_cast<size_t>(bh) * n + i);
-        }
         if (!(ok = mbar_wait(bar(Lay::B_Q), nitem & 1, abort_flag))) break;
         float acc = 0.f;
         if (i < n) {
@@ -1249,6 +1256,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++t;
       }
       if (!ok) break;
+      // The next item now (the ring holds it by the time this item's blocks are
+      // done): its row loads overlap this item's epilogue.
+      int tn = -1;
+      if (!(ok = take_item(nitem + 1, tn))) break;
+      if (tn >= 0) load_row(tn);
       // Epilogue: dQ_i = c * acc, bf16; group g reads columns CW g .. CW g + CW - 1,
       // releases the accumulator, and the rows leave through one shared-memory
       // tile in the TMA layout (64-column boxes, 128-byte swizzle) and TMA
@@ -1304,6 +1316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ok = __all_sync(0xFFFFFFFFu, ok);
+      ti = tn;
     }
     if (!ok) {
       raise_status(p.status, kStatusTimeout);
