@@ -763,7 +763,12 @@ struct QLayout {
   static constexpr int KBYTES = kBN * D * 2;
   static constexpr int VBYTES = kBN * V * 2;
   static constexpr int SLOT = KBYTES > VBYTES ? KBYTES : VBYTES;
-  static constexpr int NS = D == 128 ? 4 : 8;  // K and V tiles alternate in one ring
+  // Two rings over one slot array: K tiles in slots [0, NK), V tiles in
+  // [NK, NK + NV).  K(t) is read until dQ(t) completes, V(t) only until dP(t)
+  // does, so K gets the deeper ring: its refill then has a whole step.
+  static constexpr int NK = D == 128 ? 3 : 5;
+  static constexpr int NV = D == 128 ? 1 : 3;
+  static constexpr int NS = NK + NV;
   static constexpr int Q_OFF = 0;
   static constexpr int Y_OFF = QBYTES;
   static constexpr int SLOT_OFF = Y_OFF + YBYTES;
@@ -939,18 +944,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int kb = kb_begin; kb < kb_end && ok; ++kb) {
         if (cls_of(qb, kb) == kEmpty) continue;
+        // Block it: V(it) into slot NK + it % NV, then K(it) into slot it % NK.
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
-          const int slot = it % NS, phase = (it / NS) & 1;
-          ++it;
+          const int slot = kv == 0 ? Lay::NK + it % Lay::NV : it % Lay::NK;
+          const int phase = kv == 0 ? (it / Lay::NV) & 1 : (it / Lay::NK) & 1;
           if (!mbar_wait(bar(Lay::B_KVE + slot), phase ^ 1, abort_flag)) {
             ok = false;
             break;
           }
           const uint32_t dst = sbase + Lay::SLOT_OFF + slot * Lay::SLOT;
           if (leader) {
-            // V(t) first, then K(t): V(t) is needed one step earlier (for dP(t))
-            // and each slot is then reused two steps after its last reader.
             if (kv == 1) {
               mbar_arrive_expect_tx(bar(Lay::B_KVF + slot), Lay::KBYTES);
               for (int c = 0; c < D / 64; ++c)
@@ -964,6 +968,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        ++it;
         if (ok && t_next < 0) prefetch_next();
       }
       if (!ok) break;
@@ -975,11 +980,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       raise_status(p.status, kStatusTimeout);
       *abort_flag = 1;
     }
-    // Never leave with copies in flight: the last fill of every slot (fill
-    // i = it - 1 - u went to slot i % NS) and the last Q, dY.
-    for (int u = 0; u < NS && u < it; ++u) {
+    // Never leave with copies in flight: the last fill of every slot (block
+    // i = it - 1 - u filled K slot i % NK and V slot NK + i % NV) and the last Q, dY.
+    for (int u = 0; u < Lay::NK && u < it; ++u) {
       const int i = it - 1 - u;
-      mbar_wait(bar(Lay::B_KVF + i % NS), (i / NS) & 1, abort_flag);
+      mbar_wait(bar(Lay::B_KVF + i % Lay::NK), (i / Lay::NK) & 1, abort_flag);
+    }
+    for (int u = 0; u < Lay::NV && u < it; ++u) {
+      const int i = it - 1 - u;
+      mbar_wait(bar(Lay::B_KVF + Lay::NK + i % Lay::NV), (i / Lay::NV) & 1, abort_flag);
     }
     if (q_loads > 0) mbar_wait(bar(Lay::B_Q), (q_loads - 1) & 1, abort_flag);
   } else if (warp == kWarpMMA) {
@@ -992,9 +1001,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dSm = sdesc_sw128(sbase + Lay::SLOT_OFF, 16384, 1024);
     constexpr uint32_t kSlot16 = Lay::SLOT >> 4;
     bool ok = true;
-    // Block t (counted across items) uses ring fills 2t (V) and 2t + 1 (K).
+    // Block t (counted across items) uses K slot t % NK and V slot NK + t % NV.
     auto issue_dp = [&](int tt) {
-      const int vs = (2 * tt) % NS;
+      const int vs = Lay::NK + tt % Lay::NV;
       const uint32_t tD = tD0 + 128 * (tt & 1);
       if (leader) {
 #pragma unroll
@@ -1006,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     auto issue_s = [&](int tt) {
-      const int ks = (2 * tt + 1) % NS;
+      const int ks = tt % Lay::NK;
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -1016,8 +1025,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(bar(Lay::B_SDP));
       }
     };
-    auto kv_full = [&](int fill) {
-      return mbar_wait(bar(Lay::B_KVF + fill % NS), (fill / NS) & 1, abort_flag);
+    auto v_full = [&](int tt) {
+      return mbar_wait(bar(Lay::B_KVF + Lay::NK + tt % Lay::NV), (tt / Lay::NV) & 1, abort_flag);
+    };
+    auto k_full = [&](int tt) {
+      return mbar_wait(bar(Lay::B_KVF + tt % Lay::NK), (tt / Lay::NK) & 1, abort_flag);
     };
     int t = 0, ne = 0;  // ne: items with key blocks so far (phases of B_DPART)
     for (int nitem = 0; ok; ++nitem) {
@@ -1050,11 +1062,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Prologue: dP(t0) -> its buffer, S(t0) -> S once the previous item's
       // last S is in the elementwise warps' registers.
       if (kb < kb_end) {
-        if (!(ok = kv_full(2 * t))) break;
+        if (!(ok = v_full(t))) break;
         tc_fence_after();
         issue_dp(t);
         if (t > 0 && !(ok = mbar_wait(bar(Lay::B_SFREE), (t - 1) & 1, abort_flag))) break;
-        if (!(ok = kv_full(2 * t + 1))) break;
+        if (!(ok = k_full(t))) break;
         tc_fence_after();
         issue_s(t);
       }
@@ -1064,12 +1076,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kb_nn = more ? next_kb(kb_n) : kb_end;
         if (more) {
           // dP(t+1) -> the other buffer (its dS(t-1) was read by dQ(t-1), issued earlier).
-          if (!(ok = kv_full(2 * (t + 1)))) break;
+          if (!(ok = v_full(t + 1))) break;
           tc_fence_after();
           issue_dp(t + 1);
           // S(t+1) as soon as the elementwise warps hold S(t) in registers.
           if (!(ok = mbar_wait(bar(Lay::B_SFREE), t & 1, abort_flag))) break;
-          if (!(ok = kv_full(2 * (t + 1) + 1))) break;
+          if (!(ok = k_full(t + 1))) break;
           tc_fence_after();
           issue_s(t + 1);
           if (kb_nn >= kb_end && !(ok = free_q())) break;
@@ -1077,7 +1089,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(bar(Lay::B_DS), t & 1, abort_flag))) break;
         tc_fence_after();
         // dQ += dS(t) K_t  (A = dS bf16 in TMEM over dP(t), keys packed; B = K_t MN-major)
-        const int ks = (2 * t + 1) % NS;
+        const int ks = t % Lay::NK;
         const uint32_t tD = tD0 + 128 * (t & 1);
         if (leader) {
 #pragma unroll
