@@ -110,6 +110,11 @@ def load_library():
     lib.attn_fwd_splitkv.restype = ci
     lib.exattn_last_error.argtypes = []
     lib.exattn_last_error.restype = ctypes.c_char_p
+    lib.exattn_host_step_workspace_size.argtypes = [sp, ci]
+    lib.exattn_host_step_workspace_size.restype = sz
+    lib.attn_step_host.argtypes = [sp, vp, vp, vp, vp, cf, ci, ci, vp, vp, vp, vp, vp, vp, vp, sz,
+                                   vp]
+    lib.attn_step_host.restype = ci
     _lib = lib
     return lib
 
@@ -319,6 +324,43 @@ def bwd_noalloc(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, d
 
 KERNEL_FWD, KERNEL_DELTA, KERNEL_BWD, KERNEL_DQ_CONVERT, KERNEL_BWD_Q = 0, 1, 2, 3, 4
 KERNEL_SPLIT_PARTIAL, KERNEL_SPLIT_MERGE, KERNEL_SPLIT32 = 5, 6, 7
+
+
+def step_host(q, k, v, dy, scale, mask="none", window=0, bitmask=None, out=None, ws=None,
+              stream=None, device=None):
+    """attn_step_host: forward and reverse pass on CPU tensors (pinned for
+    asynchronous copies) -> (Y, L, dQ, dK, dV), CPU tensors.  ``out`` may give
+    the five outputs (pinned, to be reused); ``ws`` a device workspace of
+    exattn_host_step_workspace_size bytes.  Returns once the step is queued:
+    synchronise ``stream`` (default: the current stream of ``device``) before
+    reading the outputs."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    for t in (q, k, v, dy):
+        if t.device.type != "cpu" or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError("step_host takes contiguous CPU tensors of one dtype")
+    if bitmask is not None and bitmask.device.type != "cpu":
+        raise ValueError("step_host takes the bitmask on the CPU")
+    kind = _mask_kind(mask)
+    shape = _shape(q, v)
+    if out is None:
+        pin = torch.cuda.is_available()
+        out = (torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, pin_memory=pin),
+               torch.empty(q.shape[:-1], dtype=torch.float32, pin_memory=pin),
+               torch.empty(q.shape, dtype=q.dtype, pin_memory=pin),
+               torch.empty(k.shape, dtype=q.dtype, pin_memory=pin),
+               torch.empty(v.shape, dtype=q.dtype, pin_memory=pin))
+    y, L, dq, dk, dv = out
+    need = lib.exattn_host_step_workspace_size(ctypes.byref(shape), kind)
+    if ws is None:
+        ws = workspace(need, dev)
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    st = lib.attn_step_host(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(dy), float(scale),
+                            kind, int(window), _ptr(bitmask), _ptr(y), _ptr(L), _ptr(dq), _ptr(dk),
+                            _ptr(dv), _ptr(ws), ws.numel(), ctypes.c_void_p(s.cuda_stream))
+    if st != 0:
+        raise ExattnError(st, "attn_step_host")
+    return y, L, dq, dk, dv
 
 
 def record_kernel_events(which: int, start, stop) -> None:

@@ -1,5 +1,6 @@
 // The C ABI of libexattn (include/exattn.h): argument checks, workspace layout
 // and kernel dispatch.  No memory is allocated here.
+#include <algorithm>
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -467,6 +468,209 @@ int attn_fwd_splitkv(const exattn_qk_shape* shape, const void* Q, const void* K,
   }
   return cuda_status(launch_splitkv(a, shape->dtype, Y, L, static_cast<unsigned*>(workspace), s),
                      "attn_fwd_splitkv: launch");
+}
+
+// ------------------------------------------------------------ host step
+// attn_step_host: forward and reverse pass on tensors in host memory.  The
+// slices are cut into chunks; chunk k's inputs are copied in on one stream,
+// its forward and reverse pass run on a second, and its outputs are copied out
+// on a third, so the copies of neighbouring chunks overlap the kernels.  Each
+// slice is computed exactly as attn_fwd / attn_bwd compute it.
+}  // extern "C"
+
+namespace {
+
+__global__ void status_or_kernel(unsigned* dst, const unsigned* src) { *dst |= *src; }
+
+constexpr int kHostMaxChunks = 16;
+
+struct HostStepLayout {
+  int chunks;
+  int start[kHostMaxChunks + 1];  // chunk c holds slices [start[c], start[c + 1])
+  size_t q, k, v, dy, y, l, dq, dk, dv, bits, ws, ws_bytes, total;
+};
+
+HostStepLayout host_layout(const Dims& d, int mask_kind) {
+  HostStepLayout L{};
+  const int BH = d.batch * d.heads;
+  const size_t e = d.dtype == EXATTN_F32 ? 4 : 2;
+  const size_t row_q = (size_t)d.d * e, row_v = (size_t)d.v * e;
+  // Chunk boundaries must keep every slice pointer 16-byte aligned.
+  const bool split_ok = ((size_t)d.nq * row_q) % 16 == 0 && ((size_t)d.nq * row_v) % 16 == 0 &&
+                        ((size_t)d.nq * 4) % 16 == 0;
+  // Nothing computes until the first chunk is in and the last chunk's outputs
+  // leave after everything else, so those two are small (1/32 of the slices
+  // each) and the middle is cut evenly.
+  L.chunks = 1;
+  L.start[0] = 0;
+  L.start[1] = BH;
+  if (split_ok && BH >= 8) {
+    const int edge = BH >= 64 ? BH / 32 : 0;
+    const int middle = BH >= 64 ? 6 : 4;
+    int c = 0;
+    if (edge > 0) L.start[++c] = edge;
+    const int m0 = L.start[c], m1 = BH - edge;
+    for (int k = 1; k <= middle; ++k) L.start[++c] = m0 + (int)((long long)(m1 - m0) * k / middle);
+    if (edge > 0) L.start[++c] = BH;
+    L.chunks = c;
+  }
+  int per = 0;
+  for (int c = 0; c < L.chunks; ++c) per = std::max(per, L.start[c + 1] - L.start[c]);
+  size_t o = kStatusBytes;  // the step's status word (OR of the chunks') and padding
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  const size_t slice_q = (size_t)d.nq * row_q, slice_v = (size_t)d.nq * row_v;
+  L.q = take(BH * slice_q);
+  L.k = take(BH * slice_q);
+  L.v = take(BH * slice_v);
+  L.dy = take(BH * slice_v);
+  L.y = take(BH * slice_v);
+  L.l = take((size_t)BH * d.nq * 4);
+  L.dq = take(BH * slice_q);
+  L.dk = take(BH * slice_q);
+  L.dv = take(BH * slice_v);
+  L.bits = take(mask_kind == kMaskBitmask ? (size_t)d.nq * ((d.nk + 31) / 32) * 4 : 0);
+  const Dims c{1, per, d.nq, d.nk, d.d, d.v, d.dtype};
+  L.ws_bytes = std::max(fwd_ws_bytes(c), bwd_ws_bytes(c));
+  L.ws = take(L.ws_bytes);
+  L.total = o;
+  return L;
+}
+
+// Streams and events of the host step, made once per host thread and device.
+struct HostStepStreams {
+  int device = -1;
+  cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, loaded[kHostMaxChunks] = {}, done[kHostMaxChunks] = {},
+              end_comp = nullptr, end_out = nullptr;
+};
+
+cudaError_t host_streams(HostStepStreams*& hs) {
+  thread_local HostStepStreams cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (cache.device != dev) {
+    HostStepStreams n;
+    n.device = dev;
+    const unsigned f = cudaEventDisableTiming;
+    if ((e = cudaStreamCreateWithFlags(&n.in, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&n.comp, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&n.out, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&n.start, f)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&n.end_comp, f)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&n.end_out, f)) != cudaSuccess)
+      return e;
+    for (int c = 0; c < kHostMaxChunks; ++c)
+      if ((e = cudaEventCreateWithFlags(&n.loaded[c], f)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&n.done[c], f)) != cudaSuccess)
+        return e;
+    cache = n;  // the previous device's objects are kept (a thread rarely switches)
+  }
+  hs = &cache;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t exattn_host_step_workspace_size(const exattn_shape* shape, int mask_kind) {
+  if (check_shape(shape) != EXATTN_OK) return 0;
+  return host_layout(dims_of(shape), mask_kind).total;
+}
+
+int attn_step_host(const exattn_shape* shape, const void* Q, const void* K, const void* V,
+                   const void* dY, float scale, int mask_kind, int window, const uint32_t* bitmask,
+                   void* Y, float* L, void* dQ, void* dK, void* dV, void* workspace,
+                   size_t workspace_bytes, void* cuda_stream) {
+  int st = check_shape(shape);
+  if (st != EXATTN_OK) return st;
+  st = check_mask(mask_kind, window, bitmask);
+  if (st != EXATTN_OK) return st;
+  if (!Q || !K || !V || !dY || !Y || !L || !dQ || !dK || !dV || !workspace)
+    return EXATTN_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return EXATTN_MISALIGNED;
+  const Dims d = dims_of(shape);
+  const HostStepLayout lay = host_layout(d, mask_kind);
+  if (workspace_bytes < lay.total) return EXATTN_WORKSPACE_TOO_SMALL;
+  exattn::g_last_error[0] = 0;
+  HostStepStreams* hs = nullptr;
+  cudaError_t e = host_streams(hs);
+  if (e != cudaSuccess) return cuda_status(e, "attn_step_host: streams");
+  cudaStream_t user = static_cast<cudaStream_t>(cuda_stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t es = d.dtype == EXATTN_F32 ? 4 : 2;
+  const size_t sq = (size_t)d.nq * d.d * es, sv = (size_t)d.nq * d.v * es, sl = (size_t)d.nq * 4;
+  // Everything after the work already queued on the caller's stream.
+  if ((e = cudaMemsetAsync(ws, 0, kStatusBytes, user)) != cudaSuccess ||
+      (e = cudaEventRecord(hs->start, user)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hs->in, hs->start, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hs->comp, hs->start, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hs->out, hs->start, 0)) != cudaSuccess)
+    return cuda_status(e, "attn_step_host: ordering");
+  const uint32_t* bits_dev = nullptr;
+  if (mask_kind == kMaskBitmask) {
+    const size_t bytes = (size_t)d.nq * ((d.nk + 31) / 32) * 4;
+    if ((e = cudaMemcpyAsync(ws + lay.bits, bitmask, bytes, cudaMemcpyHostToDevice, hs->in)) !=
+        cudaSuccess)
+      return cuda_status(e, "attn_step_host: bitmask copy");
+    bits_dev = reinterpret_cast<const uint32_t*>(ws + lay.bits);
+  }
+  auto h2d = [&](size_t dev_off, const void* host, size_t off, size_t bytes) {
+    return cudaMemcpyAsync(ws + dev_off + off, static_cast<const uint8_t*>(host) + off, bytes,
+                           cudaMemcpyHostToDevice, hs->in);
+  };
+  auto d2h = [&](void* host, size_t dev_off, size_t off, size_t bytes) {
+    return cudaMemcpyAsync(static_cast<uint8_t*>(host) + off, ws + dev_off + off, bytes,
+                           cudaMemcpyDeviceToHost, hs->out);
+  };
+  for (int c = 0; c < lay.chunks; ++c) {
+    const int s0 = lay.start[c], cnt = lay.start[c + 1] - s0;
+    const size_t oq = s0 * sq, ov = s0 * sv, ol = s0 * sl;
+    if ((e = h2d(lay.q, Q, oq, cnt * sq)) != cudaSuccess ||
+        (e = h2d(lay.k, K, oq, cnt * sq)) != cudaSuccess ||
+        (e = h2d(lay.v, V, ov, cnt * sv)) != cudaSuccess ||
+        (e = h2d(lay.dy, dY, ov, cnt * sv)) != cudaSuccess ||
+        (e = cudaEventRecord(hs->loaded[c % kHostMaxChunks], hs->in)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hs->comp, hs->loaded[c % kHostMaxChunks], 0)) != cudaSuccess)
+      return cuda_status(e, "attn_step_host: input copies");
+    const Dims cd{1, cnt, d.nq, d.nk, d.d, d.v, d.dtype};
+    uint8_t* cws = ws + lay.ws;
+    st = fwd_impl(cd, ws + lay.q + oq, ws + lay.k + oq, ws + lay.v + ov, scale, mask_kind, window,
+                  bits_dev, 0.f, 0, ws + lay.y + ov, reinterpret_cast<float*>(ws + lay.l + ol),
+                  cws, lay.ws_bytes, hs->comp);
+    if (st != EXATTN_OK) return st;
+    g_launches.fetch_add(1);
+    status_or_kernel<<<1, 1, 0, hs->comp>>>(reinterpret_cast<unsigned*>(ws),
+                                            reinterpret_cast<const unsigned*>(cws));
+    st = bwd_impl(cd, ws + lay.q + oq, ws + lay.k + oq, ws + lay.v + ov, ws + lay.y + ov,
+                  ws + lay.dy + ov, reinterpret_cast<const float*>(ws + lay.l + ol), scale,
+                  mask_kind, window, bits_dev, 0.f, 0, ws + lay.dq + oq, ws + lay.dk + oq,
+                  ws + lay.dv + ov, cws, lay.ws_bytes, hs->comp);
+    if (st != EXATTN_OK) return st;
+    g_launches.fetch_add(1);
+    status_or_kernel<<<1, 1, 0, hs->comp>>>(reinterpret_cast<unsigned*>(ws),
+                                            reinterpret_cast<const unsigned*>(cws));
+    if ((e = cudaEventRecord(hs->done[c % kHostMaxChunks], hs->comp)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hs->out, hs->done[c % kHostMaxChunks], 0)) != cudaSuccess ||
+        (e = d2h(Y, lay.y, ov, cnt * sv)) != cudaSuccess ||
+        (e = d2h(L, lay.l, ol, cnt * sl)) != cudaSuccess ||
+        (e = d2h(dQ, lay.dq, oq, cnt * sq)) != cudaSuccess ||
+        (e = d2h(dK, lay.dk, oq, cnt * sq)) != cudaSuccess ||
+        (e = d2h(dV, lay.dv, ov, cnt * sv)) != cudaSuccess)
+      return cuda_status(e, "attn_step_host: output copies");
+  }
+  // The caller's stream continues after the last copy out.
+  if ((e = cudaEventRecord(hs->end_out, hs->out)) != cudaSuccess ||
+      (e = cudaEventRecord(hs->end_comp, hs->comp)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(user, hs->end_out, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(user, hs->end_comp, 0)) != cudaSuccess)
+    return cuda_status(e, "attn_step_host: ordering");
+  return EXATTN_OK;
 }
 
 int exattn_device_status(const void* workspace, void* cuda_stream) {

@@ -277,6 +277,38 @@ int attn_bwd_qk(const exattn_qk_shape* shape, const void* Q, const void* K, cons
                 int window, const uint32_t* bitmask, float dropout_p, uint64_t seed, void* dQ,
                 void* dK, void* dV, void* workspace, size_t workspace_bytes, void* cuda_stream);
 
+/* ---------------------------------------------------------------------------
+ * A forward and reverse step on tensors in HOST memory: attn_fwd then
+ * attn_bwd ("Exact tiled softmax attention with block-recomputed
+ * vector-Jacobian products", Forward and Reverse procedures) with the copies to
+ * and from the device inside the call.
+ *
+ * Q, K, V, dY (inputs) and Y, L, dQ, dK, dV (outputs) are host pointers with
+ * the shapes and layouts of attn_fwd / attn_bwd; page-locked (pinned) memory
+ * lets the copies run asynchronously and at full speed, pageable memory works
+ * but the copies then block the calling thread.  `bitmask` (BITMASK only) is a
+ * host pointer too.  No dropout.  `workspace` is device memory of at least
+ * exattn_host_step_workspace_size bytes, 256-byte aligned: it holds device
+ * copies of all nine tensors plus the working space of one chunk.
+ *
+ * The slices are cut into chunks (up to 8).  Chunk k's inputs are copied in on
+ * one internal stream, its forward and reverse pass run on a second, and its
+ * outputs are copied out on a third, so the copies of neighbouring chunks
+ * overlap the kernels.  The call queues everything after the work already on
+ * `cuda_stream` and returns at once; `cuda_stream` waits for the whole step,
+ * so synchronising it (or exattn_device_status on `workspace`) makes the host
+ * outputs valid.  Each slice's results are bitwise those of attn_fwd and
+ * attn_bwd.  The status word of `workspace` is the OR over the chunks.
+ * Host-side failures return before any copy is queued, except CUDA errors met
+ * while queuing, which return EXATTN_CUDA_ERROR with the text in
+ * exattn_last_error.
+ * ------------------------------------------------------------------------- */
+size_t exattn_host_step_workspace_size(const exattn_shape* shape, int mask_kind);
+int attn_step_host(const exattn_shape* shape, const void* Q, const void* K, const void* V,
+                   const void* dY, float scale, int mask_kind, int window, const uint32_t* bitmask,
+                   void* Y, float* L, void* dQ, void* dK, void* dV, void* workspace,
+                   size_t workspace_bytes, void* cuda_stream);
+
 /* Waits for `cuda_stream`, then reads the status word of `workspace` (the
  * workspace of the last call queued on it).  Returns EXATTN_OK,
  * EXATTN_EMPTY_ROW, EXATTN_TIMEOUT or EXATTN_CUDA_ERROR. */
@@ -285,11 +317,13 @@ int exattn_device_status(const void* workspace, void* cuda_stream);
 /* Profiling aid.  Kernels of the library, by role. */
 enum exattn_kernel {
   EXATTN_KERNEL_FWD = 0,        /* the forward kernel of attn_fwd */
-  EXATTN_KERNEL_DELTA = 1,      /* delta_i = dY_i . Y_i in attn_bwd */
+  EXATTN_KERNEL_DELTA = 1,      /* delta_i = dY_i . Y_i in attn_bwd (not launched on the
+                                   AUTO tensor-core path: its dQ kernel forms delta) */
   EXATTN_KERNEL_BWD = 2,        /* the reverse kernel(s) of attn_bwd: start before the first,
-                                   stop after the last (dK/dV and dQ kernels on AUTO) */
+                                   stop after the last (dQ, then dK/dV kernel on AUTO) */
   EXATTN_KERNEL_DQ_CONVERT = 3, /* fp32 dQ accumulator -> dQ (SIMT and ATOMIC_DQ paths) */
-  EXATTN_KERNEL_BWD_Q = 4,      /* the query-major dQ kernel alone (AUTO path) */
+  EXATTN_KERNEL_BWD_Q = 4,      /* the query-major dQ kernel alone (AUTO path; it also
+                                   forms delta_i and L_i log2 e for the dK/dV kernel) */
   EXATTN_KERNEL_SPLIT_PARTIAL = 5, /* per-chunk summaries of attn_fwd_splitkv */
   EXATTN_KERNEL_SPLIT_MERGE = 6,   /* the merge kernel of attn_fwd_splitkv (nq > 4) */
   EXATTN_KERNEL_SPLIT32 = 7        /* the tf32 hi / lo split of K and V (fp32 forward) */

@@ -90,6 +90,32 @@ def test_host_side_argument_checks(lib):
                         good, ws, 1 << 30, None) == 1
 
 
+def test_host_step_checks_and_workspace(lib):
+    """attn_step_host rejects bad arguments before any CUDA call; its workspace
+    holds the nine tensors plus one chunk's working space, so it is linear in n."""
+    vp = ctypes.c_void_p
+    good, ws = vp(1 << 20), vp(1 << 21)
+
+    def step(shape, mask=0, window=0, bitmask=None, q=good, ws_ptr=ws, ws_bytes=1 << 40):
+        return lib.attn_step_host(ctypes.byref(shape), q, good, good, good, 1.0, mask, window,
+                                  bitmask, good, good, good, good, good, ws_ptr, ws_bytes, None)
+
+    assert step(_shape(n=0)) == 1                      # INVALID_ARG
+    assert step(_shape(d=300)) == 2                    # UNSUPPORTED
+    assert step(_shape(), mask=3, bitmask=None) == 1   # bitmask required
+    assert step(_shape(), mask=2, window=0) == 1
+    assert step(_shape(), q=None) == 1
+    assert step(_shape(), ws_ptr=vp((1 << 21) + 16)) == 3
+    assert step(_shape(), ws_bytes=8) == 4             # WORKSPACE_TOO_SMALL
+
+    def size(n):
+        return lib.exattn_host_step_workspace_size(ctypes.byref(_shape(n=n, d=128)), 1)
+
+    s1, s2, s4 = size(1024), size(2048), size(4096)
+    assert s1 > 0 and s4 - s2 == 2 * (s2 - s1)
+    assert lib.exattn_host_step_workspace_size(None, 0) == 0
+
+
 def test_path_switch(lib):
     import exact_tiled_softmax_gb300 as ex
     assert ex.set_path("simt") == "auto"
