@@ -8,15 +8,23 @@
 // with delta_i = G_i . Y_i (HarshvardhanJ/FlashAttention, backward section).
 // Each kernel recomputes the probability block it needs; neither stores an
 // n x n matrix, and dQ is written once per query block, so no fp32
-// accumulator or reductions are needed.
+// accumulator or reductions are needed.  The dQ kernel runs first: it also
+// forms delta_i and L_i log2(e) for its query block and writes both for the
+// dK/dV kernel.
 //
-// tc_bwd_kv_kernel -- one CTA per 128-key block, loop over query blocks.
+// Both kernels are persistent: one CTA per SM takes items (a block of 128 keys
+// or queries of one slice) from a counter in the workspace, in groups of 16
+// slices with the heaviest causal blocks first, and hands them to its warps
+// through a two-entry ring in shared memory.  Results leave through swizzled
+// shared-memory tiles and TMA stores.
+// tc_bwd_kv_kernel -- item = a 128-key block; loop over query blocks.
 //   TMEM: A [0,128) S^T then P^T (bf16), B [128,256) dP^T then dS^T (bf16),
 //   dV [256, 256+V), dK [256+V, 256+V+D).  S^T and dP^T are computed in two
 //   64-query halves so that the elementwise work of one half overlaps the MMAs
 //   of the other; dV and dK then take each half as a K = 64 contraction.
-// tc_bwd_q_kernel -- one CTA per 128-query block, loop over key blocks.
-//   K/V ring order V(0), K(0), V(1), K(1), ...
+// tc_bwd_q_kernel -- item = a 128-query block; loop over key blocks.
+//   K and V in separate rings (3 + 1 slots for d = 128): V(t) is read only by
+//   dP(t), K(t) until dQ(t).
 //   TMEM: S [0,128), dP double buffer [128,256) and [256,384) (dS bf16 is
 //   written over its own dP), dQ [384, 384+D).  S(t+1) is issued as soon as
 //   the elementwise warps hold S(t) in registers (before they compute dS(t));
@@ -754,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // =========================================================================
-// Query-major kernel: dQ
+// Query-major kernel: dQ (and delta)
 // =========================================================================
 template <int D, int V>
 struct QLayout {
