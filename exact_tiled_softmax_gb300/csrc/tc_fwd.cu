@@ -78,7 +78,10 @@ struct FwdParams {
   float* pz;
 };
 
-template <int D, int V>
+// kSum: the split-KV summary mode, which writes its rows with plain stores:
+// no Y staging tiles, and the room goes to a deeper K/V ring (the mode is
+// memory-bound).
+template <int D, int V, bool kSum = false>
 struct Layout {
   static constexpr int DCH = D / 64;
   static constexpr int VCH = V / 64;
@@ -86,12 +89,12 @@ struct Layout {
   static constexpr int KBYTES = kBN * D * 2;
   static constexpr int VBYTES = kBN * V * 2;
   static constexpr int SLOT = KBYTES > VBYTES ? KBYTES : VBYTES;
-  static constexpr int NSLOT = D == 128 ? 3 : 6;
+  static constexpr int NSLOT = kSum ? (D == 128 ? 4 : 8) : (D == 128 ? 3 : 6);
   static constexpr int Q_OFF = 0;
   static constexpr int SLOT_OFF = Q_OFF + 2 * QTILE;
   // Y staging tiles, one per row tile: kBM rows as 64-column boxes (128-byte swizzle).
   static constexpr int YST_OFF = SLOT_OFF + NSLOT * SLOT;
-  static constexpr int YST = kBM * V * 2;
+  static constexpr int YST = kSum ? 0 : kBM * V * 2;
   static constexpr int BAR_OFF = YST_OFF + 2 * YST;
   // barriers: q_full, q_free, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2],
   // o_done[2], o_read[2], item ring full[2] / empty[2], Y tile free[2] / staged[2], drain
@@ -197,9 +200,9 @@ __device__ __forceinline__ FwdItem make_item(const FwdParams& p, int t) {
   return w;
 }
 
-template <int D, int V, bool kDrop>
+template <int D, int V, bool kDrop, bool kSum>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using Lay = Layout<D, V>;
+  using Lay = Layout<D, V, kSum>;
   constexpr int NS = Lay::NSLOT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -640,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       tc_fence_after();
       const bool have_o = cnt > cnt0;
       const bool valid = i < n;
-      if (p.chunk_kt > 0) {
+      if constexpr (kSum) {
         // Split-KV summary of this key chunk for row i ("Exact tiled softmax
         // attention ...", Forward procedure: the summary of a block of keys).
         const size_t row = (static_cast<size_t>(bh) * p.splits + w.split) * n + (valid ? i : 0);
@@ -823,10 +826,13 @@ cudaError_t launch_tc_fwd_d(const FwdArgs& a, cudaStream_t s, int chunk_kt = 0, 
   p.pm = pm;
   p.pl = pl;
   p.pz = pz;
-  using Lay = Layout<D, D>;
-  auto kern = pr.drop_t != 0 ? tc_fwd_kernel<D, D, true> : tc_fwd_kernel<D, D, false>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC);
+  const bool sum = chunk_kt > 0;
+  if (sum && pr.drop_t != 0) return cudaErrorInvalidValue;  // the summaries take no dropout
+  auto kern = sum ? tc_fwd_kernel<D, D, false, true>
+                  : pr.drop_t != 0 ? tc_fwd_kernel<D, D, true, false>
+                                   : tc_fwd_kernel<D, D, false, false>;
+  const int alloc = sum ? Layout<D, D, true>::ALLOC : Layout<D, D, false>::ALLOC;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, alloc);
   if (e != cudaSuccess) {
     record_error("tc_fwd: cudaFuncSetAttribute", static_cast<int>(e), cudaGetErrorString(e));
     return e;
@@ -844,7 +850,7 @@ cudaError_t launch_tc_fwd_d(const FwdArgs& a, cudaStream_t s, int chunk_kt = 0, 
   }
   const int role = chunk_kt > 0 ? kKernSplitPartial : kKernFwd;
   before_launch(role, s);
-  kern<<<grid, kThreads, Lay::ALLOC, s>>>(p);
+  kern<<<grid, kThreads, alloc, s>>>(p);
   after_launch(role, s);
   return cudaGetLastError();
 }
