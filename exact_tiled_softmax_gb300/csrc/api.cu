@@ -540,19 +540,23 @@ HostStepLayout host_layout(const Dims& d, int mask_kind) {
   return L;
 }
 
-// Streams and events of the host step, made once per host thread and device.
+// Streams and events of the host step, made once per host thread and device
+// (and kept for the thread's lifetime).
+constexpr int kHostMaxDevices = 64;
 struct HostStepStreams {
   int device = -1;
   cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
   cudaEvent_t start = nullptr, loaded[kHostMaxChunks] = {}, done[kHostMaxChunks] = {},
-              end_comp = nullptr, end_out = nullptr;
+              end_in = nullptr, end_comp = nullptr, end_out = nullptr;
 };
 
 cudaError_t host_streams(HostStepStreams*& hs) {
-  thread_local HostStepStreams cache;
+  thread_local HostStepStreams caches[kHostMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kHostMaxDevices) return cudaErrorInvalidDevice;
+  HostStepStreams& cache = caches[dev];
   if (cache.device != dev) {
     HostStepStreams n;
     n.device = dev;
@@ -561,6 +565,7 @@ cudaError_t host_streams(HostStepStreams*& hs) {
         (e = cudaStreamCreateWithFlags(&n.comp, cudaStreamNonBlocking)) != cudaSuccess ||
         (e = cudaStreamCreateWithFlags(&n.out, cudaStreamNonBlocking)) != cudaSuccess ||
         (e = cudaEventCreateWithFlags(&n.start, f)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&n.end_in, f)) != cudaSuccess ||
         (e = cudaEventCreateWithFlags(&n.end_comp, f)) != cudaSuccess ||
         (e = cudaEventCreateWithFlags(&n.end_out, f)) != cudaSuccess)
       return e;
@@ -568,7 +573,7 @@ cudaError_t host_streams(HostStepStreams*& hs) {
       if ((e = cudaEventCreateWithFlags(&n.loaded[c], f)) != cudaSuccess ||
           (e = cudaEventCreateWithFlags(&n.done[c], f)) != cudaSuccess)
         return e;
-    cache = n;  // the previous device's objects are kept (a thread rarely switches)
+    cache = n;
   }
   hs = &cache;
   return cudaSuccess;
@@ -612,65 +617,74 @@ int attn_step_host(const exattn_shape* shape, const void* Q, const void* K, cons
       (e = cudaStreamWaitEvent(hs->comp, hs->start, 0)) != cudaSuccess ||
       (e = cudaStreamWaitEvent(hs->out, hs->start, 0)) != cudaSuccess)
     return cuda_status(e, "attn_step_host: ordering");
-  const uint32_t* bits_dev = nullptr;
-  if (mask_kind == kMaskBitmask) {
-    const size_t bytes = (size_t)d.nq * ((d.nk + 31) / 32) * 4;
-    if ((e = cudaMemcpyAsync(ws + lay.bits, bitmask, bytes, cudaMemcpyHostToDevice, hs->in)) !=
-        cudaSuccess)
-      return cuda_status(e, "attn_step_host: bitmask copy");
-    bits_dev = reinterpret_cast<const uint32_t*>(ws + lay.bits);
-  }
-  auto h2d = [&](size_t dev_off, const void* host, size_t off, size_t bytes) {
-    return cudaMemcpyAsync(ws + dev_off + off, static_cast<const uint8_t*>(host) + off, bytes,
-                           cudaMemcpyHostToDevice, hs->in);
+  // The copies and kernels of every chunk.  Whatever it returns, the caller's
+  // stream then waits for all three internal streams, so no queued copy can
+  // outlive the buffers the caller frees after a failure.
+  auto queue = [&]() -> int {
+    const uint32_t* bits_dev = nullptr;
+    if (mask_kind == kMaskBitmask) {
+      const size_t bytes = (size_t)d.nq * ((d.nk + 31) / 32) * 4;
+      if ((e = cudaMemcpyAsync(ws + lay.bits, bitmask, bytes, cudaMemcpyHostToDevice, hs->in)) !=
+          cudaSuccess)
+        return cuda_status(e, "attn_step_host: bitmask copy");
+      bits_dev = reinterpret_cast<const uint32_t*>(ws + lay.bits);
+    }
+    auto h2d = [&](size_t dev_off, const void* host, size_t off, size_t bytes) {
+      return cudaMemcpyAsync(ws + dev_off + off, static_cast<const uint8_t*>(host) + off, bytes,
+                             cudaMemcpyHostToDevice, hs->in);
+    };
+    auto d2h = [&](void* host, size_t dev_off, size_t off, size_t bytes) {
+      return cudaMemcpyAsync(static_cast<uint8_t*>(host) + off, ws + dev_off + off, bytes,
+                             cudaMemcpyDeviceToHost, hs->out);
+    };
+    for (int c = 0; c < lay.chunks; ++c) {
+      const int s0 = lay.start[c], cnt = lay.start[c + 1] - s0;
+      const size_t oq = s0 * sq, ov = s0 * sv, ol = s0 * sl;
+      if ((e = h2d(lay.q, Q, oq, cnt * sq)) != cudaSuccess ||
+          (e = h2d(lay.k, K, oq, cnt * sq)) != cudaSuccess ||
+          (e = h2d(lay.v, V, ov, cnt * sv)) != cudaSuccess ||
+          (e = h2d(lay.dy, dY, ov, cnt * sv)) != cudaSuccess ||
+          (e = cudaEventRecord(hs->loaded[c % kHostMaxChunks], hs->in)) != cudaSuccess ||
+          (e = cudaStreamWaitEvent(hs->comp, hs->loaded[c % kHostMaxChunks], 0)) != cudaSuccess)
+        return cuda_status(e, "attn_step_host: input copies");
+      const Dims cd{1, cnt, d.nq, d.nk, d.d, d.v, d.dtype};
+      uint8_t* cws = ws + lay.ws;
+      st = fwd_impl(cd, ws + lay.q + oq, ws + lay.k + oq, ws + lay.v + ov, scale, mask_kind, window,
+                    bits_dev, 0.f, 0, ws + lay.y + ov, reinterpret_cast<float*>(ws + lay.l + ol),
+                    cws, lay.ws_bytes, hs->comp);
+      if (st != EXATTN_OK) return st;
+      g_launches.fetch_add(1);
+      status_or_kernel<<<1, 1, 0, hs->comp>>>(reinterpret_cast<unsigned*>(ws),
+                                              reinterpret_cast<const unsigned*>(cws));
+      st = bwd_impl(cd, ws + lay.q + oq, ws + lay.k + oq, ws + lay.v + ov, ws + lay.y + ov,
+                    ws + lay.dy + ov, reinterpret_cast<const float*>(ws + lay.l + ol), scale,
+                    mask_kind, window, bits_dev, 0.f, 0, ws + lay.dq + oq, ws + lay.dk + oq,
+                    ws + lay.dv + ov, cws, lay.ws_bytes, hs->comp);
+      if (st != EXATTN_OK) return st;
+      g_launches.fetch_add(1);
+      status_or_kernel<<<1, 1, 0, hs->comp>>>(reinterpret_cast<unsigned*>(ws),
+                                              reinterpret_cast<const unsigned*>(cws));
+      if ((e = cudaEventRecord(hs->done[c % kHostMaxChunks], hs->comp)) != cudaSuccess ||
+          (e = cudaStreamWaitEvent(hs->out, hs->done[c % kHostMaxChunks], 0)) != cudaSuccess ||
+          (e = d2h(Y, lay.y, ov, cnt * sv)) != cudaSuccess ||
+          (e = d2h(L, lay.l, ol, cnt * sl)) != cudaSuccess ||
+          (e = d2h(dQ, lay.dq, oq, cnt * sq)) != cudaSuccess ||
+          (e = d2h(dK, lay.dk, oq, cnt * sq)) != cudaSuccess ||
+          (e = d2h(dV, lay.dv, ov, cnt * sv)) != cudaSuccess)
+        return cuda_status(e, "attn_step_host: output copies");
+    }
+    return EXATTN_OK;
   };
-  auto d2h = [&](void* host, size_t dev_off, size_t off, size_t bytes) {
-    return cudaMemcpyAsync(static_cast<uint8_t*>(host) + off, ws + dev_off + off, bytes,
-                           cudaMemcpyDeviceToHost, hs->out);
-  };
-  for (int c = 0; c < lay.chunks; ++c) {
-    const int s0 = lay.start[c], cnt = lay.start[c + 1] - s0;
-    const size_t oq = s0 * sq, ov = s0 * sv, ol = s0 * sl;
-    if ((e = h2d(lay.q, Q, oq, cnt * sq)) != cudaSuccess ||
-        (e = h2d(lay.k, K, oq, cnt * sq)) != cudaSuccess ||
-        (e = h2d(lay.v, V, ov, cnt * sv)) != cudaSuccess ||
-        (e = h2d(lay.dy, dY, ov, cnt * sv)) != cudaSuccess ||
-        (e = cudaEventRecord(hs->loaded[c % kHostMaxChunks], hs->in)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(hs->comp, hs->loaded[c % kHostMaxChunks], 0)) != cudaSuccess)
-      return cuda_status(e, "attn_step_host: input copies");
-    const Dims cd{1, cnt, d.nq, d.nk, d.d, d.v, d.dtype};
-    uint8_t* cws = ws + lay.ws;
-    st = fwd_impl(cd, ws + lay.q + oq, ws + lay.k + oq, ws + lay.v + ov, scale, mask_kind, window,
-                  bits_dev, 0.f, 0, ws + lay.y + ov, reinterpret_cast<float*>(ws + lay.l + ol),
-                  cws, lay.ws_bytes, hs->comp);
-    if (st != EXATTN_OK) return st;
-    g_launches.fetch_add(1);
-    status_or_kernel<<<1, 1, 0, hs->comp>>>(reinterpret_cast<unsigned*>(ws),
-                                            reinterpret_cast<const unsigned*>(cws));
-    st = bwd_impl(cd, ws + lay.q + oq, ws + lay.k + oq, ws + lay.v + ov, ws + lay.y + ov,
-                  ws + lay.dy + ov, reinterpret_cast<const float*>(ws + lay.l + ol), scale,
-                  mask_kind, window, bits_dev, 0.f, 0, ws + lay.dq + oq, ws + lay.dk + oq,
-                  ws + lay.dv + ov, cws, lay.ws_bytes, hs->comp);
-    if (st != EXATTN_OK) return st;
-    g_launches.fetch_add(1);
-    status_or_kernel<<<1, 1, 0, hs->comp>>>(reinterpret_cast<unsigned*>(ws),
-                                            reinterpret_cast<const unsigned*>(cws));
-    if ((e = cudaEventRecord(hs->done[c % kHostMaxChunks], hs->comp)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(hs->out, hs->done[c % kHostMaxChunks], 0)) != cudaSuccess ||
-        (e = d2h(Y, lay.y, ov, cnt * sv)) != cudaSuccess ||
-        (e = d2h(L, lay.l, ol, cnt * sl)) != cudaSuccess ||
-        (e = d2h(dQ, lay.dq, oq, cnt * sq)) != cudaSuccess ||
-        (e = d2h(dK, lay.dk, oq, cnt * sq)) != cudaSuccess ||
-        (e = d2h(dV, lay.dv, ov, cnt * sv)) != cudaSuccess)
-      return cuda_status(e, "attn_step_host: output copies");
-  }
-  // The caller's stream continues after the last copy out.
+  const int queued = queue();
+  // The caller's stream continues after the last copy out and the last kernel.
   if ((e = cudaEventRecord(hs->end_out, hs->out)) != cudaSuccess ||
       (e = cudaEventRecord(hs->end_comp, hs->comp)) != cudaSuccess ||
+      (e = cudaEventRecord(hs->end_in, hs->in)) != cudaSuccess ||
       (e = cudaStreamWaitEvent(user, hs->end_out, 0)) != cudaSuccess ||
-      (e = cudaStreamWaitEvent(user, hs->end_comp, 0)) != cudaSuccess)
-    return cuda_status(e, "attn_step_host: ordering");
-  return EXATTN_OK;
+      (e = cudaStreamWaitEvent(user, hs->end_comp, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(user, hs->end_in, 0)) != cudaSuccess)
+    return queued != EXATTN_OK ? queued : cuda_status(e, "attn_step_host: ordering");
+  return queued;
 }
 
 int exattn_device_status(const void* workspace, void* cuda_stream) {

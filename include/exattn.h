@@ -299,9 +299,10 @@ int attn_bwd_qk(const exattn_qk_shape* shape, const void* Q, const void* K, cons
  * so synchronising it (or exattn_device_status on `workspace`) makes the host
  * outputs valid.  Each slice's results are bitwise those of attn_fwd and
  * attn_bwd.  The status word of `workspace` is the OR over the chunks.
- * Host-side failures return before any copy is queued, except CUDA errors met
- * while queuing, which return EXATTN_CUDA_ERROR with the text in
- * exattn_last_error.
+ * Host-side failures return before any copy is queued.  A CUDA error met while
+ * queuing returns EXATTN_CUDA_ERROR (text in exattn_last_error); `cuda_stream`
+ * still waits for whatever had been queued, so the buffers may be freed once it
+ * is synchronised.
  * ------------------------------------------------------------------------- */
 size_t exattn_host_step_workspace_size(const exattn_shape* shape, int mask_kind);
 int attn_step_host(const exattn_shape* shape, const void* Q, const void* K, const void* V,
