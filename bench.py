@@ -287,14 +287,23 @@ TF32_OVER_BF16 = 1.1 / 2.25
 def kernel_roofline(args, w, which, achieved, peaks, peak_kind):
     """Roofline object for the forward ("fwd") or reverse ("bwd") kernel(s)."""
     eligible = args.path != "simt" and w.d == w.v and w.d in (64, 128)
+    # bf16 widths up to 128 in steps of 8 run on the tensor-core kernels of width 64
+    # or 128 (zero-padded); the atomic reverse form takes only d = v in {64, 128}.
+    padded = not eligible
+    tc_bf16 = (args.path != "simt" and w.d % 8 == 0 and w.v % 8 == 0 and w.d <= 128
+               and w.v <= 128 and not (which == "bwd" and args.path == "atomic_dq" and padded))
     bf16_peak = float(peaks["bf16_tflops"])
-    if w.dtype == "bf16" and eligible:
+    if w.dtype == "bf16" and tc_bf16:
         tag = f"tc_{which}"
         if which == "bwd":
             tag += "_atomic" if args.path == "atomic_dq" else "_split"
-        return {"kernel": tag, "bound": "tensor", "achieved": achieved, "peak": bf16_peak,
-                "unit": "TFLOP/s", "frac": achieved / bf16_peak,
-                "peak_kind": f"bf16 dense burst, of {peak_kind}", "traffic": read_traffic(tag)}
+        out = {"kernel": tag, "bound": "tensor", "achieved": achieved, "peak": bf16_peak,
+               "unit": "TFLOP/s", "frac": achieved / bf16_peak,
+               "peak_kind": f"bf16 dense burst, of {peak_kind}",
+               "traffic": None if padded else read_traffic(tag)}
+        if padded:
+            out["padded_to"] = 64 if w.d <= 64 and w.v <= 64 else 128
+        return out
     if w.dtype == "f32" and eligible and which == "fwd" and not args.dropout:
         peak = bf16_peak * TF32_OVER_BF16
         return {"kernel": "tc32_fwd", "bound": "tensor", "achieved": achieved, "peak": peak,
@@ -382,8 +391,8 @@ def run_gpu(args, w):
     # The split tensor-core reverse pass (bf16, d = v in {64, 128}) also brackets
     # its dQ kernel, so the dK/dV kernel's time is the difference; its dQ kernel
     # forms delta itself (no delta launch).
-    split_bwd = (w.dtype == "bf16" and w.d == w.v and w.d in (64, 128)
-                 and args.path == "auto"
+    split_bwd = (w.dtype == "bf16" and w.d % 8 == 0 and w.v % 8 == 0 and w.d <= 128
+                 and w.v <= 128 and args.path == "auto"
                  and (w.mask != "bitmask" or max(w.n, w.n_keys) <= 256 * 128))
     roles = ((ex.KERNEL_FWD, ex.KERNEL_BWD, ex.KERNEL_BWD_Q) if split_bwd
              else (ex.KERNEL_FWD, ex.KERNEL_BWD, ex.KERNEL_DELTA))

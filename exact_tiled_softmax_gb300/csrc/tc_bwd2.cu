@@ -65,6 +65,8 @@ struct Bwd2Params {
   CUtensorMap tdq;       // dQ as a store target (dQ kernel)
   CUtensorMap ty;        // Y, for the dQ kernel's L2 prefetch of the next item's rows
   int n, npad, BH, mask_kind, window, words_per_row;
+  int d;  // columns of Q, K, dQ and dK in memory (<= the kernel's D; TMA fills the rest with zeros)
+  int v;  // columns of V, Y, dY and dV in memory (<= the kernel's V, likewise)
   int nk, off;  // keys, and the absolute position of query 0 (nk - n)
   const uint32_t* bits;
   float* delta;  // [BH][npad]: written by the dQ kernel, read by the dK/dV kernel
@@ -395,8 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t_next < items && leader) {
           int kbn, bhn;
           kv_item(t_next, nkb, p.BH, kbn, bhn);
-          for (int c = 0; c < D / 64; ++c) tma_prefetch_3d(&p.tk, 64 * c, kbn * kBN, bhn);
-          for (int c = 0; c < V / 64; ++c) tma_prefetch_3d(&p.tv, 64 * c, kbn * kBN, bhn);
+          for (int c = 0; c < D / 64; ++c)
+            if (64 * c < p.d) tma_prefetch_3d(&p.tk, 64 * c, kbn * kBN, bhn);
+          for (int c = 0; c < V / 64; ++c)
+            if (64 * c < p.v) tma_prefetch_3d(&p.tv, 64 * c, kbn * kBN, bhn);
         }
       };
       for (int qb = qb_begin; qb < qb_end; ++qb) {
@@ -731,8 +735,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (threadIdx.x == (is_dv ? 0 : 32 * (kEwWarps / 2))) {
         if (mbar_wait(bar(is_dv ? Lay::B_EPIV : Lay::B_EPIK), nitem & 1, abort_flag)) {
           const CUtensorMap* map = is_dv ? &p.tdv : &p.tdk;
+          const int cols = is_dv ? p.v : p.d;  // no box that starts past the columns
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) tma_store_3d(map, tile + c * (kBN * 128), 64 * c, k0, bh);
+          for (int c = 0; c < D / 64; ++c)
+            if (64 * c < cols) tma_store_3d(map, tile + c * (kBN * 128), 64 * c, k0, bh);
           bulk_commit();
           if (is_dv) {
             bulk_wait_read_all();
@@ -943,8 +949,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t_next < items && leader) {
           int qbn, bhn;
           item_of(t_next, qbn, bhn);
-          for (int c = 0; c < D / 64; ++c) tma_prefetch_3d(&p.tq, 64 * c, qbn * kBM, bhn);
+          for (int c = 0; c < D / 64; ++c)
+            if (64 * c < p.d) tma_prefetch_3d(&p.tq, 64 * c, qbn * kBM, bhn);
           for (int c = 0; c < V / 64; ++c) {
+            if (64 * c >= p.v) break;
             tma_prefetch_3d(&p.tdy, 64 * c, qbn * kBM, bhn);
             tma_prefetch_3d(&p.ty, 64 * c, qbn * kBM, bhn);  // for delta
           }
@@ -1146,10 +1154,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ix = qbx * kBM + r;
       Li = -INFINITY;
       if (ix < n) {
-        const uint4* yrow =
-            reinterpret_cast<const uint4*>(p.Y + (static_cast<size_t>(bhx) * n + ix) * V + CV * g);
+        const uint4* yrow = reinterpret_cast<const uint4*>(
+            p.Y + (static_cast<size_t>(bhx) * n + ix) * p.v + CV * g);
 #pragma unroll
-        for (int u = 0; u < CV / 8; ++u) yv[u] = __ldg(yrow + u);
+        for (int u = 0; u < CV / 8; ++u)  // columns past v: zero (as in the staged dY)
+          yv[u] = CV * g + 8 * u < p.v ? __ldg(yrow + u) : make_uint4(0u, 0u, 0u, 0u);
         Li = __ldg(p.L + static_cast<size_t>(bhx) * n + ix);
       }
     };
@@ -1328,8 +1337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (threadIdx.x == 0) {
         if (mbar_wait(bar(Lay::B_EPI), nitem & 1, abort_flag)) {
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_store_3d(&p.tdq, tile + c * (kBM * 128), 64 * c, q0, bh);
+          for (int c = 0; c < D / 64; ++c)  // no box that starts past dQ's columns
+            if (64 * c < p.d) tma_store_3d(&p.tdq, tile + c * (kBM * 128), 64 * c, q0, bh);
           bulk_commit();
         } else {
           ok = false;
@@ -1359,18 +1368,23 @@ template <int D>
 cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
   const Problem& pr = a.p;
   Bwd2Params p;
-  if (!make_tmap_bf16(&p.tq, a.Q, D, pr.n, pr.BH) || !make_tmap_bf16(&p.tk, a.K, D, pr.nk, pr.BH) ||
-      !make_tmap_bf16(&p.tv, a.V, D, pr.nk, pr.BH) ||
-      !make_tmap_bf16(&p.tdy, a.dY, D, pr.n, pr.BH) ||
-      !make_tmap_bf16(&p.tdk, a.dK, D, pr.nk, pr.BH) ||
-      !make_tmap_bf16(&p.tdv, a.dV, D, pr.nk, pr.BH) ||
-      !make_tmap_bf16(&p.tdq, a.dQ, D, pr.n, pr.BH) ||
-      !make_tmap_bf16(&p.ty, a.Y, D, pr.n, pr.BH))
+  // Tensor maps of the true widths: loads fill the columns up to D with zeros
+  // (no contribution to S, dP, dV or dK), stores clip them.
+  if (!make_tmap_bf16(&p.tq, a.Q, pr.d, pr.n, pr.BH) ||
+      !make_tmap_bf16(&p.tk, a.K, pr.d, pr.nk, pr.BH) ||
+      !make_tmap_bf16(&p.tv, a.V, pr.v, pr.nk, pr.BH) ||
+      !make_tmap_bf16(&p.tdy, a.dY, pr.v, pr.n, pr.BH) ||
+      !make_tmap_bf16(&p.tdk, a.dK, pr.d, pr.nk, pr.BH) ||
+      !make_tmap_bf16(&p.tdv, a.dV, pr.v, pr.nk, pr.BH) ||
+      !make_tmap_bf16(&p.tdq, a.dQ, pr.d, pr.n, pr.BH) ||
+      !make_tmap_bf16(&p.ty, a.Y, pr.v, pr.n, pr.BH))
     return cudaErrorInvalidValue;
   p.n = pr.n;
   p.nk = pr.nk;
   p.off = pr.nk - pr.n;
   p.npad = a.npad;
+  p.d = pr.d;
+  p.v = pr.v;
   p.BH = pr.BH;
   p.mask_kind = pr.mask_kind;
   p.window = pr.window;
@@ -1431,15 +1445,19 @@ cudaError_t launch_split(const BwdArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+// Widths up to 128 in steps of 8 run on the kernels of width 64 or 128 (see
+// the tensor maps in launch_split).
 bool tc_bwd_split_supported(const Problem& p) {
-  if (p.dtype != kBF16 || p.d != p.v || (p.d != 64 && p.d != 128)) return false;
+  if (p.dtype != kBF16 || p.d < 8 || p.v < 8 || p.d > 128 || p.v > 128 || p.d % 8 != 0 ||
+      p.v % 8 != 0)
+    return false;
   if (p.mask_kind == kMaskBitmask && (p.n > kMaxBlocks * kBM || p.nk > kMaxBlocks * kBN))
     return false;
   return tmap_encoder_available();
 }
 
 cudaError_t launch_tc_bwd_split(const BwdArgs& a, cudaStream_t s) {
-  return a.p.d == 128 ? launch_split<128>(a, s) : launch_split<64>(a, s);
+  return a.p.d <= 64 && a.p.v <= 64 ? launch_split<64>(a, s) : launch_split<128>(a, s);
 }
 
 }  // namespace exattn

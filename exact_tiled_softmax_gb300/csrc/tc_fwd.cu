@@ -62,6 +62,7 @@ struct FwdParams {
   unsigned* sched;  // item counter (zero at launch)
   int n, BH, n_qblocks, mask_kind, window, words_per_row;
   int nk, off;  // keys, and the absolute position of query 0 (nk - n)
+  int dw, vw;   // columns of Q, K and of V, Y in memory (<= the kernel's D, V)
   const uint32_t* bits;
   float sl2;  // scale * log2(e), > 0
   __nv_bfloat16* Y;
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             for (int X = 0; X < 2; ++X)
               if (wn.rows[X].valid)
                 for (int c = 0; c < Lay::DCH; ++c)
-                  tma_prefetch_3d(&p.tq, 64 * c, wn.q0 + X * kBM, wn.bh);
+                  if (64 * c < p.dw) tma_prefetch_3d(&p.tq, 64 * c, wn.q0 + X * kBM, wn.bh);
           }
         };
         for (int kt = w.kt_begin; kt < w.kt_end && ok; ++kt) {
@@ -723,8 +724,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           if (mbar_wait(bar(Lay::B_Y + X), nitem & 1, abort_flag)) {
             if (mine.valid)
 #pragma unroll
-              for (int c = 0; c < Lay::VCH; ++c)
-                tma_store_3d(&p.ty, tile + c * (kBM * 128), 64 * c, w.q0 + X * kBM, bh);
+              for (int c = 0; c < Lay::VCH; ++c)  // no box that starts past Y's columns
+                if (64 * c < p.vw)
+                  tma_store_3d(&p.ty, tile + c * (kBM * 128), 64 * c, w.q0 + X * kBM, bh);
             bulk_commit();
           } else {
             ok = false;
@@ -766,7 +768,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 // 3-D bf16 tensor map over [BH][n][width] with 64 x 128 x 1 boxes and 128-byte
-// swizzle; rows beyond n read as zeros.
+// swizzle; columns beyond width and rows beyond n read as zeros, and stores clip them.
 bool make_tmap_bf16(CUtensorMap* m, const void* base, int width, int n, int BH) {
   auto enc = encode_fn();
   if (!enc) return false;
@@ -787,8 +789,16 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, int width, int n, int BH) 
 bool tmap_encoder_available() { return encode_fn() != nullptr; }
 PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() { return encode_fn(); }
 
+// Widths up to 128 in steps of 8 run on the kernel of width 64 or 128: the
+// tensor maps have the true widths, so TMA loads fill the missing columns of
+// Q, K and V with zeros (which change neither S nor P.V) and TMA stores clip
+// them from Y.
+int padded_width(const Problem& p) { return p.d <= 64 && p.v <= 64 ? 64 : 128; }
+
 bool tc_fwd_supported(const Problem& p) {
-  if (p.dtype != kBF16 || p.d != p.v || (p.d != 64 && p.d != 128)) return false;
+  if (p.dtype != kBF16 || p.d < 8 || p.v < 8 || p.d > 128 || p.v > 128 || p.d % 8 != 0 ||
+      p.v % 8 != 0)
+    return false;
   if (!(p.scale > 0.f)) return false;
   if (p.mask_kind == kMaskBitmask && p.nk > kMaxKT * kBN) return false;
   return encode_fn() != nullptr;
@@ -799,12 +809,15 @@ cudaError_t launch_tc_fwd_d(const FwdArgs& a, cudaStream_t s, int chunk_kt = 0, 
                             float* pm = nullptr, float* pl = nullptr, float* pz = nullptr) {
   const Problem& pr = a.p;
   FwdParams p;
-  if (!make_tmap_bf16(&p.tq, a.Q, D, pr.n, pr.BH) || !make_tmap_bf16(&p.tk, a.K, D, pr.nk, pr.BH) ||
-      !make_tmap_bf16(&p.tv, a.V, D, pr.nk, pr.BH))
+  if (!make_tmap_bf16(&p.tq, a.Q, pr.d, pr.n, pr.BH) ||
+      !make_tmap_bf16(&p.tk, a.K, pr.d, pr.nk, pr.BH) ||
+      !make_tmap_bf16(&p.tv, a.V, pr.v, pr.nk, pr.BH))
     return cudaErrorInvalidValue;
   p.n = pr.n;
   p.nk = pr.nk;
   p.off = pr.nk - pr.n;
+  p.dw = pr.d;
+  p.vw = pr.v;
   p.BH = pr.BH;
   p.n_qblocks = (pr.n + 2 * kBM - 1) / (2 * kBM);
   p.mask_kind = pr.mask_kind;
@@ -822,7 +835,9 @@ cudaError_t launch_tc_fwd_d(const FwdArgs& a, cudaStream_t s, int chunk_kt = 0, 
   p.chunk_kt = chunk_kt;
   p.splits = chunk_kt > 0 ? splits : 1;
   p.sched = a.status + kSchedWord;
-  if (chunk_kt == 0 && !make_tmap_bf16(&p.ty, a.Y, D, pr.n, pr.BH)) return cudaErrorInvalidValue;
+  if (chunk_kt == 0 && !make_tmap_bf16(&p.ty, a.Y, pr.v, pr.n, pr.BH)) return cudaErrorInvalidValue;
+  // The summaries are written with the kernel's width: only d = v = D there.
+  if (chunk_kt > 0 && (pr.d != D || pr.v != D)) return cudaErrorInvalidValue;
   p.pm = pm;
   p.pl = pl;
   p.pz = pz;
@@ -856,7 +871,7 @@ cudaError_t launch_tc_fwd_d(const FwdArgs& a, cudaStream_t s, int chunk_kt = 0, 
 }
 
 cudaError_t launch_tc_fwd(const FwdArgs& a, cudaStream_t s) {
-  return a.p.d == 128 ? launch_tc_fwd_d<128>(a, s) : launch_tc_fwd_d<64>(a, s);
+  return padded_width(a.p) == 128 ? launch_tc_fwd_d<128>(a, s) : launch_tc_fwd_d<64>(a, s);
 }
 
 cudaError_t launch_tc_fwd_chunks(const FwdArgs& a, int chunk_keys, int splits, float* pm,

@@ -94,14 +94,17 @@ typedef struct exattn_shape {
 
 /* Kernel path selection, process-wide (default EXATTN_PATH_AUTO).
  * AUTO uses the tcgen05/TMA/TMEM kernels where the shape allows (bf16 with
- * d = v in {64, 128}; for fp32 with d = v in {64, 128} and a positive scale
+ * d, v <= 128 and multiples of 8: widths other than 64 and 128 run on the
+ * width-64 or width-128 kernels, whose TMA loads fill the missing columns with
+ * zeros and whose stores leave them out; for fp32 with d = v in {64, 128} and a positive scale
  * the forward runs 3xTF32 on the tensor cores: each operand split into two
  * tf32 parts, three products per product, partial sums promoted to fp32 every
  * key block) and the SIMT fp32 kernels otherwise; its reverse pass is a
  * key-major dK/dV kernel plus a query-major dQ kernel.  SIMT forces the SIMT
  * kernels for every shape.  ATOMIC_DQ is AUTO with the other reverse form on
  * the tensor cores: one key-major kernel that adds dQ into an fp32 accumulator
- * with vector reductions (kept for measurement).  Returns the previous
+ * with vector reductions (kept for measurement; bf16 d = v in {64, 128} only,
+ * SIMT kernels otherwise).  Returns the previous
  * setting, or -1 for an unknown value (setting unchanged). */
 enum exattn_path { EXATTN_PATH_AUTO = 0, EXATTN_PATH_SIMT = 1, EXATTN_PATH_ATOMIC_DQ = 2 };
 int exattn_set_path(int path);

@@ -70,7 +70,7 @@ CASES = [
     (1, 2, 150, 1000, 64, 64, "bf16", "window", 300),
     (1, 1, 257, 520, 128, 128, "bf16", "bitmask", 0),
     (1, 2, 128, 384, 64, 64, "bf16", "causal", 0),       # whole tiles
-    (1, 1, 130, 77, 80, 96, "bf16", "window", 20),       # SIMT (odd widths)
+    (1, 1, 130, 77, 80, 96, "bf16", "window", 20),       # widths padded to 128
     (1, 2, 90, 301, 64, 64, "f32", "causal", 0),
     (1, 1, 250, 60, 48, 24, "f32", "bitmask", 0),
 ]

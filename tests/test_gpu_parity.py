@@ -79,6 +79,12 @@ SMALL = [
     (1, 2, 390, 64, 64, "bf16", "bitmask", 0),
     (1, 1, 257, 80, 96, "bf16", "bitmask", 0),
     (1, 1, 200, 16, 32, "bf16", "causal", 0),
+    # widths padded to the tensor-core kernels' 64 or 128 (zero-filled loads, clipped stores)
+    (1, 2, 300, 112, 72, "bf16", "window", 77),
+    (2, 1, 257, 48, 64, "bf16", "none", 0),
+    (1, 1, 190, 8, 8, "bf16", "causal", 0),
+    (1, 2, 260, 96, 40, "bf16", "causal", 0),     # Y's second box past its columns
+    (1, 1, 200, 40, 128, "bf16", "none", 0),      # Q, K boxes past their columns
     (1, 2, 300, 64, 64, "f32", "none", 0),
     (1, 2, 300, 64, 64, "f32", "causal", 0),
     (1, 1, 333, 80, 96, "f32", "window", 45),
