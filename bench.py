@@ -320,6 +320,49 @@ def kernel_roofline(args, w, which, achieved, peaks, peak_kind):
             "traffic": read_traffic(f"simt_{which}")}
 
 
+def host_link(stream, h_in, d_in, h_out, d_out, reps=3):
+    """The host link as the end-to-end step sees it, after its timed region: the
+    step's own input copies alone, its result copies alone, and both at once on
+    two streams, with the lower bound they put on a step that moves those bytes."""
+    side = torch.cuda.Stream()
+    bi = sum(t.numel() * t.element_size() for t in h_in)
+    bo = sum(t.numel() * t.element_size() for t in h_out)
+
+    def copy_in(s):
+        with torch.cuda.stream(s):
+            for dst, src in zip(d_in, h_in):
+                dst.copy_(src, non_blocking=True)
+
+    def copy_out(s):
+        with torch.cuda.stream(s):
+            for dst, src in zip(h_out, d_out):
+                dst.copy_(src, non_blocking=True)
+
+    def both(_s):
+        copy_in(stream)
+        copy_out(side)
+
+    def ms(fn):
+        fn(stream)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        side.wait_event(a)
+        for _ in range(reps):
+            fn(stream)
+        side_done = torch.cuda.Event()
+        side_done.record(side)
+        stream.wait_event(side_done)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    t_in, t_out, t_both = ms(copy_in), ms(copy_out), ms(both)
+    return {"h2d_gbs": bi / t_in / 1e6, "d2h_gbs": bo / t_out / 1e6,
+            "duplex_gbs": (bi + bo) / t_both / 1e6,
+            "copy_bound_ms": max(t_in, t_out, t_both)}
+
+
 def run_gpu(args, w):
     import exact_tiled_softmax_gb300 as ex
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -474,7 +517,8 @@ def run_gpu(args, w):
         e2e = {"value": whole_job_tflops(f_fwd + f_bwd, K, world, ms_e2e), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": ms_e2e / K,
-               "call": "attn_step_host" if host_step else "copies + attn_fwd + attn_bwd"}
+               "call": "attn_step_host" if host_step else "copies + attn_fwd + attn_bwd",
+               "link": host_link(stream, pin, (q, k, v, dy), outs, (y, L, dq, dk, dv))}
 
     clocks.__exit__(None, None, None)
     peaks, peak_kind = load_peaks()

@@ -223,8 +223,11 @@ struct KvLayout {
   static constexpr int EPI_OFF = VEC_OFF + NST * 1024;
   static constexpr int EPI = kBN * (D > V ? D : V) * 2;
   static constexpr int BAR_OFF = EPI_OFF + EPI;
-  static constexpr int B_KV = 0, B_QF = 1, B_QE = B_QF + NST, B_SDP = B_QE + NST, B_DS = B_SDP + 2,
-                       B_DONE = B_DS + 2, B_DRAIN = B_DONE + 1, B_KVFREE = B_DRAIN + 1,
+  // B_S, B_DP: S^T(i), dP^T(i) complete (MMA commits); B_P, B_DSB: P^T(i), dS^T(i)
+  // written to TMEM (elementwise arrivals).
+  static constexpr int B_KV = 0, B_QF = 1, B_QE = B_QF + NST, B_S = B_QE + NST, B_DP = B_S + 1,
+                       B_P = B_DP + 1, B_DSB = B_P + 1,
+                       B_DONE = B_DSB + 1, B_DRAIN = B_DONE + 1, B_KVFREE = B_DRAIN + 1,
                        B_ACCFREE = B_KVFREE + 1, B_ITEMF = B_ACCFREE + 1, B_ITEME = B_ITEMF + 2,
                        B_EPIFV = B_ITEME + 2, B_EPIV = B_EPIFV + 1, B_EPIFK = B_EPIV + 1,
                        B_EPIK = B_EPIFK + 1, NBAR = B_EPIK + 1;
@@ -295,9 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(Lay::B_QF + s), 1);
       mbar_init(bar(Lay::B_QE + s), 1);
     }
+    mbar_init(bar(Lay::B_S), 1);
+    mbar_init(bar(Lay::B_DP), 1);
+    mbar_init(bar(Lay::B_P), kEwWarps * 32);
+    mbar_init(bar(Lay::B_DSB), kEwWarps * 32);
     for (int h = 0; h < 2; ++h) {
-      mbar_init(bar(Lay::B_SDP + h), 1);
-      mbar_init(bar(Lay::B_DS + h), 8 * 32);
       mbar_init(bar(Lay::B_ITEMF + h), 1);
       mbar_init(bar(Lay::B_ITEME + h), 1 + kEwWarps);  // MMA warp + elementwise warps
     }
@@ -440,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kv_loads > 0) mbar_wait(bar(Lay::B_KV), (kv_loads - 1) & 1, abort_flag);
   } else if (warp == kWarpMMA) {
     const bool leader = elect_one();
-    constexpr uint32_t kIdHalf = idesc_bf16(kBN, 64, false, false);
+    constexpr uint32_t kIdS = idesc_bf16(kBN, kBM, false, false);
     constexpr uint32_t kIdDV = idesc_bf16(kBN, V, false, true);
     constexpr uint32_t kIdDK = idesc_bf16(kBN, D, false, true);
     const uint64_t dK0 = sdesc_sw128(sbase + Lay::K_OFF, 16, 1024);
@@ -449,45 +454,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dSm = sdesc_sw128(sbase + Lay::STAGE_OFF, 16384, 1024);  // MN-major view
     constexpr uint32_t kStage16 = Lay::STAGE >> 4, kQ16 = Lay::QBYTES >> 4;
     bool ok = true;
-    // Per query block i and half h: A_h(i) = dP^T_h, S^T_h (N = 64) and
-    // B_h(i) = dV, dK updates from that half (K = 64).  Issue order
-    //   A0(0) A1(0) | B0(0) A0(1) B1(0) A1(1) | B0(1) A0(2) B1(1) A1(2) | ...
-    // so that each half's chain A -> elementwise -> B -> A' never waits on the
-    // other half, whose MMAs fill the tensor pipe meanwhile.
-    auto issue_a = [&](int h, int slot) {
+    // Per query block i: S^T(i) = K Q_i^T and dP^T(i) = V dY_i^T over all 128
+    // queries (each product reads K or V from shared memory once), then
+    // dV += P^T(i) dY_i and dK += dS^T(i) Q_i.  Issue order
+    //   S(0) dP(0) | dV(0) S(1) dK(0) dP(1) | dV(1) S(2) dK(1) dP(2) | ...
+    // P^T(i) sits in S^T's columns and dS^T(i) in dP^T's.  The tensor pipe runs
+    // one thread's MMAs in issue order, so S(i+1) may follow dV(i), and dP(i+1)
+    // may follow dK(i), without a wait.  While the elementwise warps form
+    // dS(i), the pipe runs dV(i) and S(i+1); while they form P(i+1), it runs
+    // dK(i) and dP(i+1).
+    auto issue_s = [&](int slot) {
       const uint64_t q_k = dSt + slot * kStage16;
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_ss(tA, dK0 + off, q_k + off, kIdS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(Lay::B_S));
+      }
+    };
+    auto issue_dp = [&](int slot) {
       const uint64_t y_k = dSt + slot * kStage16 + kQ16;
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < V / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          mma_ss(tB + 64 * h, dV0 + off, y_k + off + h * 512, kIdHalf, kk > 0 ? 1u : 0u);
+          mma_ss(tB, dV0 + off, y_k + off, kIdS, kk > 0 ? 1u : 0u);
         }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          mma_ss(tA + 64 * h, dK0 + off, q_k + off + h * 512, kIdHalf, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(Lay::B_SDP + h));
+        tc_commit(bar(Lay::B_DP));
       }
     };
-    auto issue_b = [&](int h, int slot, bool first) {
-      const uint64_t q_m = dSm + slot * kStage16;
-      const uint64_t y_m = dSm + slot * kStage16 + kQ16;
+    // acc += X^T B over the block's 128 queries, 16 per MMA: X^T (P^T or dS^T)
+    // from TMEM, whose group g holds queries 32g..32g+31 as bf16 pairs in
+    // columns 32g..32g+15; B (dY or Q) from the stage in its MN-major view.
+    auto issue_acc = [&](uint32_t tacc, uint32_t tx, uint64_t b_m, uint32_t idesc, bool first) {
       if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t acol = 64 * h + 32 * (kk >> 1) + 8 * (kk & 1);
-          const uint32_t rows16 = (64 * h + 16 * kk) * 128 >> 4;
-          const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
-          mma_ts(tdV, tA + acol, y_m + rows16, kIdDV, acc);
-          mma_ts(tdK, tB + acol, q_m + rows16, kIdDK, acc);
+        for (int kk = 0; kk < kBM / 16; ++kk) {
+          const uint32_t acol = 32 * (kk >> 1) + 8 * (kk & 1);
+          const uint32_t rows16 = (16 * kk) * 128 >> 4;
+          mma_ts(tacc, tx + acol, b_m + rows16, idesc, (!first || kk > 0) ? 1u : 0u);
         }
       }
     };
-    // K and V are read by the A products only: once the item's last ones are
-    // issued, the commit lets the TMA warp load the next item's K and V while
-    // this item's last block is still in the elementwise warps and B products.
+    // K and V are read by the S^T and dP^T products only: once the item's last
+    // ones are issued, the commit lets the TMA warp load the next item's K and V
+    // while this item's last block is still in the elementwise warps and the
+    // dV, dK products.
     auto free_kv = [&]() {
       if (leader) tc_commit(bar(Lay::B_KVFREE));
     };
@@ -513,8 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (qb < qb_end) {
         if (!(ok = mbar_wait(bar(Lay::B_QF + it % NST), (it / NST) & 1, abort_flag))) break;
         tc_fence_after();
-        issue_a(0, it % NST);
-        issue_a(1, it % NST);
+        issue_s(it % NST);
+        issue_dp(it % NST);
       }
       if (qb_n >= qb_end) free_kv();
       while (qb < qb_end) {
@@ -522,25 +536,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool more = qb_n < qb_end;
         const int qb_nn = more ? next_qb(qb_n) : qb_end;
         const int slot_n = (it + 1) % NST, phase_n = ((it + 1) / NST) & 1;
-        if (!(ok = mbar_wait(bar(Lay::B_DS + 0), it & 1, abort_flag))) break;
+        const bool first = it == it0;
+        if (!(ok = mbar_wait(bar(Lay::B_P), it & 1, abort_flag))) break;
         tc_fence_after();
-        if (it == it0 && nitem > 0) {
+        if (first && nitem > 0) {
           // dV, dK restart from zero: the previous item's epilogue has read them.
           if (!(ok = mbar_wait(bar(Lay::B_ACCFREE), (nitem - 1) & 1, abort_flag))) break;
           tc_fence_after();
         }
-        issue_b(0, slot, it == it0);
+        issue_acc(tdV, tA, dSm + slot * kStage16 + kQ16, kIdDV, first);
         if (more) {
           if (!(ok = mbar_wait(bar(Lay::B_QF + slot_n), phase_n, abort_flag))) break;
           tc_fence_after();
-          issue_a(0, slot_n);
+          issue_s(slot_n);
         }
-        if (!(ok = mbar_wait(bar(Lay::B_DS + 1), it & 1, abort_flag))) break;
+        if (!(ok = mbar_wait(bar(Lay::B_DSB), it & 1, abort_flag))) break;
         tc_fence_after();
-        issue_b(1, slot, false);
+        issue_acc(tdK, tB, dSm + slot * kStage16, kIdDK, first);
         if (leader) tc_commit(bar(Lay::B_QE + slot));  // Q_i, dY_i no longer read
         if (more) {
-          issue_a(1, slot_n);
+          issue_dp(slot_n);
           if (qb_nn >= qb_end) free_kv();
         }
         qb = qb_n;
@@ -564,8 +579,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(bar(Lay::B_DRAIN), 0, abort_flag);
   } else {
     // Elementwise: thread = key row r of the block; group g covers queries
-    // 32g..32g+31 (half h = g / 2).
-    const int g = warp >> 2, wl = warp & 3, h = g >> 1;
+    // 32g..32g+31.  Per query block two phases: P^T from S^T (then dV may
+    // start), and dS^T from dP^T and the P values kept in registers.
+    const int g = warp >> 2, wl = warp & 3;
     const int r = wl * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wl * 32) << 16;
     const float sl2 = p.sl2;
@@ -590,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t keep = 0xFFFFFFFFu;
         if constexpr (kDrop)
           keep = transpose_bits32(keep_word32(p, bh, qb * kBM + 32 * g + lane, k0 + wl * 32), lane);
-        if (!(ok = mbar_wait(bar(Lay::B_SDP + h), it & 1, abort_flag))) break;
+        if (!(ok = mbar_wait(bar(Lay::B_S), it & 1, abort_flag))) break;
         tc_fence_after();
         const float* dvec = reinterpret_cast<const float*>(smem + Lay::VEC_OFF + slot * 1024);
         const float* lvec = dvec + 128;
@@ -616,66 +632,91 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        uint32_t sv[2][16], dpv[2][16];
+        float pp[32];  // p_ij of the thread's 32 queries (masked: 0), for dS
+        {
+          uint32_t sv[2][16];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          tmem_ld16(tA + lane_off + cb + 16 * c, sv[c]);
-          tmem_ld16(tB + lane_off + cb + 16 * c, dpv[c]);
-        }
-        tmem_ld_wait();
+          for (int c = 0; c < 2; ++c) tmem_ld16(tA + lane_off + cb + 16 * c, sv[c]);
+          tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          reg_fence(sv[c]);
-          reg_fence(dpv[c]);
-        }
+          for (int c = 0; c < 2; ++c) reg_fence(sv[c]);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {  // two chunks of 16 queries
-          const uint32_t (&s)[16] = sv[c];
-          const uint32_t (&dp)[16] = dpv[c];
-          uint32_t pk[8], dk[8];
+          for (int c = 0; c < 2; ++c) {  // two chunks of 16 queries
+            uint32_t pk[8];
 #pragma unroll
-          for (int e = 0; e < 16; e += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lvec + cb + 16 * c + e);
-            const float4 d4 = *reinterpret_cast<const float4*>(dvec + cb + 16 * c + e);
-            const float la[4] = {l4.x, l4.y, l4.z, l4.w};
-            const float da[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], gv[4];
+            for (int e = 0; e < 16; e += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(lvec + cb + 16 * c + e);
+              const float la[4] = {l4.x, l4.y, l4.z, l4.w};
+              float pv[4];
 #pragma unroll
-            for (int u = 0; u < 4; u += 2) {  // query pairs: packed fp32 arithmetic
-              float x0, x1;
-              ffma2(x0, x1, __uint_as_float(s[e + u]), __uint_as_float(s[e + u + 1]), sl2, sl2,
-                    -la[u], -la[u + 1]);
-              float pp[2] = {ex2(x0), ex2(x1)};
-#pragma unroll
-              for (int w = 0; w < 2; ++w)
-                if (!((allow >> (16 * c + e + u + w)) & 1u)) pp[w] = 0.f;
-              float dq0 = __uint_as_float(dp[e + u]), dq1 = __uint_as_float(dp[e + u + 1]);
-              if constexpr (kDrop) {
-                // Replayed mask: dV takes p xi s; dP = xi s (G_i . V_j).
-                const float xs0 = ((keep >> (16 * c + e + u)) & 1u) ? p.drop_scale : 0.f;
-                const float xs1 = ((keep >> (16 * c + e + u + 1)) & 1u) ? p.drop_scale : 0.f;
-                fmul2(dq0, dq1, dq0, dq1, xs0, xs1);
-                fmul2(pv[u], pv[u + 1], pp[0], pp[1], xs0, xs1);
-              } else {
-                pv[u] = pp[0];
-                pv[u + 1] = pp[1];
+              for (int u = 0; u < 4; u += 2) {  // query pairs: packed fp32 arithmetic
+                const int q = 16 * c + e + u;
+                float x0, x1;
+                ffma2(x0, x1, __uint_as_float(sv[c][e + u]), __uint_as_float(sv[c][e + u + 1]),
+                      sl2, sl2, -la[u], -la[u + 1]);
+                pp[q] = ((allow >> q) & 1u) ? ex2(x0) : 0.f;
+                pp[q + 1] = ((allow >> (q + 1)) & 1u) ? ex2(x1) : 0.f;
+                if constexpr (kDrop) {
+                  // Replayed mask: dV takes p xi s.
+                  const float xs0 = ((keep >> q) & 1u) ? p.drop_scale : 0.f;
+                  const float xs1 = ((keep >> (q + 1)) & 1u) ? p.drop_scale : 0.f;
+                  fmul2(pv[u], pv[u + 1], pp[q], pp[q + 1], xs0, xs1);
+                } else {
+                  pv[u] = pp[q];
+                  pv[u + 1] = pp[q + 1];
+                }
               }
-              float t0, t1;
-              fadd2(t0, t1, dq0, dq1, -da[u], -da[u + 1]);
-              fmul2(gv[u], gv[u + 1], pp[0], pp[1], t0, t1);
+              pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
+              pk[e / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
             }
-            pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
-            pk[e / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-            dk[e / 2] = pack_bf16x2(gv[0], gv[1]);
-            dk[e / 2 + 1] = pack_bf16x2(gv[2], gv[3]);
+            // P^T (bf16 pairs) over the first 16 columns of this group's range.
+            tmem_st8(tA + lane_off + cb + 8 * c, pk);
           }
-          // P^T / dS^T (bf16 pairs) over the first 16 columns of this group's range.
-          tmem_st8(tA + lane_off + cb + 8 * c, pk);
-          tmem_st8(tB + lane_off + cb + 8 * c, dk);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(Lay::B_P));
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(Lay::B_DS + h));
+        if (!(ok = mbar_wait(bar(Lay::B_DP), it & 1, abort_flag))) break;
+        tc_fence_after();
+        {
+          uint32_t dpv[2][16];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) tmem_ld16(tB + lane_off + cb + 16 * c, dpv[c]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) reg_fence(dpv[c]);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t dk[8];
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+              const float4 d4 = *reinterpret_cast<const float4*>(dvec + cb + 16 * c + e);
+              const float da[4] = {d4.x, d4.y, d4.z, d4.w};
+              float gv[4];
+#pragma unroll
+              for (int u = 0; u < 4; u += 2) {
+                const int q = 16 * c + e + u;
+                float dq0 = __uint_as_float(dpv[c][e + u]), dq1 = __uint_as_float(dpv[c][e + u + 1]);
+                if constexpr (kDrop) {
+                  // Replayed mask: dP = xi s (G_i . V_j).
+                  const float xs0 = ((keep >> q) & 1u) ? p.drop_scale : 0.f;
+                  const float xs1 = ((keep >> (q + 1)) & 1u) ? p.drop_scale : 0.f;
+                  fmul2(dq0, dq1, dq0, dq1, xs0, xs1);
+                }
+                float t0, t1;
+                fadd2(t0, t1, dq0, dq1, -da[u], -da[u + 1]);
+                fmul2(gv[u], gv[u + 1], pp[q], pp[q + 1], t0, t1);
+              }
+              dk[e / 2] = pack_bf16x2(gv[0], gv[1]);
+              dk[e / 2 + 1] = pack_bf16x2(gv[2], gv[3]);
+            }
+            // dS^T (bf16 pairs) over the first 16 columns of this group's range.
+            tmem_st8(tB + lane_off + cb + 8 * c, dk);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(Lay::B_DSB));
+        }
         ++it;
       }
       if (!ok) break;
