@@ -19,9 +19,10 @@
 // shared-memory tiles and TMA stores.
 // tc_bwd_kv_kernel -- item = a 128-key block; loop over query blocks.
 //   TMEM: A [0,128) S^T then P^T (bf16), B [128,256) dP^T then dS^T (bf16),
-//   dV [256, 256+V), dK [256+V, 256+V+D).  S^T and dP^T are computed in two
-//   64-query halves so that the elementwise work of one half overlaps the MMAs
-//   of the other; dV and dK then take each half as a K = 64 contraction.
+//   dV [256, 256+V), dK [256+V, 256+V+D).  S^T and dP^T cover the block's 128
+//   queries (K and V are read once per block); the issue order
+//   S(0) dP(0) | dV(0) S(1) dK(0) dP(1) | ... relies on the in-order tensor
+//   pipe, so the MMAs of one block overlap the elementwise work of the next.
 // tc_bwd_q_kernel -- item = a 128-query block; loop over key blocks.
 //   K and V in separate rings (3 + 1 slots for d = 128): V(t) is read only by
 //   dP(t), K(t) until dQ(t).
