@@ -512,17 +512,21 @@ def run_gpu(args, w):
         for _ in range(max(1, args.warmup)):
             e2e_step()
         barrier()
-        s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s3.record(stream)
-        for _ in range(K):
+        # One event per step boundary on the call's stream (the call joins its
+        # internal streams back to it), so the spread of the steps shows too.
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+        marks[0].record(stream)
+        for j in range(K):
             e2e_step()
-        e3.record(stream)
+            marks[j + 1].record(stream)
         barrier()
-        ms_e2e = rank_max(s3.elapsed_time(e3))
+        ms_e2e = rank_max(marks[0].elapsed_time(marks[K]))
+        steps_ms = sorted(marks[j].elapsed_time(marks[j + 1]) for j in range(K))
         e2e = {"value": whole_job_tflops(f_fwd + f_bwd, K, world, ms_e2e), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": ms_e2e / K,
                "call": "attn_step_host" if host_step else "copies + attn_fwd + attn_bwd",
+               "step_ms": {"min": steps_ms[0], "median": steps_ms[K // 2], "max": steps_ms[-1]},
                "link": host_link(stream, pin, (q, k, v, dy), outs, (y, L, dq, dk, dv))}
 
     clocks.__exit__(None, None, None)
