@@ -24,19 +24,20 @@ def ex():
 
 
 CASES = [
-    # (B, H, n, d, dtype, mask, window)
-    (2, 8, 300, 128, "bf16", "causal", 0),    # 16 slices: 4 chunks of 4
-    (1, 3, 200, 64, "bf16", "none", 0),       # 3 slices: one chunk
-    (2, 41, 136, 64, "bf16", "window", 50),   # 82 slices: 8 chunks, the last one short
-    (1, 9, 130, 64, "f32", "bitmask", 0),     # fp32, bitmask copied from the host
-    (1, 4, 1000, 128, "bf16", "causal", 0),
+    # (B, H, n, d, v, dtype, mask, window)
+    (2, 8, 300, 128, 128, "bf16", "causal", 0),    # 16 slices: 4 chunks of 4
+    (1, 3, 200, 64, 64, "bf16", "none", 0),        # 3 slices: one chunk
+    (2, 41, 136, 64, 64, "bf16", "window", 50),    # 82 slices: 8 chunks, the last one short
+    (1, 9, 130, 64, 64, "f32", "bitmask", 0),      # fp32, bitmask copied from the host
+    (1, 4, 1000, 128, 128, "bf16", "causal", 0),
+    (1, 6, 260, 80, 96, "bf16", "causal", 0),      # widths padded to the 128-wide kernels
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
 def test_host_step_matches_the_device_calls(ex, case):
-    B, H, n, d, dtype, mask, window = case
-    w = workloads.small(B, H, n, d, d, dtype, mask, 1 / math.sqrt(d), seed=CASES.index(case) + 5)
+    B, H, n, d, vw, dtype, mask, window = case
+    w = workloads.small(B, H, n, d, vw, dtype, mask, 1 / math.sqrt(d), seed=CASES.index(case) + 5)
     x = workloads.make_inputs(w)
     dev = torch.device("cuda:0")
     bm = None

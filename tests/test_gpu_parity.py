@@ -85,6 +85,8 @@ SMALL = [
     (1, 1, 190, 8, 8, "bf16", "causal", 0),
     (1, 2, 260, 96, 40, "bf16", "causal", 0),     # Y's second box past its columns
     (1, 1, 200, 40, 128, "bf16", "none", 0),      # Q, K boxes past their columns
+    (1, 1, 300, 128, 8, "bf16", "window", 64),    # one 8-column box of V, Y, dY, dV
+    (1, 2, 150, 8, 120, "bf16", "none", 0),       # one 8-column box of Q, K, dQ, dK
     (1, 2, 300, 64, 64, "f32", "none", 0),
     (1, 2, 300, 64, 64, "f32", "causal", 0),
     (1, 1, 333, 80, 96, "f32", "window", 45),
