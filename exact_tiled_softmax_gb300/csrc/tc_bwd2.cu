@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++kv_loads;
       // The next item's K and V go into L2 after this item's first stage load,
-      // so that their load (issued once this item's last A products are done)
+      // so that their load (issued once this item's last S^T, dP^T products are done)
       // does not wait on HBM.
       int t_next = -1;
       auto prefetch_next = [&]() {
@@ -607,8 +607,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t keep = 0xFFFFFFFFu;
         if constexpr (kDrop)
           keep = transpose_bits32(keep_word32(p, bh, qb * kBM + 32 * g + lane, k0 + wl * 32), lane);
-        if (!(ok = mbar_wait(bar(Lay::B_S), it & 1, abort_flag))) break;
-        tc_fence_after();
         const float* dvec = reinterpret_cast<const float*>(smem + Lay::VEC_OFF + slot * 1024);
         const float* lvec = dvec + 128;
         const int q0 = qb * kBM;
@@ -633,6 +631,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        // The mask bits above need no product: they are formed before the wait.
+        if (!(ok = mbar_wait(bar(Lay::B_S), it & 1, abort_flag))) break;
+        tc_fence_after();
         float pp[32];  // p_ij of the thread's 32 queries (masked: 0), for dS
         {
           uint32_t sv[2][16];
