@@ -835,7 +835,7 @@ struct QLayout {
   static constexpr int PART_OFF = EPI_OFF + kBM * D * 2;
   static constexpr int BAR_OFF = PART_OFF + 4 * kBM * 4;
   static constexpr int B_Q = 0, B_QFREE = 1, B_KVF = 2, B_KVE = B_KVF + NS, B_SDP = B_KVE + NS,
-                       B_DS = B_SDP + 1, B_SFREE = B_DS + 1, B_DONE = B_SFREE + 1,
+                       B_DS = B_SDP + 1, B_SFREE = B_DS + 2, B_DONE = B_SFREE + 1,
                        B_DREAD = B_DONE + 1, B_ITEMF = B_DREAD + 1, B_ITEME = B_ITEMF + 2,
                        B_EPIF = B_ITEME + 2, B_EPI = B_EPIF + 1, B_DPART = B_EPI + 1,
                        B_DRAIN = B_DPART + 1, NBAR = B_DRAIN + 1;
@@ -895,7 +895,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(Lay::B_KVE + s), 1);
     }
     mbar_init(bar(Lay::B_SDP), 1);
-    mbar_init(bar(Lay::B_DS), kEwWarps * 32);
+    // dS(t) written: one barrier per block parity.  dS(t + 2) needs S(t + 2),
+    // which the MMA warp issues only after its wait for dS(t), so neither
+    // barrier ever runs a phase ahead of that wait; with one barrier the
+    // elementwise warps could complete dS(t) and dS(t + 1) before it.
+    mbar_init(bar(Lay::B_DS + 0), kEwWarps * 32);
+    mbar_init(bar(Lay::B_DS + 1), kEwWarps * 32);
     mbar_init(bar(Lay::B_SFREE), kEwWarps * 32);
     mbar_init(bar(Lay::B_DONE), 1);
     mbar_init(bar(Lay::B_DREAD), kEwWarps * 32);  // the epilogue has read dQ
@@ -1145,7 +1150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_s(t + 1);
           if (kb_nn >= kb_end && !(ok = free_q())) break;
         }
-        if (!(ok = mbar_wait(bar(Lay::B_DS), t & 1, abort_flag))) break;
+        if (!(ok = mbar_wait(bar(Lay::B_DS + (t & 1)), (t >> 1) & 1, abort_flag))) break;
         tc_fence_after();
         // dQ += dS(t) K_t  (A = dS bf16 in TMEM over dP(t), keys packed; B = K_t MN-major)
         const int ks = t % Lay::NK;
@@ -1214,6 +1219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = qb * kBM;
       const int i = q0 + r;
       const size_t vo = static_cast<size_t>(bh) * p.npad + q0 + r;
+      // A row whose L is -inf had an empty allowed set: p = 0 below, and the
+      // status word says so.
+      if (g == 0 && i < n && Li == -INFINITY) raise_status(p.status, kStatusEmptyRow);
       // delta_i = dY_i . Y_i ("Exact tiled softmax attention ...", Reverse
       // procedure) and L_i log2(e) for this query block: group g sums columns
       // V/4 g .. of dY (from the staged tile) times Y, the four partial sums
@@ -1324,7 +1332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(Lay::B_DS));
+        mbar_arrive(bar(Lay::B_DS + (t & 1)));
         ++t;
       }
       if (!ok) break;
