@@ -25,6 +25,7 @@ Modules:
 Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
 reference arm of ``bench.py`` may import this package.  It shares no code with
 the CUDA path and never imports it.  Every function here is pinned by the CPU
-tests in ``tests/test_oracle.py``; none is "parity unpinned".
+tests in ``tests/test_oracle.py`` (directly, or as a step of a pinned
+procedure); none is "parity unpinned".
 """
 from . import dense, masks, philox, tiled  # noqa: F401

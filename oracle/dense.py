@@ -52,15 +52,6 @@ def head_forward(Q, K, V, c, allowed):
     return Y, L
 
 
-def head_probabilities(Q, K, c, allowed):
-    """One head: the full probability matrix P [n,n] (small cases only)."""
-    _check_rows(allowed)
-    s = np.where(allowed, c * (Q @ K.T), -np.inf)
-    m = s.max(axis=1)
-    e = np.exp(s - m[:, None])
-    return e / e.sum(axis=1)[:, None]
-
-
 def head_backward(Q, K, V, G, c, allowed):
     """One head. Returns (dQ, dK, dV, delta) for the upstream G [n,v]."""
     _check_rows(allowed)

@@ -26,8 +26,6 @@ merge).
 """
 import numpy as np
 
-from .masks import allowed_matrix
-
 
 def key_blocks(n, b):
     """The key blocks J_t as (start, stop) pairs, the last one possibly shorter."""
@@ -125,8 +123,3 @@ def recompute_backward(Q, K, V, G, Y, m, l, c, allowed, b):
         dK[j0:j1] += c * (gamma.T @ Q)
         dV[j0:j1] += p.T @ G
     return dQ, dK, dV, delta
-
-
-def head_allowed(n, mask_kind, window=0, bitmask=None):
-    """Convenience re-export of the mask reading used by these procedures."""
-    return allowed_matrix(n, mask_kind, window, bitmask)
