@@ -17,6 +17,7 @@ import torch
 __all__ = ["fwd", "bwd", "fwd_workspace_size", "bwd_workspace_size", "device_status",
            "set_path", "library_path", "load_library", "ExattnError", "Shape",
            "record_kernel_events", "launch_count", "workspace", "bwd_noalloc",
+           "noalloc_device_status",
            "fwd_splitkv", "QKShape",
            "MASK_NONE", "MASK_CAUSAL", "MASK_WINDOW", "MASK_BITMASK"]
 
@@ -101,6 +102,8 @@ def load_library():
     lib.exattn_launch_count.restype = ctypes.c_ulonglong
     lib.attn_bwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, cf, ci, ci, vp, vp, vp, vp, vp]
     lib.attn_bwd_noalloc.restype = ci
+    lib.exattn_noalloc_device_status.argtypes = [vp]
+    lib.exattn_noalloc_device_status.restype = ci
     lib.exattn_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint, vp]
     lib.exattn_selftest_wait_timeout.restype = ci
     qp = ctypes.POINTER(QKShape)
@@ -159,6 +162,30 @@ def _check(ts, dtype, device):
             raise ValueError("tensors must be contiguous and on the same CUDA device")
         if dtype is not None and t.dtype != dtype:
             raise ValueError(f"dtype mismatch: {t.dtype} vs {dtype}")
+
+
+def _check_shapes(q, k, v, y=None, dy=None, L=None, dq=None, dk=None, dv=None, same_n=False):
+    """Shapes agree with q [B,H,nq,d], k [B,H,nk,d], v [B,H,nk,v]: Y and dY are
+    [B,H,nq,v], L fp32 [B,H,nq], dQ/dK/dV like Q/K/V.  Raises ValueError before
+    anything reaches the library, which trusts the sizes it is given."""
+    for name, t, nd in (("q", q, 4), ("k", k, 4), ("v", v, 4), ("y", y, 4), ("dy", dy, 4),
+                        ("L", L, 3), ("dq", dq, 4), ("dk", dk, 4), ("dv", dv, 4)):
+        if t is not None and t.dim() != nd:
+            raise ValueError(f"{name} must have {nd} dimensions, got shape {tuple(t.shape)}")
+    B, H, nq, d = q.shape
+    nk, vw = k.shape[2], v.shape[3]
+    want = {"k": (B, H, nk, d), "v": (B, H, nk, vw), "y": (B, H, nq, vw),
+            "dy": (B, H, nq, vw), "L": (B, H, nq), "dq": (B, H, nq, d), "dk": (B, H, nk, d),
+            "dv": (B, H, nk, vw)}
+    for name, t in (("k", k), ("v", v), ("y", y), ("dy", dy), ("L", L), ("dq", dq),
+                    ("dk", dk), ("dv", dv)):
+        if t is not None and tuple(t.shape) != want[name]:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {want[name]}")
+    if same_n and nk != nq:
+        raise ValueError(f"k and v must have q's sequence length {nq}, got {nk}")
+    if L is not None:
+        if L.dtype != torch.float32 or not L.is_contiguous() or L.device != q.device:
+            raise ValueError("L must be a contiguous float32 tensor on q's device")
 
 
 def _stream(stream):
@@ -220,7 +247,8 @@ def fwd(q, k, v, scale, mask="none", window=0, bitmask=None, y=None, L=None, ws=
     the keys).  ``dropout_p`` > 0 drops probabilities with the replayable mask of
     ``seed``; the reverse pass must get the same two values."""
     lib = load_library()
-    _check((k, v, y), q.dtype, q.device)
+    _check((q, k, v, y), q.dtype, q.device)
+    _check_shapes(q, k, v, y=y, L=L)
     kind = _mask_kind(mask)
     if k.shape[2] != q.shape[2]:
         return _fwd_qk(lib, q, k, v, scale, kind, window, bitmask, y, L, ws, stream, dropout_p,
@@ -251,7 +279,8 @@ def bwd(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, dq=None, 
     """Reverse pass -> (dQ, dK, dV) for the upstream gradient dy (with the forward
     pass's ``dropout_p`` and ``seed`` when it used dropout)."""
     lib = load_library()
-    _check((k, v, y, dy, dq, dk, dv), q.dtype, q.device)
+    _check((q, k, v, y, dy, dq, dk, dv), q.dtype, q.device)
+    _check_shapes(q, k, v, y=y, dy=dy, L=L, dq=dq, dk=dk, dv=dv)
     kind = _mask_kind(mask)
     if k.shape[2] != q.shape[2]:
         return _bwd_qk(lib, q, k, v, y, dy, L, scale, kind, window, bitmask, dq, dk, dv, ws,
@@ -285,7 +314,8 @@ def fwd_splitkv(q, k, v, scale, mask="none", window=0, bitmask=None, num_splits=
     lib = load_library()
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("expected [batch, heads, n, width] tensors")
-    _check((k, v, y), q.dtype, q.device)
+    _check((q, k, v, y), q.dtype, q.device)
+    _check_shapes(q, k, v, y=y, L=L)
     B, H, nq, d = q.shape
     shape = QKShape(B, H, nq, k.shape[2], d, v.shape[-1], _DTYPES[q.dtype])
     kind = _mask_kind(mask)
@@ -305,12 +335,16 @@ def fwd_splitkv(q, k, v, scale, mask="none", window=0, bitmask=None, num_splits=
 
 
 def bwd_noalloc(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, dq=None,
-                dk=None, dv=None, stream=None):
+                dk=None, dv=None, stream=None, check_status=False):
     """Reverse pass through attn_bwd_noalloc: no workspace is passed or allocated;
-    the library's own 64 MiB scratch array is used instead."""
+    the library's own 64 MiB scratch array is used instead.  With
+    ``check_status`` the call then synchronises the stream and raises
+    ExattnError if the kernels recorded a condition (an empty allowed set or a
+    bounded wait that gave up) in the scratch array's status word."""
     lib = load_library()
+    _check((q, k, v, y, dy, dq, dk, dv), q.dtype, q.device)
+    _check_shapes(q, k, v, y=y, dy=dy, L=L, dq=dq, dk=dk, dv=dv, same_n=True)
     shape = _shape(q, v)
-    _check((k, v, y, dy, dq, dk, dv), q.dtype, q.device)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -319,7 +353,17 @@ def bwd_noalloc(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, d
                               _ptr(bitmask), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream))
     if st != 0:
         raise ExattnError(st, "attn_bwd_noalloc")
+    if check_status:
+        st = noalloc_device_status(stream)
+        if st != 0:
+            raise ExattnError(st, "attn_bwd_noalloc (device status)")
     return dq, dk, dv
+
+
+def noalloc_device_status(stream=None) -> int:
+    """exattn_noalloc_device_status: synchronise the stream, then read the status
+    word that the last attn_bwd_noalloc call left in the library's scratch array."""
+    return load_library().exattn_noalloc_device_status(_stream(stream))
 
 
 KERNEL_FWD, KERNEL_DELTA, KERNEL_BWD, KERNEL_DQ_CONVERT, KERNEL_BWD_Q = 0, 1, 2, 3, 4
@@ -341,6 +385,7 @@ def step_host(q, k, v, dy, scale, mask="none", window=0, bitmask=None, out=None,
             raise ValueError("step_host takes contiguous CPU tensors of one dtype")
     if bitmask is not None and bitmask.device.type != "cpu":
         raise ValueError("step_host takes the bitmask on the CPU")
+    _check_shapes(q, k, v, dy=dy, same_n=True)
     kind = _mask_kind(mask)
     shape = _shape(q, v)
     if out is None:

@@ -16,7 +16,9 @@
 // first call should come before any stream capture.  Every call shares the
 // array: attn_bwd clears the status word and the dQ accumulator itself on each
 // call, and calls whose work overlaps on the GPU (for example on two streams)
-// race on the array and must not be issued.
+// race on the array and must not be issued.  The kernels' status word (an
+// empty allowed set, a bounded wait that gave up) is word 0 of the array;
+// exattn_noalloc_device_status reads it back.
 #include <atomic>
 
 #include "../../include/exattn.h"
@@ -74,4 +76,26 @@ extern "C" int attn_bwd_noalloc(const exattn_shape* shape, const void* Q, const 
   if (!scratch) return EXATTN_CUDA_ERROR;
   return attn_bwd(shape, Q, K, V, Y, dY, L, scale, mask_kind, window, bitmask, dQ, dK, dV,
                   scratch, kScratchBytes, cuda_stream);
+}
+
+extern "C" int exattn_noalloc_device_status(void* cuda_stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    exattn::record_error("exattn_noalloc_device_status: cudaStreamSynchronize",
+                         static_cast<int>(e), cudaGetErrorString(e));
+    return EXATTN_CUDA_ERROR;
+  }
+  void* scratch = scratch_on_current_device();
+  if (!scratch) return EXATTN_CUDA_ERROR;
+  unsigned word = 0;
+  e = cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) {
+    exattn::record_error("exattn_noalloc_device_status: cudaMemcpy", static_cast<int>(e),
+                         cudaGetErrorString(e));
+    return EXATTN_CUDA_ERROR;
+  }
+  if (word & 2u) return EXATTN_TIMEOUT;
+  if (word & 1u) return EXATTN_EMPTY_ROW;
+  return EXATTN_OK;
 }

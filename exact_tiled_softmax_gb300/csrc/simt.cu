@@ -303,6 +303,7 @@ struct DeltaArgs {
   float* lse2;
   int n, npad, v;
   size_t rows;  // BH * npad
+  unsigned* status;  // EMPTY_ROW when a row's L is -inf (its allowed set was empty)
 };
 
 __device__ __forceinline__ void delta_store(const DeltaArgs& a, size_t row, float acc) {
@@ -312,6 +313,7 @@ __device__ __forceinline__ void delta_store(const DeltaArgs& a, size_t row, floa
     const float L = a.L[bh * a.n + i];
     a.delta[row] = acc;
     a.lse2[row] = L == -INFINITY ? INFINITY : L * kLog2e;
+    if (L == -INFINITY) raise_status(a.status, kStatusEmptyRow);
   } else {
     a.delta[row] = 0.f;
     a.lse2[row] = INFINITY;
@@ -366,6 +368,7 @@ __global__ void __launch_bounds__(256, 4) delta_vec_kernel(DeltaArgs a) {
       if (r0 + u < a.rows && lane == u % G) {
         a.delta[r0 + u] = live[u] ? acc : 0.f;
         a.lse2[r0 + u] = live[u] && Lr[u] != -INFINITY ? Lr[u] * kLog2e : INFINITY;
+        if (live[u] && Lr[u] == -INFINITY) raise_status(a.status, kStatusEmptyRow);
       }
     }
   }
@@ -454,7 +457,8 @@ cudaError_t bwd_dispatch(const BwdArgs& a, cudaStream_t s) {
 template <typename T>
 cudaError_t delta_dispatch(const BwdArgs& a, cudaStream_t s) {
   const Problem& p = a.p;
-  DeltaArgs d{a.Y, a.dY, a.L, a.delta, a.lse2, p.n, a.npad, p.v, (size_t)p.BH * a.npad};
+  DeltaArgs d{a.Y, a.dY, a.L, a.delta, a.lse2, p.n, a.npad, p.v, (size_t)p.BH * a.npad,
+              a.status};
   constexpr int E = 16 / sizeof(T);
   const int vecs = p.v / E;
   before_launch(kKernDelta, s);

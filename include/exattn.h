@@ -130,7 +130,9 @@ int attn_fwd(const exattn_shape* shape, const void* Q, const void* K, const void
 
 /* Reverse pass for the upstream gradient dY (= G): writes dQ, dK (dtype,
  * [B][H][n][d]) and dV (dtype, [B][H][n][v]).  Y and L must come from attn_fwd
- * with the same Q, K, V, scale and mask.  `workspace` is a device buffer of at
+ * with the same Q, K, V, scale and mask.  A row whose L_i is -inf (its allowed
+ * set was empty) contributes nothing, gets dQ_i = 0, and the status word of the
+ * workspace records EXATTN_EMPTY_ROW.  `workspace` is a device buffer of at
  * least exattn_bwd_workspace_size bytes, 256-byte aligned.  Returns an
  * exattn_status. */
 int attn_bwd(const exattn_shape* shape, const void* Q, const void* K, const void* V,
@@ -190,12 +192,23 @@ int attn_bwd_dropout(const exattn_shape* shape, const void* Q, const void* K, co
  * address with that device current; make that first call before any stream
  * capture.  All calls share the one array (each call clears what must start at
  * zero): calls whose work overlaps on the GPU, for example on two streams,
- * race and must not be issued.  The device status word lives in the array; it
- * is not readable through exattn_device_status.  Returns an exattn_status. */
+ * race and must not be issued.  The device status word lives in the array;
+ * read it with exattn_noalloc_device_status (not exattn_device_status).
+ * Returns an exattn_status. */
 int attn_bwd_noalloc(const exattn_shape* shape, const void* Q, const void* K, const void* V,
                      const void* Y, const void* dY, const float* L, float scale, int mask_kind,
                      int window, const uint32_t* bitmask, void* dQ, void* dK, void* dV,
                      void* cuda_stream);
+
+/* The device status word of the last attn_bwd_noalloc call on the current
+ * device, which that call's kernels write into the library's scratch array
+ * (no counterpart in the pages either).  Synchronises `cuda_stream` first (the
+ * stream of that call), then reads the word.  Returns EXATTN_OK,
+ * EXATTN_EMPTY_ROW (some allowed-key set was empty), EXATTN_TIMEOUT (a bounded
+ * device wait gave up: the gradients are not valid) or EXATTN_CUDA_ERROR.  The
+ * word is shared by every attn_bwd_noalloc call on the device and is cleared
+ * at the start of each, so read it before the next call is queued. */
+int exattn_noalloc_device_status(void* cuda_stream);
 
 /* ---------------------------------------------------------------------------
  * Split-KV forward: a few queries against a long key sequence (a decode step).

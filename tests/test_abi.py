@@ -188,3 +188,36 @@ def test_splitkv_host_side_argument_checks(lib):
     assert call(_qk(), q=vp((1 << 20) + 8)) == 3
     assert call(_qk(), ws_ptr=vp((1 << 21) + 64)) == 3
     assert call(_qk(), ws_bytes=100) == 4
+
+
+@pytest.mark.parametrize("bad", ["k_len", "k_heads", "k_width", "v_len", "y", "dy", "L", "L_dtype",
+                                 "dq"])
+def test_binding_rejects_mismatched_shapes_before_any_launch(lib, bad):
+    """The library trusts the sizes in its shape argument, so the Python binding
+    checks every tensor against q, k and v first.  CPU tensors: a ValueError
+    here means nothing reached the library (which would need device memory)."""
+    import torch
+    import exact_tiled_softmax_gb300 as ex
+    B, H, n, d = 1, 2, 32, 64
+    bf = torch.bfloat16
+    t = dict(q=torch.zeros(B, H, n, d, dtype=bf), k=torch.zeros(B, H, n, d, dtype=bf),
+             v=torch.zeros(B, H, n, d, dtype=bf), y=torch.zeros(B, H, n, d, dtype=bf),
+             dy=torch.zeros(B, H, n, d, dtype=bf), L=torch.zeros(B, H, n),
+             dq=torch.zeros(B, H, n, d, dtype=bf))
+    change = {"k_len": ("k", (B, H, n + 8, d)), "k_heads": ("k", (B, H + 1, n, d)),
+              "k_width": ("k", (B, H, n, d + 8)), "v_len": ("v", (B, H, n + 8, d)),
+              "y": ("y", (B, H, n, d + 8)), "dy": ("dy", (B, H, n - 1, d)),
+              "L": ("L", (B, H, n + 1)), "dq": ("dq", (B, H, n, d - 8))}
+    if bad == "L_dtype":
+        t["L"] = torch.zeros(B, H, n, dtype=torch.float64)
+    else:
+        name, shape = change[bad]
+        t[name] = torch.zeros(shape, dtype=torch.float32 if name == "L" else bf)
+    count = lib.exattn_launch_count()
+    with pytest.raises(ValueError):
+        ex.bwd_noalloc(t["q"], t["k"], t["v"], t["y"], t["dy"], t["L"], 0.1, "causal",
+                       dq=t["dq"])
+    if bad not in ("k_len", "v_len"):  # a different key length is cross-attention for bwd
+        with pytest.raises(ValueError):
+            ex.bwd(t["q"], t["k"], t["v"], t["y"], t["dy"], t["L"], 0.1, "causal", dq=t["dq"])
+    assert lib.exattn_launch_count() == count
