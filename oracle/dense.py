@@ -129,6 +129,25 @@ def row_forward(Q, K, V, c, allowed_row, i):
     return (e @ V) / l, m + np.log(l)
 
 
+def row_backward(Q, K, V, G, c, allowed_row, i):
+    """dQ_i and delta_i of one head's row i (for sampled full-size checks).
+
+    The Reverse procedure of "Exact tiled softmax attention with block-recomputed
+    vector-Jacobian products" restricted to one query row: p_ij from the row's
+    own scores, dP_ij = G_i . V_j, delta_i = sum_j p_ij dP_ij (formed this way,
+    not as G_i . Y_i), gamma_ij = p_ij (dP_ij - delta_i), dQ_i = c sum_j gamma_ij K_j.
+    """
+    if not allowed_row.any():
+        raise ValueError("every allowed-key set A_i must be nonempty")
+    s = np.where(allowed_row, c * (K @ Q[i]), -np.inf)
+    e = np.exp(s - s.max())
+    p = e / e.sum()
+    dP = V @ G[i]
+    delta = p @ dP
+    gamma = p * (dP - delta)
+    return c * (gamma @ K), delta
+
+
 def _rect_keep(h, nq, nk, dropout):
     from .philox import keep_mask, keep_scale
     q, seed = dropout

@@ -264,14 +264,8 @@ def _sampled_heads(ex, w, heads):
     return compare(w.dtype, got, dict(Y=Y, L=L, dQ=dQ, dK=dK, dV=dV), heads=heads)
 
 
-def test_workload2_full_size_sampled_heads(ex):
-    w = workloads.workload(2)
-    _sampled_heads(ex, w, [0, w.B * w.H - 1])
-
-
-def test_workload3_full_size_sampled_heads(ex):
-    w = workloads.workload(3)
-    _sampled_heads(ex, w, [0, 77, w.B * w.H - 1])
+# Workloads 2 and 3 at full size: tests/test_gpu_fullsize.py (every slice on
+# sampled rows and identities, whole gradients on one slice per item group).
 
 
 @pytest.mark.parametrize("variant", ["", "window"])
