@@ -541,13 +541,72 @@ HostStepLayout host_layout(const Dims& d, int mask_kind) {
 }
 
 // Streams and events of the host step, made once per host thread and device
-// (and kept for the thread's lifetime).
+// and released when the thread exits (or right away if making one of them
+// fails).  Destroying a stream or event whose work is still queued is allowed:
+// CUDA releases it once that work completes.  At process exit the runtime may
+// already be unloading; the calls then fail harmlessly.
 constexpr int kHostMaxDevices = 64;
 struct HostStepStreams {
   int device = -1;
   cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
   cudaEvent_t start = nullptr, loaded[kHostMaxChunks] = {}, done[kHostMaxChunks] = {},
               end_in = nullptr, end_comp = nullptr, end_out = nullptr;
+
+  HostStepStreams() = default;
+  HostStepStreams(const HostStepStreams&) = delete;
+  HostStepStreams& operator=(const HostStepStreams&) = delete;
+  ~HostStepStreams() { release(); }
+
+  // Destroys whatever was made, on the device it was made on.
+  void release() {
+    if (device < 0) return;
+    int cur = -1;
+    const bool switched = cudaGetDevice(&cur) == cudaSuccess && cur != device &&
+                          cudaSetDevice(device) == cudaSuccess;
+    for (cudaStream_t* st : {&in, &comp, &out})
+      if (*st) {
+        cudaStreamDestroy(*st);
+        *st = nullptr;
+      }
+    for (cudaEvent_t* ev : {&start, &end_in, &end_comp, &end_out})
+      if (*ev) {
+        cudaEventDestroy(*ev);
+        *ev = nullptr;
+      }
+    for (int c = 0; c < kHostMaxChunks; ++c)
+      for (cudaEvent_t* ev : {&loaded[c], &done[c]})
+        if (*ev) {
+          cudaEventDestroy(*ev);
+          *ev = nullptr;
+        }
+    if (switched) cudaSetDevice(cur);
+    device = -1;
+  }
+
+  // Makes every stream and event on the current device `dev`; on failure
+  // releases those already made and returns the error.
+  cudaError_t create(int dev) {
+    device = dev;
+    const unsigned f = cudaEventDisableTiming;
+    cudaError_t e;
+    if ((e = cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&comp, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&start, f)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&end_in, f)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&end_comp, f)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&end_out, f)) != cudaSuccess) {
+      release();
+      return e;
+    }
+    for (int c = 0; c < kHostMaxChunks; ++c)
+      if ((e = cudaEventCreateWithFlags(&loaded[c], f)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&done[c], f)) != cudaSuccess) {
+        release();
+        return e;
+      }
+    return cudaSuccess;
+  }
 };
 
 cudaError_t host_streams(HostStepStreams*& hs) {
@@ -557,24 +616,7 @@ cudaError_t host_streams(HostStepStreams*& hs) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kHostMaxDevices) return cudaErrorInvalidDevice;
   HostStepStreams& cache = caches[dev];
-  if (cache.device != dev) {
-    HostStepStreams n;
-    n.device = dev;
-    const unsigned f = cudaEventDisableTiming;
-    if ((e = cudaStreamCreateWithFlags(&n.in, cudaStreamNonBlocking)) != cudaSuccess ||
-        (e = cudaStreamCreateWithFlags(&n.comp, cudaStreamNonBlocking)) != cudaSuccess ||
-        (e = cudaStreamCreateWithFlags(&n.out, cudaStreamNonBlocking)) != cudaSuccess ||
-        (e = cudaEventCreateWithFlags(&n.start, f)) != cudaSuccess ||
-        (e = cudaEventCreateWithFlags(&n.end_in, f)) != cudaSuccess ||
-        (e = cudaEventCreateWithFlags(&n.end_comp, f)) != cudaSuccess ||
-        (e = cudaEventCreateWithFlags(&n.end_out, f)) != cudaSuccess)
-      return e;
-    for (int c = 0; c < kHostMaxChunks; ++c)
-      if ((e = cudaEventCreateWithFlags(&n.loaded[c], f)) != cudaSuccess ||
-          (e = cudaEventCreateWithFlags(&n.done[c], f)) != cudaSuccess)
-        return e;
-    cache = n;
-  }
+  if (cache.device != dev && (e = cache.create(dev)) != cudaSuccess) return e;
   hs = &cache;
   return cudaSuccess;
 }

@@ -79,3 +79,46 @@ def test_host_step_status_reports_empty_rows(ex):
     assert ex.device_status(ws) == 5  # EXATTN_EMPTY_ROW
     assert torch.isneginf(L[:, :, 5]).all()
     assert (y[:, :, 5] == 0).all()
+
+
+def test_host_step_from_threads_that_exit(ex):
+    """attn_step_host keeps its streams and events per host thread and releases
+    them when the thread exits.  Several short-lived threads each run a step
+    (making and, at exit, destroying their own set); the results match the
+    main thread's bitwise, and the main thread's calls still work afterwards."""
+    import threading
+
+    w = workloads.small(1, 5, 256, 64, 64, "bf16", "causal", 0.125, seed=31)
+    x = workloads.make_inputs(w)
+    dev = torch.device("cuda:0")
+    pin = [t.contiguous().pin_memory() for t in (x.Q, x.K, x.V, x.dY)]
+    want = ex.step_host(*pin, w.scale, "causal", 0, None, device=dev)
+    torch.cuda.synchronize()
+    want = [t.clone() for t in want]
+    results, errors = {}, []
+
+    def worker(idx):
+        try:
+            torch.cuda.set_device(dev)
+            s = torch.cuda.Stream(dev)
+            out = ex.step_host(*pin, w.scale, "causal", 0, None, stream=s, device=dev)
+            s.synchronize()
+            results[idx] = [t.clone() for t in out]
+        except Exception as e:  # reported below, in the main thread
+            errors.append(repr(e))
+
+    for rnd in range(3):
+        threads = [threading.Thread(target=worker, args=(4 * rnd + i,)) for i in range(4)]
+        for t in threads:
+            t.start()
+        for t in threads:
+            t.join()
+    assert not errors, errors
+    assert len(results) == 12
+    for got in results.values():
+        for a, b in zip(got, want):
+            assert torch.equal(a, b)
+    again = ex.step_host(*pin, w.scale, "causal", 0, None, device=dev)
+    torch.cuda.synchronize()
+    for a, b in zip(again, want):
+        assert torch.equal(a, b)
