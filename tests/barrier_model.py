@@ -175,9 +175,12 @@ def _ring_fill(slot_bar_empty, slot_bar_full, fill):
 # with a number of non-empty key blocks.
 # ---------------------------------------------------------------------------
 def dq_kernel(blocks, ew_warps=3, two_ds=True, NK=3, NV=1):
-    """Roles of the dQ kernel for items with blocks[n] key blocks each.
+    """Roles of the dQ kernel (tc_bwd_q_kernel) for items with blocks[n] key
+    blocks each: TMA, MMA and the elementwise warps, which also form delta
+    (meeting at B_DPART) and run the dQ epilogue (B_DONE / B_DREAD, staging
+    tile: B_EPIF / B_EPI).
 
-    two_ds=False models the older form with one dS barrier (waited with
+    two_ds=False models its first form, with one dS barrier (waited with
     parity t & 1), which a schedule can break: the elementwise warps complete
     dS(t) and dS(t + 1) before the MMA warp's first poll of dS(t)."""
     W = ew_warps

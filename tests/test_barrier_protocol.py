@@ -75,6 +75,7 @@ def test_atomic_kernel_protocol_holds():
 
 
 @pytest.mark.parametrize("factory,drop", [(bm.dq_kernel, "QFREE"), (bm.dq_kernel, "SFREE"),
+                                           (bm.dq_kernel, "DREAD"), (bm.dq_kernel, "DPART"),
                                            (bm.kv_kernel, "ACCFREE"), (bm.kv_kernel, "P"),
                                            (bm.fwd_kernel, "OREAD0")])
 def test_model_catches_a_missing_wait(factory, drop):
