@@ -352,6 +352,16 @@ def kernel_roofline(args, w, which, achieved, peaks, peak_kind):
                 "tensor_work_frac": 3 * achieved / peak,
                 "note": "3xTF32: the tensor pipe runs three tf32 products per product",
                 "traffic": read_traffic("tc32_fwd")}
+    if (w.dtype == "f32" and which == "bwd" and args.path == "auto" and not args.dropout
+            and w.d == 64 and w.v == 64):
+        peak = bf16_peak * TF32_OVER_BF16
+        return {"kernel": "tc32_bwd", "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_kind": f"tf32 dense = bf16 burst of {peak_kind} x 1.1/2.25 (nominal ratio)",
+                "tensor_work_frac": 21 / 5 * achieved / peak,
+                "note": "3xTF32 reverse: 7 products per tile (S, dP twice; dV, dK, dQ), "
+                        "three tf32 products each, against the convention's 5",
+                "traffic": read_traffic("tc32_bwd")}
     mhz = float(peaks.get("sm_max_mhz", 2070.0))
     peak = 152 * 128 * 2 * mhz * 1e6 / 1e12
     return {"kernel": f"simt_{which}", "bound": "alu", "achieved": achieved, "peak": peak,

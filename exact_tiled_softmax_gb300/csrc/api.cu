@@ -99,8 +99,18 @@ size_t bwd_vec_bytes(const Dims& s) {
 size_t bwd_delta_offset() { return kStatusBytes; }
 size_t bwd_lse2_offset(const Dims& s) { return kStatusBytes + bwd_vec_bytes(s); }
 size_t bwd_dqacc_offset(const Dims& s) { return kStatusBytes + 2 * bwd_vec_bytes(s); }
+size_t bwd_bwd32_offset(const Dims& s) {
+  return align_up(bwd_dqacc_offset(s) + sizeof(float) * (size_t)s.batch * s.heads * s.nq * s.d,
+                  256);
+}
+// fp32 with d = v = 64 (the 3xTF32 reverse pass) also holds the tf32 parts of
+// Q, dY, K, V after the accumulator.
+bool bwd32_shape(const Dims& s) { return s.dtype == EXATTN_F32 && s.d == 64 && s.v == 64; }
 size_t bwd_ws_bytes(const Dims& s) {
-  return bwd_dqacc_offset(s) + sizeof(float) * (size_t)s.batch * s.heads * s.nq * s.d;
+  if (!bwd32_shape(s))
+    return bwd_dqacc_offset(s) + sizeof(float) * (size_t)s.batch * s.heads * s.nq * s.d;
+  return bwd_bwd32_offset(s) +
+         bwd32_bytes(make_problem(s, 1.f, EXATTN_MASK_NONE, 0, nullptr));
 }
 
 }  // namespace
@@ -266,6 +276,14 @@ int bwd_impl(const Dims& dims, const void* Q, const void* K, const void* V, cons
   cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes, s);
   if (e != cudaSuccess) return cuda_status(e, "attn_bwd: clearing the status word");
   const int path = g_path.load();
+  if (path == EXATTN_PATH_AUTO && bwd32_shape(dims) && tc_bwd32_supported(a.p)) {
+    // 3xTF32: delta and L log2(e), then the split of the operands, the dQ and
+    // the dK / dV kernels; dQ is written directly.
+    e = launch_delta(a, s);
+    if (e != cudaSuccess) return cuda_status(e, "attn_bwd: delta launch");
+    return cuda_status(launch_tc_bwd32(a, bwd32_layout(a.p, ws + bwd_bwd32_offset(dims)), s),
+                       "attn_bwd: 3xTF32 reverse launch");
+  }
   if (path == EXATTN_PATH_AUTO && tc_bwd_split_supported(a.p)) {
     // Split form: dQ is written directly, no accumulator; the dQ kernel also
     // forms delta and L log2(e).

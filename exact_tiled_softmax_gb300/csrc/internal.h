@@ -124,6 +124,23 @@ size_t split32_bytes(const Problem& p);
 Split32 split32_layout(const Problem& p, void* base);
 cudaError_t launch_tc_fwd32(const FwdArgs& a, const Split32& ws, cudaStream_t s);
 
+// 3xTF32 tensor-core reverse pass for fp32 inputs (d = v = 64): a
+// preparation kernel writes the tf32 hi / lo parts of Q, dY, K, V (and of Q,
+// dY, K transposed) to the workspace, then a query-major dQ kernel and a
+// key-major dK / dV kernel.  delta and L log2(e) must be in place (launch_delta).
+struct Bwd32Split {
+  float *qh, *ql, *yh, *yl;      // [BH][n][64]
+  float *kh, *kl, *vh, *vl;      // [BH][nk][64]
+  float *qth, *qtl, *yth, *ytl;  // [BH][64][ldq]
+  float *kth, *ktl;              // [BH][64][ldk]
+  int ldq, ldk;                  // n, nk rounded up to 32
+  size_t bytes;
+};
+bool tc_bwd32_supported(const Problem& p);
+size_t bwd32_bytes(const Problem& p);
+Bwd32Split bwd32_layout(const Problem& p, void* base);
+cudaError_t launch_tc_bwd32(const BwdArgs& a, const Bwd32Split& w, cudaStream_t s);
+
 // Split-KV forward (nq queries aligned to the end of nk keys).
 struct SplitArgs {
   const void* Q;

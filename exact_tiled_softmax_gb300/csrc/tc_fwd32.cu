@@ -43,6 +43,8 @@
 namespace exattn {
 
 PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder();  // tc_fwd.cu
+bool make_tmap_f32(CUtensorMap* m, const void* base, int inner, int ld, int rows, int BH,
+                   int box_rows);
 
 namespace {
 
@@ -93,15 +95,6 @@ struct Layout32 {
   static_assert(T_OM + V <= kTmemCols, "TMEM columns");
   static_assert(ALLOC <= 232448, "shared memory");
 };
-
-// x rounded to the nearest tf32 (ties away from zero): clear the 13 low
-// fraction bits after adding half of their weight.
-__device__ __forceinline__ float tf32_hi(float x) {
-  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
-}
-// The lo part x - hi, itself rounded to tf32 so that the tensor core reads it
-// exactly (|x - hi - lo| <= 2^-22 |x|).
-__device__ __forceinline__ float tf32_lo(float x, float hi) { return tf32_hi(x - hi); }
 
 __device__ __forceinline__ uint32_t range_bits(int a, int b) {
   a = max(a, 0);
@@ -554,24 +547,6 @@ __global__ void __launch_bounds__(256) split32_kernel(const float* K, const floa
   }
 }
 
-// 3-D fp32 tensor map {inner, rows, BH} with row stride `ld` elements, boxes
-// of 32 x box_rows x 1 and 128-byte swizzle; elements past the extents read 0.
-bool make_tmap_f32(CUtensorMap* m, const void* base, int inner, int ld, int rows, int BH,
-                   int box_rows) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
-                        static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4,
-                           static_cast<cuuint64_t>(ld) * rows * 4};
-  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(box_rows), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 cudaError_t launch_d(const FwdArgs& a, const Split32& ws, cudaStream_t s) {
   const Problem& pr = a.p;
@@ -615,6 +590,24 @@ cudaError_t launch_d(const FwdArgs& a, const Split32& ws, cudaStream_t s) {
 }
 
 }  // namespace
+
+// 3-D fp32 tensor map {inner, rows, BH} with row stride `ld` elements, boxes
+// of 32 x box_rows x 1 and 128-byte swizzle; elements past the extents read 0.
+bool make_tmap_f32(CUtensorMap* m, const void* base, int inner, int ld, int rows, int BH,
+                   int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4,
+                           static_cast<cuuint64_t>(ld) * rows * 4};
+  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool tc_fwd32_supported(const Problem& p) {
   if (p.dtype != kF32 || p.d != p.v || (p.d != 64 && p.d != 128)) return false;

@@ -286,6 +286,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Four fp32 adds into global memory, no value returned.
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+// x rounded to the nearest tf32 (ties away from zero): clear the 13 low
+// fraction bits after adding half of their weight.
+__device__ __forceinline__ float tf32_hi(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+}
+// The lo part x - hi, itself rounded to tf32 so that the tensor core reads it
+// exactly (|x - hi - lo| <= 2^-22 |x|).
+__device__ __forceinline__ float tf32_lo(float x, float hi) { return tf32_hi(x - hi); }
+
 // Instruction descriptor of tcgen05.mma kind::tf32: tf32 A and B (format 2),
 // both K-major, fp32 D.
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {

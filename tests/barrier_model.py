@@ -619,3 +619,97 @@ def atomic_kernel(n_blocks, ew_warps=2, drain_warps=2):
     for w in range(Dw):
         roles[f"drain{w}"] = drain()
     return need, roles
+
+
+# ---------------------------------------------------------------------------
+# 3xTF32 reverse pass (tc_bwd32.cu): one CTA per block, steps of 32 rows.
+# ---------------------------------------------------------------------------
+def kv32_kernel(n_steps, ew_warps=2, NST=3):
+    """dK/dV kernel: the elementwise warps write K, V to TMEM (B_A), then per
+    step wait for S^T, dP^T (B_SP) and write P^T, dS^T (B_P)."""
+    W = ew_warps
+    need = defaultdict(lambda: 1)
+    need["A"] = need["P"] = W
+    k = n_steps
+
+    def tma():
+        for it in range(k):
+            yield from _ring_fill(f"QE{it % NST}", f"QF{it % NST}", it // NST)
+        for u in range(min(NST, k)):
+            i = k - 1 - u
+            yield ("wait", f"QF{i % NST}", i // NST)
+
+    def mma():
+        yield ("wait", "A", 0)
+        for it in range(k):
+            yield ("wait", f"QF{it % NST}", it // NST)
+            yield ("mma", "S")
+            yield ("mma", "dP")
+            yield ("commit", "SP")
+            yield ("wait", "P", it)
+            yield ("mma", "dV")
+            yield ("mma", "dK")
+            yield ("commit", f"QE{it % NST}")
+        yield ("commit", "DONE")
+        yield ("commit", "DRAIN")
+        yield ("wait", "DRAIN", 0)
+
+    def ew():
+        yield ("arrive", "A")
+        for it in range(k):
+            yield ("wait", "SP", it)
+            yield ("arrive", "P")
+        if k > 0:
+            yield ("wait", "DONE", 0)
+
+    roles = {"tma": tma(), "mma": mma()}
+    for w in range(W):
+        roles[f"ew{w}"] = ew()
+    return need, roles
+
+
+def q32_kernel(n_steps, ew_warps=2, NST=4):
+    """dQ kernel: S and dP double-buffered (B_SP per buffer); dS per buffer
+    (B_DS); dQ(t) after dS(t), S(t+1) and dP(t+1) before it."""
+    W = ew_warps
+    need = defaultdict(lambda: 1)
+    need["A"] = need["DS0"] = need["DS1"] = W
+    k = n_steps
+
+    def tma():
+        for it in range(k):
+            yield from _ring_fill(f"KE{it % NST}", f"KF{it % NST}", it // NST)
+        for u in range(min(NST, k)):
+            i = k - 1 - u
+            yield ("wait", f"KF{i % NST}", i // NST)
+
+    def mma():
+        yield ("wait", "A", 0)
+        if k > 0:
+            yield ("wait", "KF0", 0)
+            yield ("mma", "SdP0")
+            yield ("commit", "SP0")
+        for t in range(k):
+            if t + 1 < k:
+                yield ("wait", f"KF{(t + 1) % NST}", (t + 1) // NST)
+                yield ("mma", f"SdP{t + 1}")
+                yield ("commit", f"SP{(t + 1) & 1}")
+            yield ("wait", f"DS{t & 1}", t >> 1)
+            yield ("mma", f"dQ{t}")
+            yield ("commit", f"KE{t % NST}")
+        yield ("commit", "DONE")
+        yield ("commit", "DRAIN")
+        yield ("wait", "DRAIN", 0)
+
+    def ew():
+        yield ("arrive", "A")
+        for t in range(k):
+            yield ("wait", f"SP{t & 1}", t >> 1)
+            yield ("arrive", f"DS{t & 1}")
+        if k > 0:
+            yield ("wait", "DONE", 0)
+
+    roles = {"tma": tma(), "mma": mma()}
+    for w in range(W):
+        roles[f"ew{w}"] = ew()
+    return need, roles

@@ -86,3 +86,16 @@ def test_model_catches_a_missing_wait(factory, drop):
     else:
         make = lambda rnd: bm.random_counts(rnd, rnd.randint(3, 8), (0, 1, 2, 3))
     assert _search(factory, make, 51, n=200, skip_waits={drop})
+
+
+def test_fp32_reverse_kernels_protocol_holds():
+    steps = lambda rnd: rnd.randint(0, 11)
+    assert _search(bm.kv32_kernel, steps, 61) == []
+    assert _search(bm.q32_kernel, steps, 62) == []
+    assert _search(bm.q32_kernel, steps, 63, NST=2, ew_warps=3) == []
+
+
+@pytest.mark.parametrize("factory,drop", [(bm.kv32_kernel, "QE0"), (bm.q32_kernel, "SP0"),
+                                          (bm.q32_kernel, "DS0")])
+def test_fp32_reverse_model_catches_a_missing_wait(factory, drop):
+    assert _search(factory, lambda rnd: rnd.randint(3, 11), 64, n=200, skip_waits={drop})

@@ -80,11 +80,22 @@ def test_fp32_forward_uses_the_derived_tf32_peak(no_traffic):
     assert r["kernel"] == "tc32_fwd"
     assert r["peak"] == pytest.approx(PEAKS["bf16_tflops"] * 1.1 / 2.25)
     assert r["tensor_work_frac"] == pytest.approx(3 * r["frac"])
-    # With dropout, or for its reverse pass, fp32 runs on the SIMT kernels.
+    # With dropout, or for the reverse pass of d = 128, fp32 runs on the SIMT kernels.
     assert bench.kernel_roofline(_args(dropout=0.1), _w(128, 128, "f32"), "fwd", 1.0, PEAKS,
                                  "measured")["kernel"] == "simt_fwd"
     assert bench.kernel_roofline(_args(), _w(128, 128, "f32"), "bwd", 1.0, PEAKS,
                                  "measured")["kernel"] == "simt_bwd"
+
+
+def test_fp32_reverse_of_width_64_is_the_3xtf32_kernel_pair(no_traffic):
+    r = bench.kernel_roofline(_args(), _w(64, 64, "f32"), "bwd", 90.0, PEAKS, "measured")
+    assert r["kernel"] == "tc32_bwd" and r["bound"] == "tensor"
+    assert r["peak"] == pytest.approx(PEAKS["bf16_tflops"] * 1.1 / 2.25)
+    # 7 products per tile, each three tf32 products, against the convention's 5
+    assert r["tensor_work_frac"] == pytest.approx(21 / 5 * r["frac"])
+    for args, w in ((_args("simt"), _w(64, 64, "f32")), (_args(dropout=0.1), _w(64, 64, "f32")),
+                    (_args("atomic_dq"), _w(64, 64, "f32")), (_args(), _w(80, 96, "f32"))):
+        assert bench.kernel_roofline(args, w, "bwd", 1.0, PEAKS, "measured")["kernel"] == "simt_bwd"
 
 
 def test_read_traffic_rejects_a_changed_source(tmp_path, monkeypatch):
