@@ -145,9 +145,10 @@ class ClockSampler:
 # The oracle on the host cores (cpu_baseline and the reference arm)
 # --------------------------------------------------------------------------- #
 
-def oracle_sample_step(w, Q, K, V, G, rows, dropout=None):
+def oracle_sample_step(w, Q, K, V, G, rows, dropout=None, bits=None):
     """Oracle forward + reverse over the last ``rows`` query rows of head 0.
-    ``dropout`` = (keep mask of those rows, keep scale) for the dropout forms.
+    ``dropout`` = (keep mask of those rows, keep scale) for the dropout forms;
+    ``bits`` = the workload's bit rows for the bitmask mask.
 
     Returns the algorithmic flops of that sample (same convention as the GPU
     metric: 2 |A| (d+v) forward, 2.5x that reverse)."""
@@ -163,7 +164,7 @@ def oracle_sample_step(w, Q, K, V, G, rows, dropout=None):
         pairs = sum(max(0, min(w.n_keys, i + off + 1)) if w.mask == "causal" else w.n_keys
                     for i in range(r0, n))
         return 3.5 * 2.0 * pairs * (w.d + w.v)
-    allowed = masks.allowed_matrix(n, w.mask_kind, w.window, None)[r0:]
+    allowed = masks.allowed_matrix(n, w.mask_kind, w.window, bits)[r0:]
     if dropout is None:
         dense.head_forward(Q[r0:], K, V, w.scale, allowed)
         dense.head_backward(Q[r0:], K, V, G[r0:], w.scale, allowed)
@@ -191,19 +192,25 @@ def oracle_dropout(w, rows, q, seed):
 _BLAS_ENV = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
 
 
-def _oracle_worker(w, arrays, rows, drop, budget_s, barrier, out):
+def _oracle_worker(w, arrays, bits, rows, drop, budget_s, barrier, out):
     """One process of the CPU baseline: the oracle sample on one BLAS thread,
-    started with the others at the barrier, for ``budget_s`` seconds."""
-    Q, K, V, G = arrays
-    oracle_sample_step(w, Q, K, V, G, min(rows, 32), drop and (drop[0][-32:], drop[1]))  # warm-up
-    barrier.wait()
-    done, samples, t0 = 0.0, 0, time.perf_counter()
-    while True:
-        done += oracle_sample_step(w, Q, K, V, G, rows, drop)
-        samples += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    out.put((done, samples, time.perf_counter() - t0))
+    started with the others at the barrier, for ``budget_s`` seconds.  A failure
+    is reported on the queue (and breaks the barrier) instead of hanging it."""
+    try:
+        Q, K, V, G = arrays
+        oracle_sample_step(w, Q, K, V, G, min(rows, 32),
+                           drop and (drop[0][-32:], drop[1]), bits)  # warm-up
+        barrier.wait()
+        done, samples, t0 = 0.0, 0, time.perf_counter()
+        while True:
+            done += oracle_sample_step(w, Q, K, V, G, rows, drop, bits)
+            samples += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        out.put((done, samples, time.perf_counter() - t0))
+    except BaseException as e:  # noqa: BLE001 -- reported to the parent
+        barrier.abort()
+        out.put(("error", repr(e)))
 
 
 def cpu_baseline(w, x, budget_s=12.0, rows=512, q=0.0, seed=0):
@@ -213,6 +220,7 @@ def cpu_baseline(w, x, budget_s=12.0, rows=512, q=0.0, seed=0):
     rows of head 0) for ``budget_s`` seconds after a common start."""
     import multiprocessing as mp
     Q, K, V, G = oracle_inputs(w, x)
+    rows = min(rows, w.n)
     drop = oracle_dropout(w, rows, q, seed)
     procs_n = max(1, host_cores())
     ctx = mp.get_context("spawn")
@@ -222,11 +230,19 @@ def cpu_baseline(w, x, budget_s=12.0, rows=512, q=0.0, seed=0):
     try:
         barrier, out = ctx.Barrier(procs_n), ctx.Queue()
         procs = [ctx.Process(target=_oracle_worker,
-                             args=(w, (Q, K, V, G), rows, drop, budget_s, barrier, out))
+                             args=(w, (Q, K, V, G), x.bitmask, rows, drop, budget_s, barrier,
+                                   out))
                  for _ in range(procs_n)]
         for pr in procs:
             pr.start()
-        res = [out.get(timeout=budget_s + 600) for _ in procs]
+        res = []
+        for _ in procs:
+            r = out.get(timeout=budget_s + 300)
+            if r[0] == "error":
+                for pr in procs:
+                    pr.terminate()
+                raise RuntimeError(f"CPU baseline worker failed: {r[1]}")
+            res.append(r)
         for pr in procs:
             pr.join()
     finally:
@@ -257,14 +273,14 @@ def run_reference(args, w):
         return
     x = workloads.make_inputs(w, heads=1)
     Q, K, V, G = oracle_inputs(w, x)
-    rows = args.ref_rows
+    rows = min(args.ref_rows, w.n)
     drop = oracle_dropout(w, rows, args.dropout, args.seed)
     for _ in range(args.warmup):
-        oracle_sample_step(w, Q, K, V, G, rows, drop)
+        oracle_sample_step(w, Q, K, V, G, rows, drop, x.bitmask)
     t0 = time.perf_counter()
     total = 0.0
     for _ in range(args.steps):
-        total += oracle_sample_step(w, Q, K, V, G, rows, drop)
+        total += oracle_sample_step(w, Q, K, V, G, rows, drop, x.bitmask)
     el = time.perf_counter() - t0
     value = total / el / 1e12
     line = {

@@ -488,8 +488,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(Lay::B_P));
     }
-    // Epilogue: the last partial dV_j, c dK_j (zeros when no query reaches the block).
-    const bool have = ok && nsteps > 0 && mbar_wait(bar(Lay::B_DONE), 0, abort_flag);
+    // Epilogue: the last partial dV_j, c dK_j (zeros when no query reaches the
+    // block).  The TMEM reads are warp-collective: the predicate is the warp's.
+    const bool have = __all_sync(
+        0xFFFFFFFFu, ok && nsteps > 0 && mbar_wait(bar(Lay::B_DONE), 0, abort_flag));
     if (ok && nsteps > 0 && !have) ok = false;
     tc_fence_after();
     if (have) {
@@ -741,8 +743,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(Lay::B_DS + b));
     }
-    // Epilogue: c dQ_i, an fp32 row (zeros when the block reaches no key).
-    const bool have = ok && nsteps > 0 && mbar_wait(bar(Lay::B_DONE), 0, abort_flag);
+    // Epilogue: c dQ_i, an fp32 row (zeros when the block reaches no key).  The
+    // TMEM reads are warp-collective: the predicate is the warp's.
+    const bool have = __all_sync(
+        0xFFFFFFFFu, ok && nsteps > 0 && mbar_wait(bar(Lay::B_DONE), 0, abort_flag));
     if (ok && nsteps > 0 && !have) ok = false;
     tc_fence_after();
 #pragma unroll 1
