@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         *abort_flag = 1;
       }
       for (int s = 0; s < 2; ++s)
-        if (last_phase[s] >= 0) mbar_wait(bar(Lay::B_QF + s), last_phase[s], abort_flag);
+        if (last_phase[s] >= 0) mbar_wait_inflight(bar(Lay::B_QF + s), last_phase[s]);
       mbar_wait(bar(Lay::B_KV), 0, abort_flag);
     }
   } else if (warp == kWarpMMA) {
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         *abort_flag = 1;
       }
       tc_commit(bar(Lay::B_DRAIN));
-      mbar_wait(bar(Lay::B_DRAIN), 0, abort_flag);
+      mbar_wait_inflight(bar(Lay::B_DRAIN), 0);
     }
   } else if (warp < 8) {
     // Elementwise: thread = key row r, query half X.

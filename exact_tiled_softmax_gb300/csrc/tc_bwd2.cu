@@ -412,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int qb = qb_begin; qb < qb_end; ++qb) {
         if (cls_of(qb, kb) == kEmpty) continue;
         const int slot = it % NST, phase = (it / NST) & 1;
-        ++it;
         if (!(ok = mbar_wait(bar(Lay::B_QE + slot), phase ^ 1, abort_flag))) break;
+        ++it;  // fills issued
         const uint32_t st = sbase + Lay::STAGE_OFF + slot * Lay::STAGE;
         const uint32_t fb = bar(Lay::B_QF + slot);
         if (leader) {
@@ -441,9 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The last fill of each stage (iteration i = it - 1 - u fills stage i % NST).
     for (int u = 0; u < NST && u < it; ++u) {
       const int i = it - 1 - u;
-      mbar_wait(bar(Lay::B_QF + i % NST), (i / NST) & 1, abort_flag);
+      mbar_wait_inflight(bar(Lay::B_QF + i % NST), (i / NST) & 1);
     }
-    if (kv_loads > 0) mbar_wait(bar(Lay::B_KV), (kv_loads - 1) & 1, abort_flag);
+    if (kv_loads > 0) mbar_wait_inflight(bar(Lay::B_KV), (kv_loads - 1) & 1);
   } else if (warp == kWarpMMA) {
     const bool leader = elect_one();
     constexpr uint32_t kIdS = idesc_bf16(kBN, kBM, false, false);
@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
     }
     if (leader) tc_commit(bar(Lay::B_DRAIN));
-    mbar_wait(bar(Lay::B_DRAIN), 0, abort_flag);
+    mbar_wait_inflight(bar(Lay::B_DRAIN), 0);
   } else {
     // Elementwise: thread = key row r of the block; group g covers queries
     // 32g..32g+31.  Per query block two phases: P^T from S^T (then dV may
@@ -959,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&p.ty);
     }
     const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
-    int it = 0, q_loads = 0;
+    int it = 0, q_loads = 0, k_fills = 0, v_fills = 0;  // blocks; copies issued
     bool ok = true;
     int t = blockIdx.x;
     for (int nitem = 0;; ++nitem) {
@@ -1031,6 +1031,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             keep);
             }
           }
+          ++(kv == 0 ? v_fills : k_fills);
         }
         ++it;
         if (ok && t_next < 0) prefetch_next();
@@ -1044,17 +1045,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       raise_status(p.status, kStatusTimeout);
       *abort_flag = 1;
     }
-    // Never leave with copies in flight: the last fill of every slot (block
-    // i = it - 1 - u filled K slot i % NK and V slot NK + i % NV) and the last Q, dY.
-    for (int u = 0; u < Lay::NK && u < it; ++u) {
-      const int i = it - 1 - u;
-      mbar_wait(bar(Lay::B_KVF + i % Lay::NK), (i / Lay::NK) & 1, abort_flag);
+    // Never leave with copies in flight: the last fill of every slot (the i-th
+    // K copy went to slot i % NK, the i-th V copy to slot NK + i % NV) and the
+    // last Q, dY.
+    for (int u = 0; u < Lay::NK && u < k_fills; ++u) {
+      const int i = k_fills - 1 - u;
+      mbar_wait_inflight(bar(Lay::B_KVF + i % Lay::NK), (i / Lay::NK) & 1);
     }
-    for (int u = 0; u < Lay::NV && u < it; ++u) {
-      const int i = it - 1 - u;
-      mbar_wait(bar(Lay::B_KVF + Lay::NK + i % Lay::NV), (i / Lay::NV) & 1, abort_flag);
+    for (int u = 0; u < Lay::NV && u < v_fills; ++u) {
+      const int i = v_fills - 1 - u;
+      mbar_wait_inflight(bar(Lay::B_KVF + Lay::NK + i % Lay::NV), (i / Lay::NV) & 1);
     }
-    if (q_loads > 0) mbar_wait(bar(Lay::B_Q), (q_loads - 1) & 1, abort_flag);
+    if (q_loads > 0) mbar_wait_inflight(bar(Lay::B_Q), (q_loads - 1) & 1);
   } else if (warp == kWarpMMA) {
     const bool leader = elect_one();
     constexpr uint32_t kIdSS = idesc_bf16(kBM, kBN, false, false);
@@ -1180,7 +1182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
     }
     if (leader) tc_commit(bar(Lay::B_DRAIN));
-    mbar_wait(bar(Lay::B_DRAIN), 0, abort_flag);
+    mbar_wait_inflight(bar(Lay::B_DRAIN), 0);
   } else {
     // Elementwise: thread = query row r; group g covers keys 32g..32g+31.
     const int g = warp >> 2, wl = warp & 3;

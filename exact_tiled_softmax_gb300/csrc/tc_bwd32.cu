@@ -21,11 +21,13 @@
 // delta_i and L_i log2(e) come from the delta kernel (padded vectors).
 //
 // tc_bwd32_kv_kernel -- one CTA = 128 keys of one slice; steps of 32 queries.
-//   TMEM: K_hi, K_lo, V_hi, V_lo (64 columns each, A operands), dV, dK (64
-//   each), S^T then P^T_hi, P^T_lo, dP^T then dS^T_hi, dS^T_lo (32 each).
-//   Per step: S^T = K Q^T, dP^T = V dY^T; the elementwise warps (thread = key)
-//   form P^T and dS^T and write their tf32 parts; dV += P^T dY, dK += dS^T Q.
-//   Every kPromote steps the partial dV, dK rows go into the fp32 outputs.
+//   TMEM: K_hi, V_hi (64 columns each, A operands; K_lo, V_lo are A operands
+//   in shared memory), dV, dK (64 each), and two buffers of S^T then P^T_hi,
+//   P^T_lo, dP^T then dS^T_hi, dS^T_lo (32 each).  Per step: S^T = K Q^T,
+//   dP^T = V dY^T; the elementwise warps (thread = key) form P^T and dS^T and
+//   write their tf32 parts; dV += P^T dY, dK += dS^T Q.  S^T(t+1), dP^T(t+1)
+//   run while the elementwise warps work on step t.  Every kPromote steps the
+//   partial dV, dK rows go into the fp32 outputs.
 // tc_bwd32_q_kernel -- one CTA = 128 queries of one slice; steps of 32 keys.
 //   TMEM: Q_hi, Q_lo, dY_hi, dY_lo (64 each), dQ (64), and two buffers of
 //   S then dS_hi, dP, dS_lo (32 each): S(t+1) and dP(t+1) run while the
@@ -222,32 +224,86 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // ===========================================================================
 // Key-major kernel: dK, dV
 // ===========================================================================
-// Shared memory: NST stages of eight 8 KB tiles -- Q_hi, Q_lo, dY_hi, dY_lo
-// (32 queries x 64, two 128-byte-swizzled chunks of 32 rows x 32 columns) and
-// Q^T_hi, Q^T_lo, dY^T_hi, dY^T_lo (64 rows x 32 queries, one chunk) -- then
-// per stage delta and L log2(e) of the step's 32 queries.
+// Shared memory: NSS S halves (Q_lo, Q_hi, dY_lo, dY_hi: 32 queries x 64, in
+// 128-byte-swizzled chunks of 32 rows x 32 columns, a chunk's lo and hi tiles
+// adjacent), each free once S^T and dP^T of its step are done; NTS T halves (Q^T_hi, Q^T_lo, dY^T_hi, dY^T_lo:
+// 64 rows x 32 queries, one chunk), each free once dK of its step is; NV
+// slots of delta and L log2(e) for the step's 32 queries, free once the
+// elementwise warps have read them; then K_lo and V_lo (128 keys x 64, the A
+// operands of K_lo Q_hi^T and V_lo dY_hi^T), written by their rows' threads.
+// TMEM: K_hi [0,64), V_hi [64,128), dV [128,192), dK [192,256) and two step
+// buffers at 256 + 128 b of four 32-column blocks: S^T in two parts (then
+// P^T_hi, P^T_lo), dP^T in two parts (then dS^T_hi, dS^T_lo).  The MMA warp
+// issues S^T(t+1), dP^T(t+1) before dV(t), dK(t): the tensor pipe forms the
+// next step's products while the elementwise warps form P^T(t), dS^T(t);
+// dV(t) is issued once P^T(t) is written, dK(t) once dS^T(t) is.
+// A tcgen05.mma of M = 128 costs about as much for N = 32 as for N = 64
+// (measured: ~48 cycles each, 64 for N = 128), so S^T = K Q^T is formed as
+// K_hi [Q_lo; Q_hi]^T (one N = 64 product: K_hi Q_lo^T into the first block,
+// K_hi Q_hi^T into the second) plus K_lo Q_hi^T (N = 32, into the second
+// block), and the elementwise threads add the two blocks: 16 instructions
+// per product instead of 24.
 struct KvLay32 {
-  static constexpr int NST = 3;
-  static constexpr int QH = 0, QL = kTile, YH = 2 * kTile, YL = 3 * kTile, QTH = 4 * kTile,
-                       QTL = 5 * kTile, YTH = 6 * kTile, YTL = 7 * kTile, STAGE = 8 * kTile;
-  static constexpr int VEC_OFF = NST * STAGE;
-  static constexpr int BAR_OFF = VEC_OFF + NST * 256;
-  // B_A: K, V in TMEM; B_QF / B_QE: stage full / free; B_SP: S^T, dP^T done;
-  // B_P: P^T, dS^T parts written; B_DONE: dV, dK done.
-  static constexpr int B_A = 0, B_QF = 1, B_QE = B_QF + NST, B_SP = B_QE + NST, B_P = B_SP + 1,
-                       B_DONE = B_P + 1, B_DRAIN = B_DONE + 1, NBAR = B_DRAIN + 1;
+  static constexpr int NSS = 3, NTS = 2, NV = 4;
+  // S half: per 32-column chunk c the lo tile then the hi tile (4 KB each), so
+  // that [Q_lo; Q_hi] of a chunk is one 64-row B operand
+  static constexpr int QS = 0, YS = 2 * kTile, CHUNK = 2 * 4096, SHALF = 4 * kTile;
+  static constexpr int QTH = 0, QTL = kTile, YTH = 2 * kTile, YTL = 3 * kTile, THALF = 4 * kTile;
+  static constexpr int S_OFF = 0;
+  static constexpr int T_OFF = S_OFF + NSS * SHALF;
+  static constexpr int KLO_OFF = T_OFF + NTS * THALF;
+  static constexpr int VLO_OFF = KLO_OFF + kBlk * kD * 4;
+  static constexpr int VEC_OFF = VLO_OFF + kBlk * kD * 4;
+  static constexpr int BAR_OFF = VEC_OFF + NV * 256;
+  // B_A: K, V split; B_QSF / B_QSE, B_QTF / B_QTE, B_VF / B_VE: S half, T half,
+  // vector slot full / free; B_SP: S^T, dP^T of a buffer done; B_P, B_DS: P^T,
+  // dS^T parts of a buffer written; B_SEG: dV, dK of a kPromote-step segment
+  // done; B_DONE: all products done; B_DRAIN: the MMA warp's last commit.
+  static constexpr int B_A = 0, B_QSF = 1, B_QSE = B_QSF + NSS, B_QTF = B_QSE + NSS,
+                       B_QTE = B_QTF + NTS, B_VF = B_QTE + NTS, B_VE = B_VF + NV,
+                       B_SP = B_VE + NV, B_P = B_SP + 2, B_DS = B_P + 2, B_SEG = B_DS + 2,
+                       B_DONE = B_SEG + 1, B_DRAIN = B_DONE + 1, NBAR = B_DRAIN + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int ALLOC = MISC_OFF + 16 + 1024;
-  // TMEM columns (K_lo, V_lo sit 64 columns after K_hi, V_hi)
-  static constexpr uint32_t T_KH = 0, T_VH = 128, T_DV = 256, T_DK = 320, T_S = 384, T_PL = 416,
-                            T_DP = 448, T_DSL = 480;
+  static constexpr uint32_t T_KH = 0, T_VH = 64, T_DV = 128, T_DK = 192, T_BUF = 256,
+                            B_S = 0, B_PL = 32, B_DP = 64, B_DSL = 96, B_STRIDE = 128;
+  static_assert(SHALF % 1024 == 0 && THALF % 1024 == 0, "1024-byte aligned tiles");
+  static_assert(T_BUF + 2 * B_STRIDE <= kTmemCols, "TMEM columns");
   static_assert(ALLOC <= 232448, "shared memory");
 };
+
+// Row r of a 64-wide fp32 operand: its tf32 hi parts into TMEM (lane = r,
+// columns [taddr, taddr + 64)) and its lo parts into row r of a K-major,
+// 128-byte-swizzled shared-memory tile of 128 rows (two chunks of 32 columns,
+// 16 KB apart); zeros for a row past the end.
+__device__ __forceinline__ void row_split_tmem_smem(const float* row, bool valid, uint32_t taddr,
+                                                    uint8_t* tile, int r) {
+  const float4* r4 = reinterpret_cast<const float4*>(row);
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t hi[32];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float4 x = valid ? __ldg(r4 + 8 * c + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float xs[4] = {x.x, x.y, x.z, x.w};
+      float lo4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float h = tf32_hi(xs[u]);
+        hi[4 * e + u] = __float_as_uint(h);
+        lo4[u] = tf32_lo(xs[u], h);
+      }
+      *reinterpret_cast<float4*>(tile + c * (kBlk * 128) + r * 128 + ((e ^ (r & 7)) << 4)) =
+          make_float4(lo4[0], lo4[1], lo4[2], lo4[3]);
+    }
+    tmem_st32(taddr + 32 * c, hi);
+  }
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd32_kv_kernel(const __grid_constant__ Bwd32Params p) {
   using Lay = KvLay32;
-  constexpr int NST = Lay::NST;
+  constexpr int NSS = Lay::NSS, NTS = Lay::NTS, NV = Lay::NV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sbase = smem_u32(smem);
@@ -255,6 +311,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int k) { return bar0 + 8u * k; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  // Every role's waits are warp-uniform: a lane that timed out alone must not
+  // leave the others in a warp-collective instruction.
+  auto wait_warp = [&](int k, int parity) {
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar(k), static_cast<uint32_t>(parity), abort_flag));
+  };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = p.n, nk = p.nk, off = p.off;
@@ -270,12 +331,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Lay::B_A), kBlk);
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(bar(Lay::B_QF + s), 1);
-      mbar_init(bar(Lay::B_QE + s), 1);
+    for (int s = 0; s < NSS; ++s) {
+      mbar_init(bar(Lay::B_QSF + s), 1);
+      mbar_init(bar(Lay::B_QSE + s), 1);
     }
-    mbar_init(bar(Lay::B_SP), 1);
-    mbar_init(bar(Lay::B_P), kBlk);
+    for (int s = 0; s < NTS; ++s) {
+      mbar_init(bar(Lay::B_QTF + s), 1);
+      mbar_init(bar(Lay::B_QTE + s), 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(bar(Lay::B_VF + s), 1);
+      mbar_init(bar(Lay::B_VE + s), kBlk);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(Lay::B_SP + b), 1);
+      mbar_init(bar(Lay::B_P + b), kBlk);
+      mbar_init(bar(Lay::B_DS + b), kBlk);
+    }
+    mbar_init(bar(Lay::B_SEG), 1);
     mbar_init(bar(Lay::B_DONE), 1);
     mbar_init(bar(Lay::B_DRAIN), 1);
     misc[1] = 0;
@@ -304,106 +377,175 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint64_t keep = policy_evict_last();  // read by every key block of the slice
     bool ok = true;
-    for (int it = 0; it < nsteps && ok; ++it) {
-      const int slot = it % NST, fill = it / NST;
-      if (fill >= 1 && !(ok = mbar_wait(bar(Lay::B_QE + slot), (fill - 1) & 1, abort_flag))) break;
-      const uint32_t st = sbase + slot * Lay::STAGE, fb = bar(Lay::B_QF + slot);
-      const int q0 = (s_begin + it) * kStep;
+    int ns = 0, nt = 0, nv = 0;  // S halves, T halves, vector slots filled
+    // The S half and the vectors of step s (issued one step ahead of the T half).
+    auto load_s = [&](int s) {
+      const int q0 = (s_begin + s) * kStep;
+      const int slot = s % NSS, fill = s / NSS;
+      if (fill >= 1 && !(ok = wait_warp(Lay::B_QSE + slot, (fill - 1) & 1)))
+        return;
+      const uint32_t sh = sbase + Lay::S_OFF + slot * Lay::SHALF, fs = bar(Lay::B_QSF + slot);
       if (leader) {
-        mbar_arrive_expect_tx(fb, Lay::STAGE + 256);
+        mbar_arrive_expect_tx(fs, Lay::SHALF);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          tma_load_3d(st + Lay::QH + c * 4096, &p.tqh, fb, 32 * c, q0, bh, keep);
-          tma_load_3d(st + Lay::QL + c * 4096, &p.tql, fb, 32 * c, q0, bh, keep);
-          tma_load_3d(st + Lay::YH + c * 4096, &p.tyh, fb, 32 * c, q0, bh, keep);
-          tma_load_3d(st + Lay::YL + c * 4096, &p.tyl, fb, 32 * c, q0, bh, keep);
+          const uint32_t qc = sh + Lay::QS + c * Lay::CHUNK, yc = sh + Lay::YS + c * Lay::CHUNK;
+          tma_load_3d(qc, &p.tql, fs, 32 * c, q0, bh, keep);
+          tma_load_3d(qc + 4096, &p.tqh, fs, 32 * c, q0, bh, keep);
+          tma_load_3d(yc, &p.tyl, fs, 32 * c, q0, bh, keep);
+          tma_load_3d(yc + 4096, &p.tyh, fs, 32 * c, q0, bh, keep);
         }
-        tma_load_3d(st + Lay::QTH, &p.tqth, fb, q0, 0, bh, keep);
-        tma_load_3d(st + Lay::QTL, &p.tqtl, fb, q0, 0, bh, keep);
-        tma_load_3d(st + Lay::YTH, &p.tyth, fb, q0, 0, bh, keep);
-        tma_load_3d(st + Lay::YTL, &p.tytl, fb, q0, 0, bh, keep);
-        const size_t vo = static_cast<size_t>(bh) * p.npad + q0;
-        const uint32_t vec = sbase + Lay::VEC_OFF + slot * 256;
-        bulk_load_g2s(vec, p.delta + vo, 128, fb);
-        bulk_load_g2s(vec + 128, p.lse2 + vo, 128, fb);
       }
+      ++ns;
+      const int vs = s % NV, vfill = s / NV;
+      if (vfill >= 1 && !(ok = wait_warp(Lay::B_VE + vs, (vfill - 1) & 1)))
+        return;
+      const uint32_t vec = sbase + Lay::VEC_OFF + vs * 256, fv = bar(Lay::B_VF + vs);
+      if (leader) {
+        mbar_arrive_expect_tx(fv, 256);
+        const size_t vo = static_cast<size_t>(bh) * p.npad + q0;
+        bulk_load_g2s(vec, p.delta + vo, 128, fv);
+        bulk_load_g2s(vec + 128, p.lse2 + vo, 128, fv);
+      }
+      ++nv;
+    };
+    if (nsteps > 0) load_s(0);
+    for (int it = 0; it < nsteps && ok; ++it) {
+      if (it + 1 < nsteps) {
+        load_s(it + 1);
+        if (!ok) break;
+      }
+      const int slot = it % NTS, fill = it / NTS;
+      if (fill >= 1 && !(ok = wait_warp(Lay::B_QTE + slot, (fill - 1) & 1)))
+        break;
+      const uint32_t th = sbase + Lay::T_OFF + slot * Lay::THALF, ft = bar(Lay::B_QTF + slot);
+      const int q0 = (s_begin + it) * kStep;
+      if (leader) {
+        mbar_arrive_expect_tx(ft, Lay::THALF);
+        tma_load_3d(th + Lay::QTH, &p.tqth, ft, q0, 0, bh, keep);
+        tma_load_3d(th + Lay::QTL, &p.tqtl, ft, q0, 0, bh, keep);
+        tma_load_3d(th + Lay::YTH, &p.tyth, ft, q0, 0, bh, keep);
+        tma_load_3d(th + Lay::YTL, &p.tytl, ft, q0, 0, bh, keep);
+      }
+      ++nt;
     }
     __syncwarp();
     if (!ok && leader) {
       raise_status(p.status, kStatusTimeout);
       *abort_flag = 1;
     }
-    // Never leave with copies in flight: the last fill of every stage.
-    for (int u = 0; u < NST && u < nsteps; ++u) {
-      const int i = nsteps - 1 - u;
-      mbar_wait(bar(Lay::B_QF + i % NST), (i / NST) & 1, abort_flag);
+    // Never leave with copies in flight: the last fill of every slot.
+    for (int u = 0; u < NSS && u < ns; ++u) {
+      const int i = ns - 1 - u;
+      mbar_wait_inflight(bar(Lay::B_QSF + i % NSS), (i / NSS) & 1);
+    }
+    for (int u = 0; u < NTS && u < nt; ++u) {
+      const int i = nt - 1 - u;
+      mbar_wait_inflight(bar(Lay::B_QTF + i % NTS), (i / NTS) & 1);
+    }
+    for (int u = 0; u < NV && u < nv; ++u) {
+      const int i = nv - 1 - u;
+      mbar_wait_inflight(bar(Lay::B_VF + i % NV), (i / NV) & 1);
     }
   } else if (warp == kWarpMMA) {
+    // One elected lane runs the whole issue loop: it alone waits, issues and
+    // commits; the other lanes wait for it at the end.
     const bool leader = elect_one();
-    constexpr uint32_t kIdS = idesc_tf32(kBlk, kStep);
+    constexpr uint32_t kIdS = idesc_tf32(kBlk, kStep), kIdS2 = idesc_tf32(kBlk, 2 * kStep);
     constexpr uint32_t kIdAcc = idesc_tf32(kBlk, kD);
+    // One descriptor base for every shared-memory operand (tiles 1024-byte
+    // aligned, 8-row groups 1024 bytes apart); an operand adds its offset in
+    // units of 16 bytes.
     const uint64_t d0 = sdesc_sw128(sbase, 16, 1024);
-    bool ok = mbar_wait(bar(Lay::B_A), 0, abort_flag);
-    tc_fence_after();
-    // D[128 x 32] = A[128 x 64] B^T over 8 K-steps, three tf32 products:
-    // A_hi B_lo + A_lo B_hi + A_hi B_hi (A in TMEM, B = 32 x 64 stage tile).
-    auto issue_xt = [&](uint32_t d_col, uint32_t a_col, uint32_t st, int b_hi, int b_lo) {
-      if (leader) {
+    // S^T = K Q^T or dP^T = V dY^T of step t into buffer t & 1, over 8 K-steps
+    // of the width: A_hi [B_lo; B_hi]^T (N = 64, A_hi in TMEM, B the chunk's lo
+    // and hi tiles of the S half) into blocks 0 and 1, then A_lo B_hi^T (N = 32,
+    // A_lo in shared memory: 128 rows, chunks 16 KB apart) into block 1.
+    auto issue_xt = [&](uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t b) {
 #pragma unroll
-        for (int part = 0; part < 3; ++part) {
-          const uint32_t a = tmem + a_col + (part == 1 ? 64u : 0u);
-          const uint64_t b = d0 + ((st + (part == 0 ? b_lo : b_hi)) >> 4);
+      for (int kk = 0; kk < kD / 8; ++kk)
+        mma_ts_tf32(d, a_hi + 8 * kk, b + (((kk >> 2) * Lay::CHUNK + (kk & 3) * 32) >> 4), kIdS2,
+                    kk > 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < kD / 8; ++kk) {
-            const uint32_t o16 = ((kk >> 2) * 4096 + (kk & 3) * 32) >> 4;
-            mma_ts_tf32(tmem + d_col, a + 8 * kk, b + o16, kIdS, (part > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
-      }
+      for (int kk = 0; kk < kD / 8; ++kk)
+        mma_ss_tf32(d + kStep, d0 + ((a_lo + (kk >> 2) * (kBlk * 128) + (kk & 3) * 32) >> 4),
+                    b + (((kk >> 2) * Lay::CHUNK + 4096 + (kk & 3) * 32) >> 4), kIdS, 1u);
+    };
+    auto issue_step = [&](int t) {
+      const uint64_t sd = d0 + ((Lay::S_OFF + (t % NSS) * Lay::SHALF) >> 4);
+      const uint32_t buf = tmem + Lay::T_BUF + Lay::B_STRIDE * (t & 1);
+      issue_xt(buf + Lay::B_S, tmem + Lay::T_KH, Lay::KLO_OFF, sd + (Lay::QS >> 4));
+      issue_xt(buf + Lay::B_DP, tmem + Lay::T_VH, Lay::VLO_OFF, sd + (Lay::YS >> 4));
     };
     // D[128 x 64] += A[128 x 32] B^T over 4 K-steps (the step's queries), three
-    // products; A = the hi / lo parts in TMEM, B = 64 x 32 stage tile.
-    auto issue_acc = [&](uint32_t d_col, uint32_t a_hi, uint32_t a_lo, uint32_t st, int b_hi,
-                         int b_lo, bool first) {
-      if (leader) {
+    // products; A = the hi / lo parts in the step's TMEM buffer, B = a 64 x 32
+    // tile of the T half.
+    auto issue_acc = [&](uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t b_hi, uint64_t b_lo,
+                         bool first) {
 #pragma unroll
-        for (int part = 0; part < 3; ++part) {
-          const uint32_t a = tmem + (part == 1 ? a_lo : a_hi);
-          const uint64_t b = d0 + ((st + (part == 0 ? b_lo : b_hi)) >> 4);
+      for (int part = 0; part < 3; ++part) {
+        const uint32_t a = part == 1 ? a_lo : a_hi;
+        const uint64_t b = part == 0 ? b_lo : b_hi;
 #pragma unroll
-          for (int kk = 0; kk < kStep / 8; ++kk)
-            mma_ts_tf32(tmem + d_col, a + 8 * kk, b + ((kk * 32) >> 4), kIdAcc,
-                        (first && part == 0 && kk == 0) ? 0u : 1u);
-        }
+        for (int kk = 0; kk < kStep / 8; ++kk)
+          mma_ts_tf32(d, a + 8 * kk, b + ((kk * 32) >> 4), kIdAcc,
+                      (first && part == 0 && kk == 0) ? 0u : 1u);
       }
     };
-    for (int it = 0; it < nsteps && ok; ++it) {
-      const int slot = it % NST;
-      const uint32_t st = slot * Lay::STAGE;
-      if (!(ok = mbar_wait(bar(Lay::B_QF + slot), (it / NST) & 1, abort_flag))) break;
+    bool ok = true;
+    if (leader) {
+      ok = mbar_wait(bar(Lay::B_A), 0, abort_flag);
       tc_fence_after();
-      issue_xt(Lay::T_S, Lay::T_KH, st, Lay::QH, Lay::QL);   // S^T = K Q^T
-      issue_xt(Lay::T_DP, Lay::T_VH, st, Lay::YH, Lay::YL);  // dP^T = V dY^T
-      if (leader) tc_commit(bar(Lay::B_SP));
-      if (!(ok = mbar_wait(bar(Lay::B_P), it & 1, abort_flag))) break;
-      tc_fence_after();
-      // dV += P^T dY and dK += dS^T Q (c applied in the epilogue); S^T(it+1)
-      // and dP^T(it+1) then overwrite P^T_hi and dS^T_hi after these read
-      // them (the tensor pipe runs one thread's MMAs in issue order).
-      // (the accumulators restart at every kPromote-th step: the elementwise
-      // warps have moved their partial sums out before arriving on B_P)
-      issue_acc(Lay::T_DV, Lay::T_S, Lay::T_PL, st, Lay::YTH, Lay::YTL, it % kPromote == 0);
-      issue_acc(Lay::T_DK, Lay::T_DP, Lay::T_DSL, st, Lay::QTH, Lay::QTL, it % kPromote == 0);
-      if (leader) tc_commit(bar(Lay::B_QE + slot));
+      // S^T(0), dP^T(0); then per step t: S^T(t+1), dP^T(t+1), dV(t), dK(t).
+      // S^T(t+2) overwrites buffer t & 1 after dV(t), dK(t) have read it (the
+      // tensor pipe runs one thread's MMAs in issue order), and the elementwise
+      // warps write P^T(t+2) there only after S^T(t+2) is done.
+      if (ok && nsteps > 0 && (ok = mbar_wait(bar(Lay::B_QSF), 0, abort_flag))) {
+        tc_fence_after();
+        issue_step(0);
+        tc_commit(bar(Lay::B_SP));
+        tc_commit(bar(Lay::B_QSE));
+      }
+      for (int it = 0; it < nsteps && ok; ++it) {
+        const int b = it & 1;
+        if (it + 1 < nsteps) {
+          const int s1 = (it + 1) % NSS;
+          if (!(ok = mbar_wait(bar(Lay::B_QSF + s1), ((it + 1) / NSS) & 1, abort_flag))) break;
+          tc_fence_after();
+          issue_step(it + 1);
+          tc_commit(bar(Lay::B_SP + ((it + 1) & 1)));
+          tc_commit(bar(Lay::B_QSE + s1));
+        }
+        const int ts = it % NTS;
+        const uint64_t td = d0 + ((Lay::T_OFF + ts * Lay::THALF) >> 4);
+        const uint32_t buf = tmem + Lay::T_BUF + Lay::B_STRIDE * b;
+        // The accumulators restart at every kPromote-th step: the elementwise
+        // warps have moved the partial sums out before writing P^T(it).
+        const bool first = it % kPromote == 0;
+        if (!(ok = mbar_wait(bar(Lay::B_QTF + ts), (it / NTS) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait(bar(Lay::B_P + b), (it >> 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        // dV += P^T dY
+        issue_acc(tmem + Lay::T_DV, buf + Lay::B_S, buf + Lay::B_PL, td + (Lay::YTH >> 4),
+                  td + (Lay::YTL >> 4), first);
+        if (!(ok = mbar_wait(bar(Lay::B_DS + b), (it >> 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        // dK += dS^T Q (c applied when the rows leave TMEM)
+        issue_acc(tmem + Lay::T_DK, buf + Lay::B_DP, buf + Lay::B_DSL, td + (Lay::QTH >> 4),
+                  td + (Lay::QTL >> 4), first);
+        if ((it + 1) % kPromote == 0 && it + 1 < nsteps) tc_commit(bar(Lay::B_SEG));
+        tc_commit(bar(Lay::B_QTE + ts));
+      }
+      tc_commit(bar(Lay::B_DONE));
+      if (!ok) {
+        raise_status(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      // Every MMA issued has completed before TMEM is freed, abort or not.
+      tc_commit(bar(Lay::B_DRAIN));
     }
-    if (leader) tc_commit(bar(Lay::B_DONE));
     __syncwarp();
-    if (!ok && leader) {
-      raise_status(p.status, kStatusTimeout);
-      *abort_flag = 1;
-    }
-    if (leader) tc_commit(bar(Lay::B_DRAIN));
-    mbar_wait(bar(Lay::B_DRAIN), 0, abort_flag);
+    mbar_wait_inflight(bar(Lay::B_DRAIN), 0);
   } else {
     // Elementwise: thread = key j = k0 + r (TMEM lane r); its 32 columns of a
     // step are the step's queries.
@@ -411,9 +553,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j = k0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const size_t jrow = (static_cast<size_t>(bh) * nk + (j < nk ? j : 0)) * kD;
-    row_to_tmem(p.K + jrow, j < nk, tmem + lane_off + Lay::T_KH);
-    row_to_tmem(p.V + jrow, j < nk, tmem + lane_off + Lay::T_VH);
+    row_split_tmem_smem(p.K + jrow, j < nk, tmem + lane_off + Lay::T_KH, smem + Lay::KLO_OFF, r);
+    row_split_tmem_smem(p.V + jrow, j < nk, tmem + lane_off + Lay::T_VH, smem + Lay::VLO_OFF, r);
     tmem_st_wait();
+    fence_proxy_async_smem();  // the lo tiles are read by the tensor core
     tc_fence_before();
     mbar_arrive(bar(Lay::B_A));
     const float sl2 = p.sl2;
@@ -451,20 +594,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (int it = 0; it < nsteps; ++it) {
       const int q0 = (s_begin + it) * kStep;
-      const uint32_t allow = col_allow(p, j, q0);  // needs no product: before the wait
-      const float* dvec = reinterpret_cast<const float*>(smem + Lay::VEC_OFF + (it % NST) * 256);
-      const float* lvec = dvec + 32;
-      if (!(ok = mbar_wait(bar(Lay::B_SP), it & 1, abort_flag))) break;
+      const int b = it & 1, vs = it % NV;
+      const uint32_t tb = tmem + lane_off + Lay::T_BUF + Lay::B_STRIDE * b;
+      const uint32_t allow = col_allow(p, j, q0);  // needs no product: before the waits
+      if (!(ok = wait_warp(Lay::B_VF + vs, (it / NV) & 1))) break;
+      if (!(ok = wait_warp(Lay::B_SP + b, (it >> 1) & 1))) break;
       tc_fence_after();
-      // S^T(it) done means dV(it-1), dK(it-1) are too (issue order): move the
-      // partial sums of the last kPromote steps out before dV(it) restarts them.
-      if (it > 0 && it % kPromote == 0) move_out(it == kPromote);
-      uint32_t s[32], dp[32], lo[32];
-      tmem_ld32(tmem + lane_off + Lay::T_S, s);
-      tmem_ld32(tmem + lane_off + Lay::T_DP, dp);
+      if (it > 0 && it % kPromote == 0) {
+        // dV, dK of the last kPromote steps are done: move them out before
+        // dV(it), dK(it) restart the accumulators.
+        if (!(ok = wait_warp(Lay::B_SEG, (it / kPromote - 1) & 1))) break;
+        tc_fence_after();
+        move_out(it == kPromote);
+      }
+      const float* dvec = reinterpret_cast<const float*>(smem + Lay::VEC_OFF + vs * 256);
+      const float* lvec = dvec + 32;
+      uint32_t s[32], dp[32], lo[32], t2[32];
+      tmem_ld32(tb + Lay::B_S, s);
+      tmem_ld32(tb + Lay::B_S + kStep, lo);
+      tmem_ld32(tb + Lay::B_DP, dp);
+      tmem_ld32(tb + Lay::B_DP + kStep, t2);
       tmem_ld_wait();
       reg_fence(s);
+      reg_fence(lo);
       reg_fence(dp);
+      reg_fence(t2);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {  // the two parts of S^T and of dP^T
+        s[e] = __float_as_uint(__uint_as_float(s[e]) + __uint_as_float(lo[e]));
+        dp[e] = __float_as_uint(__uint_as_float(dp[e]) + __uint_as_float(t2[e]));
+      }
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
         const float4 l4 = *reinterpret_cast<const float4*>(lvec + e);
@@ -478,20 +637,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           dp[e + u] = __float_as_uint(pij * (__uint_as_float(dp[e + u]) - da[u]));
         }
       }
+      mbar_arrive(bar(Lay::B_VE + vs));  // the vectors are in registers
       split32(s, lo);
-      tmem_st32(tmem + lane_off + Lay::T_S, s);
-      tmem_st32(tmem + lane_off + Lay::T_PL, lo);
-      split32(dp, lo);
-      tmem_st32(tmem + lane_off + Lay::T_DP, dp);
-      tmem_st32(tmem + lane_off + Lay::T_DSL, lo);
+      tmem_st32(tb + Lay::B_S, s);
+      tmem_st32(tb + Lay::B_PL, lo);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(Lay::B_P));
+      mbar_arrive(bar(Lay::B_P + b));
+      split32(dp, lo);
+      tmem_st32(tb + Lay::B_DP, dp);
+      tmem_st32(tb + Lay::B_DSL, lo);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(Lay::B_DS + b));
     }
     // Epilogue: the last partial dV_j, c dK_j (zeros when no query reaches the
-    // block).  The TMEM reads are warp-collective: the predicate is the warp's.
-    const bool have = __all_sync(
-        0xFFFFFFFFu, ok && nsteps > 0 && mbar_wait(bar(Lay::B_DONE), 0, abort_flag));
+    // block).  The TMEM reads are warp-collective: ok and the wait are uniform.
+    const bool have = ok && nsteps > 0 && wait_warp(Lay::B_DONE, 0);
     if (ok && nsteps > 0 && !have) ok = false;
     tc_fence_after();
     if (have) {
@@ -602,6 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint64_t keep = policy_evict_last();  // read by every query block of the slice
     bool ok = true;
+    int fills = 0;
     for (int it = 0; it < nsteps && ok; ++it) {
       const int slot = it % NST, fill = it / NST;
       if (fill >= 1 && !(ok = mbar_wait(bar(Lay::B_KE + slot), (fill - 1) & 1, abort_flag))) break;
@@ -619,15 +782,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(st + Lay::KTH, &p.tkth, fb, k0, 0, bh, keep);
         tma_load_3d(st + Lay::KTL, &p.tktl, fb, k0, 0, bh, keep);
       }
+      ++fills;
     }
     __syncwarp();
     if (!ok && leader) {
       raise_status(p.status, kStatusTimeout);
       *abort_flag = 1;
     }
-    for (int u = 0; u < NST && u < nsteps; ++u) {
-      const int i = nsteps - 1 - u;
-      mbar_wait(bar(Lay::B_KF + i % NST), (i / NST) & 1, abort_flag);
+    // Never leave with copies in flight: the last fill of every stage.
+    for (int u = 0; u < NST && u < fills; ++u) {
+      const int i = fills - 1 - u;
+      mbar_wait_inflight(bar(Lay::B_KF + i % NST), (i / NST) & 1);
     }
   } else if (warp == kWarpMMA) {
     const bool leader = elect_one();
@@ -702,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
     }
     if (leader) tc_commit(bar(Lay::B_DRAIN));
-    mbar_wait(bar(Lay::B_DRAIN), 0, abort_flag);
+    mbar_wait_inflight(bar(Lay::B_DRAIN), 0);
   } else {
     // Elementwise: thread = query row i = q0 + r (TMEM lane r); its 32 columns
     // of a step are the step's keys.

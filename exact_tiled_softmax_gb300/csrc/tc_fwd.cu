@@ -353,11 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
             const int slot = it % NS, phase = (it / NS) & 1;
-            ++it;
             if (!mbar_wait(bar(Lay::B_KVE + slot), phase ^ 1, abort_flag)) {
               ok = false;
               break;
             }
+            ++it;  // fills issued
             const uint32_t dst = sbase + Lay::SLOT_OFF + slot * Lay::SLOT;
             if (leader) {
               if (kv == 0) {
@@ -388,9 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       // every slot (fill i = it - 1 - u went to slot i % NS) and for the last Q.
       for (int u = 0; u < NS && u < it; ++u) {
         const int i = it - 1 - u;
-        mbar_wait(bar(Lay::B_KVF + i % NS), (i / NS) & 1, abort_flag);
+        mbar_wait_inflight(bar(Lay::B_KVF + i % NS), (i / NS) & 1);
       }
-      if (q_loads > 0) mbar_wait(bar(Lay::B_Q), (q_loads - 1) & 1, abort_flag);
+      if (q_loads > 0) mbar_wait_inflight(bar(Lay::B_Q), (q_loads - 1) & 1);
     } else if (warp == kWarpMMA) {
       constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16(kBM, V, false, true);
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       }
       // Drain: every MMA issued by this warp has completed before teardown.
       commit(Lay::B_DRAIN);
-      mbar_wait(bar(Lay::B_DRAIN), 0, abort_flag);
+      mbar_wait_inflight(bar(Lay::B_DRAIN), 0);
     }
   } else {
     // Softmax warpgroups: thread = one query row of tile X.

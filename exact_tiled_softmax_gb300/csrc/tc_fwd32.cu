@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
     }
     for (int s = 0; s < NS; ++s)
-      if (last_phase[s] >= 0) mbar_wait(bar(Lay::B_KVF + s), last_phase[s], abort_flag);
+      if (last_phase[s] >= 0) mbar_wait_inflight(bar(Lay::B_KVF + s), last_phase[s]);
   } else if (warp == kWarpMMA) {
     const bool leader = elect_one();
     constexpr uint32_t kIdS = idesc_tf32(kBM, kBN);
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
     }
     commit(Lay::B_DRAIN);
-    mbar_wait(bar(Lay::B_DRAIN), 0, abort_flag);
+    mbar_wait_inflight(bar(Lay::B_DRAIN), 0);
   } else {
     // Softmax warps: thread = query row r of the tile.
     const int r = warp * 32 + lane;

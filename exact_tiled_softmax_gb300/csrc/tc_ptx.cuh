@@ -67,6 +67,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// The same bounded wait for work already in flight (TMA copies, issued MMAs),
+// which completes by itself: no abort cuts it short, so that a CTA that gave
+// up still frees its shared memory and TMEM only after its own copies and
+// products have landed.
+__device__ __forceinline__ bool mbar_wait_inflight(uint32_t bar, uint32_t parity,
+                                                   uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int k = 0; k < 32; ++k)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // One lane of a converged warp (the same lane each time) returns true.
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;

@@ -624,32 +624,58 @@ def atomic_kernel(n_blocks, ew_warps=2, drain_warps=2):
 # ---------------------------------------------------------------------------
 # 3xTF32 reverse pass (tc_bwd32.cu): one CTA per block, steps of 32 rows.
 # ---------------------------------------------------------------------------
-def kv32_kernel(n_steps, ew_warps=2, NST=3):
-    """dK/dV kernel: the elementwise warps write K, V to TMEM (B_A), then per
-    step wait for S^T, dP^T (B_SP) and write P^T, dS^T (B_P)."""
+def kv32_kernel(n_steps, ew_warps=2, NSS=3, NTS=2, NV=4, promote=3):
+    """dK/dV kernel: the elementwise warps write K, V (B_A); the TMA warp fills
+    S halves (QSF / QSE) and vector slots (VF / VE) one step ahead of T halves
+    (QTF / QTE); S^T, dP^T double-buffered (SP per buffer); P^T and dS^T per
+    buffer (P, DS); S^T(t+1), dP^T(t+1) before dV(t), dK(t); every `promote`
+    steps the elementwise warps wait for the segment's dV, dK (SEG) before
+    moving them out (the kernel's interval is 32: a short one here so that
+    SEG turns over within a few steps)."""
     W = ew_warps
     need = defaultdict(lambda: 1)
-    need["A"] = need["P"] = W
+    for name in ["A", "P0", "P1", "DS0", "DS1"] + [f"VE{s}" for s in range(NV)]:
+        need[name] = W
     k = n_steps
 
     def tma():
+        def load_s(s):
+            yield from _ring_fill(f"QSE{s % NSS}", f"QSF{s % NSS}", s // NSS)
+            yield from _ring_fill(f"VE{s % NV}", f"VF{s % NV}", s // NV)
+        if k > 0:
+            yield from load_s(0)
         for it in range(k):
-            yield from _ring_fill(f"QE{it % NST}", f"QF{it % NST}", it // NST)
-        for u in range(min(NST, k)):
-            i = k - 1 - u
-            yield ("wait", f"QF{i % NST}", i // NST)
+            if it + 1 < k:
+                yield from load_s(it + 1)
+            yield from _ring_fill(f"QTE{it % NTS}", f"QTF{it % NTS}", it // NTS)
+        for full, m in (("QSF", NSS), ("QTF", NTS), ("VF", NV)):
+            for u in range(min(m, k)):
+                i = k - 1 - u
+                yield ("wait", f"{full}{i % m}", i // m)
 
     def mma():
         yield ("wait", "A", 0)
+        if k > 0:
+            yield ("wait", "QSF0", 0)
+            yield ("mma", "SdP0")
+            yield ("commit", "SP0")
+            yield ("commit", "QSE0")
         for it in range(k):
-            yield ("wait", f"QF{it % NST}", it // NST)
-            yield ("mma", "S")
-            yield ("mma", "dP")
-            yield ("commit", "SP")
-            yield ("wait", "P", it)
-            yield ("mma", "dV")
-            yield ("mma", "dK")
-            yield ("commit", f"QE{it % NST}")
+            b = it & 1
+            if it + 1 < k:
+                s1 = (it + 1) % NSS
+                yield ("wait", f"QSF{s1}", (it + 1) // NSS)
+                yield ("mma", f"SdP{it + 1}")
+                yield ("commit", f"SP{(it + 1) & 1}")
+                yield ("commit", f"QSE{s1}")
+            yield ("wait", f"QTF{it % NTS}", it // NTS)
+            yield ("wait", f"P{b}", it >> 1)
+            yield ("mma", f"dV{it}")
+            yield ("wait", f"DS{b}", it >> 1)
+            yield ("mma", f"dK{it}")
+            if (it + 1) % promote == 0 and it + 1 < k:
+                yield ("commit", "SEG")
+            yield ("commit", f"QTE{it % NTS}")
         yield ("commit", "DONE")
         yield ("commit", "DRAIN")
         yield ("wait", "DRAIN", 0)
@@ -657,8 +683,14 @@ def kv32_kernel(n_steps, ew_warps=2, NST=3):
     def ew():
         yield ("arrive", "A")
         for it in range(k):
-            yield ("wait", "SP", it)
-            yield ("arrive", "P")
+            b, vs = it & 1, it % NV
+            yield ("wait", f"VF{vs}", it // NV)
+            yield ("wait", f"SP{b}", it >> 1)
+            if it > 0 and it % promote == 0:
+                yield ("wait", "SEG", it // promote - 1)
+            yield ("arrive", f"VE{vs}")
+            yield ("arrive", f"P{b}")
+            yield ("arrive", f"DS{b}")
         if k > 0:
             yield ("wait", "DONE", 0)
 

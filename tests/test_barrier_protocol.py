@@ -91,11 +91,16 @@ def test_model_catches_a_missing_wait(factory, drop):
 def test_fp32_reverse_kernels_protocol_holds():
     steps = lambda rnd: rnd.randint(0, 11)
     assert _search(bm.kv32_kernel, steps, 61) == []
+    assert _search(bm.kv32_kernel, steps, 65, NSS=2, NV=2, promote=1, ew_warps=3) == []
     assert _search(bm.q32_kernel, steps, 62) == []
     assert _search(bm.q32_kernel, steps, 63, NST=2, ew_warps=3) == []
 
 
-@pytest.mark.parametrize("factory,drop", [(bm.kv32_kernel, "QE0"), (bm.q32_kernel, "SP0"),
-                                          (bm.q32_kernel, "DS0")])
-def test_fp32_reverse_model_catches_a_missing_wait(factory, drop):
-    assert _search(factory, lambda rnd: rnd.randint(3, 11), 64, n=200, skip_waits={drop})
+@pytest.mark.parametrize("factory,drop,kw", [
+    (bm.kv32_kernel, "QSE0", {}), (bm.kv32_kernel, "QTE0", {}), (bm.kv32_kernel, "SP0", {}),
+    # with four vector slots the T-half ring already orders a slot's reuse;
+    # with two, the vector ring's own release is what does
+    (bm.kv32_kernel, "VE0", {"NV": 2}),
+    (bm.q32_kernel, "SP0", {}), (bm.q32_kernel, "DS0", {})])
+def test_fp32_reverse_model_catches_a_missing_wait(factory, drop, kw):
+    assert _search(factory, lambda rnd: rnd.randint(3, 11), 64, n=200, skip_waits={drop}, **kw)

@@ -2,7 +2,8 @@
 
 Normwise = max|x - ref| / max|ref|:
   fp32 inputs  Y normwise <= 1e-5, dQ/dK/dV normwise <= 1e-4
-  bf16 inputs  Y max abs err <= 1e-2 plus half a bf16 ulp of the oracle value,
+  bf16 inputs  Y max abs err <= 1e-2 plus half a bf16 ulp of the oracle value
+               (and <= 1e-2 with no allowance wherever |ref| < 2),
                each gradient max abs err <= 2e-2 * max|ref|
   both         L max abs err <= 1e-4 (rows with an empty allowed set: exactly -inf)
 A gradient that is identically zero in exact arithmetic has its denominator
@@ -49,6 +50,13 @@ def compare(dtype, got, ref, heads=None):
             excess = np.abs(g - r) - half_ulp_bf16(r)
             err = float(excess.max()) if excess.size else 0.0
             bound = tol["y"]
+            # Where |Y| < 2 the bf16 rounding is at most 2^-8: there the plain
+            # 1e-2 bar holds without the half-ulp allowance.
+            small = np.abs(r) < 2.0
+            if small.any():
+                plain = float(np.abs(g - r)[small].max())
+                assert plain <= tol["y"], f"Y (|ref| < 2): max abs err {plain:.3e} > {tol['y']}"
+                errs["Y_plain_small"] = (plain, tol["y"])
         elif key == "Y":
             err = float(np.abs(g - r).max())
             bound = tol["y"] * float(np.abs(r).max())
