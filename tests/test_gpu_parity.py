@@ -24,7 +24,7 @@ import torch
 
 import workloads
 from oracle import dense, masks
-from tolerances import TOL, compare, half_ulp_bf16  # noqa: F401
+from tolerances import TOL, compare, half_ulp_bf16, single_key_cancellation  # noqa: F401
 
 pytestmark = pytest.mark.gpu
 
@@ -117,7 +117,13 @@ def test_edge_lengths(ex, n, dtype):
     for mask in ("none", "causal"):
         w = workloads.small(1, 1, n, 64, 64, dtype, mask, 0.125, seed=n)
         x = workloads.make_inputs(w)
-        compare(dtype, run_gpu(ex, w, x), oracle_all(w, x))
+        got, ref = run_gpu(ex, w, x), oracle_all(w, x)
+        if dtype == "f32" and n == 1:
+            # dQ = dK = 0 exactly; the computed ones are a cancellation's rounding.
+            compare(dtype, got, {k: ref[k] for k in ("Y", "L", "dV")})
+            single_key_cancellation(got, *x.as_f64(), w.scale)
+        else:
+            compare(dtype, got, ref)
 
 
 def test_window_wider_than_n_is_causal(ex):

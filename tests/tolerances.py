@@ -8,6 +8,10 @@ Normwise = max|x - ref| / max|ref|:
   both         L max abs err <= 1e-4 (rows with an empty allowed set: exactly -inf)
 A gradient that is identically zero in exact arithmetic has its denominator
 floored at 1e-3 x the largest max|ref| over dQ, dK, dV of the same call.
+With fp32 inputs and a single key (n = 1) dQ and dK are zero in exact
+arithmetic and the computed ones are the rounding of dP - delta, a difference of
+two width-long fp32 dot products that cancel: they are held element by element
+to 2^-18 x sum |dY| |V| times c |K| (dQ) or c |Q| (dK) instead.
 """
 import numpy as np
 import torch
@@ -67,3 +71,16 @@ def compare(dtype, got, ref, heads=None):
         errs[key] = (err, bound)
         assert err <= bound, f"{key}: max abs err {err:.3e} > bound {bound:.3e}"
     return errs
+
+
+def single_key_cancellation(got, Q, K, V, dY, c):
+    """fp32, one key per slice: p = 1, so gamma = dP - delta = 0 in exact
+    arithmetic ("Exact tiled softmax attention with block-recomputed
+    vector-Jacobian products", Reverse procedure), dQ = dK = 0 and dV = dY.
+    The computed dQ and dK are the rounding of that cancellation; Q, K, V, dY
+    are float64 arrays [..., 1, width]."""
+    cancel = 2.0 ** -18 * np.sum(np.abs(dY) * np.abs(V), axis=-1, keepdims=True)
+    dq, dk, dv = (_np(got[k]).reshape(r.shape) for k, r in (("dQ", Q), ("dK", K), ("dV", V)))
+    assert np.all(np.abs(dq) <= c * np.abs(K) * cancel), "dQ beyond the cancellation bound"
+    assert np.all(np.abs(dk) <= c * np.abs(Q) * cancel), "dK beyond the cancellation bound"
+    assert np.allclose(dv, dY, rtol=1e-6, atol=0), "dV differs from dY"
