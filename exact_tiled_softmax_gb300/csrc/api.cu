@@ -166,9 +166,9 @@ int exattn_set_path(int path) {
 }
 
 // Forward workspace: the status word, plus for fp32 shapes that the 3xTF32
-// tensor-core forward takes (d = v in {64, 128}) the split copies of K and V.
+// tensor-core forward takes (d, v <= 128, multiples of 4) the split copies of K and V.
 static size_t fwd_ws_bytes(const Dims& s) {
-  if (s.dtype != EXATTN_F32 || s.d != s.v || (s.d != 64 && s.d != 128)) return kStatusBytes;
+  if (s.dtype != EXATTN_F32 || !tc_fwd32_shape(s.d, s.v)) return kStatusBytes;
   Problem p = make_problem(s, 1.f, EXATTN_MASK_NONE, 0, nullptr);
   return kStatusBytes + split32_bytes(p);
 }

@@ -119,6 +119,7 @@ struct Split32 {
   float* vtl;
   int ldt;     // nk rounded up to 32
 };
+bool tc_fwd32_shape(int d, int v);  // widths the 3xTF32 forward takes (fp32)
 bool tc_fwd32_supported(const Problem& p);
 size_t split32_bytes(const Problem& p);
 Split32 split32_layout(const Problem& p, void* base);

@@ -1,4 +1,7 @@
-// Register-tiled SIMT reverse pass (fp32 arithmetic) for d, v in {64, 128}.
+// Register-tiled SIMT reverse pass (fp32 arithmetic) for d, v <= 128.  Widths
+// other than 64 and 128 (multiples of 4) run on the kernel of width 64 or 128:
+// rows are loaded with their own widths and zero-filled, and only the true
+// columns are stored.
 //
 // The Reverse procedure of "Exact tiled softmax attention with block-
 // recomputed vector-Jacobian products": per key block, for every query tile
@@ -78,26 +81,27 @@ __global__ void __launch_bounds__(kThreads, 1) simt_bwd_rt_kernel(BwdArgs a) {
   const int n = p.n, nk = p.nk, off = nk - n;
   const int bh = blockIdx.y, j0 = blockIdx.x * kBK;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-  const T* Qh = static_cast<const T*>(a.Q) + (size_t)bh * n * D;
-  const T* Kh = static_cast<const T*>(a.K) + (size_t)bh * nk * D;
-  const T* Vh = static_cast<const T*>(a.V) + (size_t)bh * nk * V;
-  const T* Yh = static_cast<const T*>(a.dY) + (size_t)bh * n * V;
+  const int dw = p.d, vw = p.v;  // widths in memory (<= D, V)
+  const T* Qh = static_cast<const T*>(a.Q) + (size_t)bh * n * dw;
+  const T* Kh = static_cast<const T*>(a.K) + (size_t)bh * nk * dw;
+  const T* Vh = static_cast<const T*>(a.V) + (size_t)bh * nk * vw;
+  const T* Yh = static_cast<const T*>(a.dY) + (size_t)bh * n * vw;
   const float* Lh = a.lse2 + (size_t)bh * a.npad;
   const float* Dh = a.delta + (size_t)bh * a.npad;
-  float* dQh = a.dQacc + (size_t)bh * n * D;
+  float* dQh = a.dQacc + (size_t)bh * n * dw;
   MaskView mask{p.mask_kind, nk, off, p.window, p.words_per_row, p.bitmask};
   const float c = p.scale, sl2 = p.scale * kLog2e;
 
   // K, V of the block: transposed (S, dP operands) and K row-major (dQ operand).
   for (int idx = tid; idx < kBK * D; idx += kThreads) {
     const int r = idx / D, col = idx - r * D, g = j0 + r;
-    const float x = g < nk ? Elem<T>::load(Kh + (size_t)g * D + col) : 0.f;
+    const float x = g < nk && col < dw ? Elem<T>::load(Kh + (size_t)g * dw + col) : 0.f;
     Kt[col * LK + r] = x;
     Ks[r * (D + 4) + col] = x;
   }
   for (int idx = tid; idx < kBK * V; idx += kThreads) {
     const int r = idx / V, col = idx - r * V, g = j0 + r;
-    Vt[col * LK + r] = g < nk ? Elem<T>::load(Vh + (size_t)g * V + col) : 0.f;
+    Vt[col * LK + r] = g < nk && col < vw ? Elem<T>::load(Vh + (size_t)g * vw + col) : 0.f;
   }
 
   float dv[4][4 * CV], dk[4][4 * CD];
@@ -133,13 +137,13 @@ __global__ void __launch_bounds__(kThreads, 1) simt_bwd_rt_kernel(BwdArgs a) {
     __syncthreads();  // the previous tile's operands are no longer read
     for (int idx = tid; idx < kBQ * D; idx += kThreads) {
       const int r = idx / D, col = idx - r * D, g = q0 + r;
-      const float x = g < n ? Elem<T>::load(Qh + (size_t)g * D + col) : 0.f;
+      const float x = g < n && col < dw ? Elem<T>::load(Qh + (size_t)g * dw + col) : 0.f;
       Qt[col * LQ + r] = x;
       Qs[r * (D + 4) + col] = x;
     }
     for (int idx = tid; idx < kBQ * V; idx += kThreads) {
       const int r = idx / V, col = idx - r * V, g = q0 + r;
-      const float x = g < n ? Elem<T>::load(Yh + (size_t)g * V + col) : 0.f;
+      const float x = g < n && col < vw ? Elem<T>::load(Yh + (size_t)g * vw + col) : 0.f;
       Yt[col * LQ + r] = x;
       Ys[r * (V + 4) + col] = x;
     }
@@ -260,8 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1) simt_bwd_rt_kernel(BwdArgs a) {
         if (gi < n)
 #pragma unroll
           for (int h = 0; h < CD; ++h)
-            red_add_v4(dQh + (size_t)gi * D + 64 * h + 4 * tx, c * acc[u][4 * h],
-                       c * acc[u][4 * h + 1], c * acc[u][4 * h + 2], c * acc[u][4 * h + 3]);
+            if (64 * h + 4 * tx < dw)  // dw is a multiple of 4: the 4 columns are all in
+              red_add_v4(dQh + (size_t)gi * dw + 64 * h + 4 * tx, c * acc[u][4 * h],
+                         c * acc[u][4 * h + 1], c * acc[u][4 * h + 2], c * acc[u][4 * h + 3]);
       }
     }
   }
@@ -271,16 +276,19 @@ __global__ void __launch_bounds__(kThreads, 1) simt_bwd_rt_kernel(BwdArgs a) {
   for (int r = 0; r < 4; ++r) {
     const int j = j0 + 4 * ty + r;
     if (j >= nk) continue;
-    T* dKr = static_cast<T*>(a.dK) + ((size_t)bh * nk + j) * D;
-    T* dVr = static_cast<T*>(a.dV) + ((size_t)bh * nk + j) * V;
+    T* dKr = static_cast<T*>(a.dK) + ((size_t)bh * nk + j) * dw;
+    T* dVr = static_cast<T*>(a.dV) + ((size_t)bh * nk + j) * vw;
 #pragma unroll
     for (int h = 0; h < CD; ++h)
+      if (64 * h + 4 * tx < dw)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) Elem<T>::store(dKr + 64 * h + 4 * tx + e, c * dk[r][4 * h + e]);
+        for (int e = 0; e < 4; ++e)
+          Elem<T>::store(dKr + 64 * h + 4 * tx + e, c * dk[r][4 * h + e]);
 #pragma unroll
     for (int h = 0; h < CV; ++h)
+      if (64 * h + 4 * tx < vw)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) Elem<T>::store(dVr + 64 * h + 4 * tx + e, dv[r][4 * h + e]);
+        for (int e = 0; e < 4; ++e) Elem<T>::store(dVr + 64 * h + 4 * tx + e, dv[r][4 * h + e]);
   }
 }
 
@@ -297,19 +305,20 @@ cudaError_t rt_launch(const BwdArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Kernel widths: 64 for d (or v) <= 64, 128 above.
 template <typename T>
 cudaError_t rt_dispatch(const BwdArgs& a, cudaStream_t s) {
-  const int d = a.p.d, v = a.p.v;
-  if (d == 128 && v == 128) return rt_launch<T, 128, 128>(a, s);
-  if (d == 64 && v == 64) return rt_launch<T, 64, 64>(a, s);
-  if (d == 128) return rt_launch<T, 128, 64>(a, s);
+  const bool d64 = a.p.d <= 64, v64 = a.p.v <= 64;
+  if (!d64 && !v64) return rt_launch<T, 128, 128>(a, s);
+  if (d64 && v64) return rt_launch<T, 64, 64>(a, s);
+  if (!d64) return rt_launch<T, 128, 64>(a, s);
   return rt_launch<T, 64, 128>(a, s);
 }
 
 }  // namespace
 
 bool simt_bwd_rt_supported(const Problem& p) {
-  return (p.d == 64 || p.d == 128) && (p.v == 64 || p.v == 128);
+  return p.d >= 4 && p.v >= 4 && p.d <= 128 && p.v <= 128 && p.d % 4 == 0 && p.v % 4 == 0;
 }
 
 cudaError_t launch_simt_bwd_rt(const BwdArgs& a, cudaStream_t s) {

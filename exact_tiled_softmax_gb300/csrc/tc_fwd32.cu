@@ -65,6 +65,7 @@ struct Fwd32Params {
   CUtensorMap tkh, tkl, tvh, tvl;
   const float* Q;
   int n, nk, off, BH, mask_kind, window, words_per_row;
+  int dw, vw;  // columns of Q, K and of V, Y in memory (multiples of 4, <= the kernel's D, V)
   const uint32_t* bits;
   float sl2;  // scale * log2(e), > 0
   float* Y;
@@ -346,13 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // past the last row.
     {
       const float4* qrow = reinterpret_cast<const float4*>(
-          p.Q + (static_cast<size_t>(bh) * n + (i < n ? i : 0)) * D);
+          p.Q + (static_cast<size_t>(bh) * n + (i < n ? i : 0)) * p.dw);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t hi[32];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float4 x = i < n ? __ldg(qrow + 8 * c + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 x = (i < n && 32 * c + 4 * e < p.dw) ? __ldg(qrow + 8 * c + e)
+                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
           const float xs[4] = {x.x, x.y, x.z, x.w};
           float lo4[4];
 #pragma unroll
@@ -473,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const bool valid = i < n;
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    float* yrow = p.Y + (static_cast<size_t>(bh) * n + (valid ? i : 0)) * V;
+    float* yrow = p.Y + (static_cast<size_t>(bh) * n + (valid ? i : 0)) * p.vw;
 #pragma unroll
     for (int ch = 0; ch < V / 32; ++ch) {
       uint32_t o[32];
@@ -497,9 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float4* dst = reinterpret_cast<float4*>(yrow + ch * 32);
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
-                               __uint_as_float(o[4 * e + 2]) * inv,
-                               __uint_as_float(o[4 * e + 3]) * inv);
+          if (32 * ch + 4 * e < p.vw)  // no column past Y's width
+            dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv,
+                                 __uint_as_float(o[4 * e + 1]) * inv,
+                                 __uint_as_float(o[4 * e + 2]) * inv,
+                                 __uint_as_float(o[4 * e + 3]) * inv);
       }
     }
     if (valid) {
@@ -551,12 +555,16 @@ template <int D>
 cudaError_t launch_d(const FwdArgs& a, const Split32& ws, cudaStream_t s) {
   const Problem& pr = a.p;
   Fwd32Params p;
-  if (!make_tmap_f32(&p.tkh, ws.kh, D, D, pr.nk, pr.BH, kBN) ||
-      !make_tmap_f32(&p.tkl, ws.kl, D, D, pr.nk, pr.BH, kBN) ||
-      !make_tmap_f32(&p.tvh, ws.vth, pr.nk, ws.ldt, D, pr.BH, D) ||
-      !make_tmap_f32(&p.tvl, ws.vtl, pr.nk, ws.ldt, D, pr.BH, D))
+  // The split arrays keep the true widths; the kernel's loads read zeros for
+  // the columns of K and the rows of V^T past them.
+  if (!make_tmap_f32(&p.tkh, ws.kh, pr.d, pr.d, pr.nk, pr.BH, kBN) ||
+      !make_tmap_f32(&p.tkl, ws.kl, pr.d, pr.d, pr.nk, pr.BH, kBN) ||
+      !make_tmap_f32(&p.tvh, ws.vth, pr.nk, ws.ldt, pr.v, pr.BH, D) ||
+      !make_tmap_f32(&p.tvl, ws.vtl, pr.nk, ws.ldt, pr.v, pr.BH, D))
     return cudaErrorInvalidValue;
   p.Q = static_cast<const float*>(a.Q);
+  p.dw = pr.d;
+  p.vw = pr.v;
   p.n = pr.n;
   p.nk = pr.nk;
   p.off = pr.nk - pr.n;
@@ -609,8 +617,15 @@ bool make_tmap_f32(CUtensorMap* m, const void* base, int inner, int ld, int rows
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Widths up to 128 in steps of 4 run on the kernel of width 64 or 128 (zero
+// padding, as for bf16): Q rows are loaded and Y rows stored with their own
+// widths, and the split copies of K and V keep theirs.
+bool tc_fwd32_shape(int d, int v) {
+  return d >= 4 && v >= 4 && d <= 128 && v <= 128 && d % 4 == 0 && v % 4 == 0;
+}
+
 bool tc_fwd32_supported(const Problem& p) {
-  if (p.dtype != kF32 || p.d != p.v || (p.d != 64 && p.d != 128)) return false;
+  if (p.dtype != kF32 || !tc_fwd32_shape(p.d, p.v)) return false;
   if (!(p.scale > 0.f) || p.drop_t != 0) return false;
   if (p.mask_kind == kMaskBitmask && p.nk > kMaxKT * kBN) return false;
   return tmap_encoder() != nullptr;
@@ -638,7 +653,7 @@ Split32 split32_layout(const Problem& p, void* base) {
 }
 
 cudaError_t launch_tc_fwd32(const FwdArgs& a, const Split32& ws, cudaStream_t s) {
-  return a.p.d == 128 ? launch_d<128>(a, ws, s) : launch_d<64>(a, ws, s);
+  return a.p.d <= 64 && a.p.v <= 64 ? launch_d<64>(a, ws, s) : launch_d<128>(a, ws, s);
 }
 
 }  // namespace exattn

@@ -96,11 +96,14 @@ typedef struct exattn_shape {
  * AUTO uses the tcgen05/TMA/TMEM kernels where the shape allows (bf16 with
  * d, v <= 128 and multiples of 8: widths other than 64 and 128 run on the
  * width-64 or width-128 kernels, whose TMA loads fill the missing columns with
- * zeros and whose stores leave them out; for fp32 with d = v in {64, 128} and a positive scale
- * the forward runs 3xTF32 on the tensor cores: each operand split into two
- * tf32 parts, three products per product, partial sums promoted to fp32 every
- * key block) and the SIMT fp32 kernels otherwise; its reverse pass is a
- * key-major dK/dV kernel plus a query-major dQ kernel.  SIMT forces the SIMT
+ * zeros and whose stores leave them out; for fp32 with d, v <= 128 and multiples
+ * of 4, a positive scale and no dropout the forward runs 3xTF32 on the tensor
+ * cores, zero-padded the same way: each operand split into two tf32 parts,
+ * three products per product, partial sums promoted to fp32 every key block;
+ * the fp32 reverse pass runs 3xTF32 for d = v = 64 without dropout) and the
+ * SIMT fp32 kernels otherwise (register-tiled for d, v <= 128 and multiples of
+ * 4); the bf16 reverse pass is a key-major dK/dV kernel plus a query-major dQ
+ * kernel.  SIMT forces the SIMT
  * kernels for every shape.  ATOMIC_DQ is AUTO with the other reverse form on
  * the tensor cores: one key-major kernel that adds dQ into an fp32 accumulator
  * with vector reductions (kept for measurement; bf16 d = v in {64, 128} only,
@@ -111,7 +114,7 @@ int exattn_set_path(int path);
 
 /* Workspace bytes that attn_fwd / attn_bwd need for this shape and mask kind.
  * The workspace holds the device status word (first 256 bytes); for an fp32
- * forward with d = v in {64, 128} (the 3xTF32 tensor-core forward) also the
+ * forward with d, v <= 128, multiples of 4 (the 3xTF32 tensor-core forward) also the
  * tf32 hi / lo split of K and V (4 copies of K's and V's size, V transposed
  * with rows padded to 32 keys); for the reverse pass delta [B][H][n], L log2(e)
  * [B][H][n] and the fp32 dQ accumulator [B][H][n][d].  Every size is linear in

@@ -1,5 +1,5 @@
-"""GPU parity of the 3xTF32 tensor-core forward for fp32 inputs (d = v in
-{64, 128}) against the float64 oracle, at the fp32 bar: Y normwise <= 1e-5,
+"""GPU parity of the 3xTF32 tensor-core forward for fp32 inputs (d, v <= 128,
+multiples of 4; widths other than 64 and 128 zero-padded) against the float64 oracle, at the fp32 bar: Y normwise <= 1e-5,
 L max abs <= 1e-4 (tests/tolerances.py).  The same cases also run the SIMT
 kernels, and the launch counter shows which path ran: the tensor-core forward
 is two launches (the K/V split and the kernel), the SIMT forward one."""
@@ -66,6 +66,47 @@ def test_fp32_forward_parity(ex, case, path):
     Yr, Lr = dense.forward_rect(Q.double().numpy(), K.double().numpy(), V.double().numpy(), c,
                                 kind, window, bm)
     compare("f32", dict(Y=y, L=L), dict(Y=Yr, L=Lr))
+
+
+PADDED = [
+    # (B, H, n, d, v, mask, window): widths that run zero-padded on the kernel of
+    # width 64 or 128, with their own row strides in memory
+    (2, 8, 1000, 80, 96, "bitmask", 0),    # the irregular workload's shape
+    (1, 2, 300, 48, 24, "causal", 0),      # width-64 kernel
+    (1, 1, 257, 100, 36, "window", 70),    # d above 64: width-128 kernel, v far below
+    (1, 1, 200, 4, 128, "none", 0),        # one 16-byte piece of Q, K
+]
+
+
+@pytest.mark.parametrize("path", ["auto", "simt"])
+@pytest.mark.parametrize("case", PADDED, ids=lambda c: "-".join(map(str, c)))
+def test_fp32_padded_widths_forward_and_reverse(ex, case, path):
+    """fp32 widths other than 64 and 128 (multiples of 4): the 3xTF32 forward and
+    the register-tiled SIMT reverse pass on zero-padded kernels, Y and L and the
+    gradients against the oracle at the fp32 bar; outputs NaN-filled first so
+    that a column left unwritten fails."""
+    B, H, n, d, v, mask, window = case
+    w = workloads.small(B, H, n, d, v, "f32", mask, 0.1, window=window, seed=600 + d + v)
+    x = workloads.make_inputs(w)
+    dev = torch.device("cuda:0")
+    q, k, vv, g = (t.to(dev) for t in (x.Q, x.K, x.V, x.dY))
+    bm = None if x.bitmask is None else torch.from_numpy(x.bitmask.view(np.int32)).to(dev)
+    prev = ex.set_path(path)
+    try:
+        y = torch.full((B, H, n, v), float("nan"), device=dev)
+        L = torch.full((B, H, n), float("nan"), device=dev)
+        n0 = ex.launch_count()
+        ex.fwd(q, k, vv, w.scale, mask, window, bm, y=y, L=L)
+        launches = ex.launch_count() - n0
+        dq, dk, dv = ex.bwd(q, k, vv, y, g, L, w.scale, mask, window, bm)
+        torch.cuda.synchronize()
+    finally:
+        ex.set_path(prev)
+    assert launches == (2 if path == "auto" else 1)
+    Q, K, V, G = x.as_f64()
+    Yr, Lr = dense.forward(Q, K, V, w.scale, w.mask_kind, window, x.bitmask)
+    dQ, dK, dV, _ = dense.backward(Q, K, V, G, w.scale, w.mask_kind, window, x.bitmask)
+    compare("f32", dict(Y=y, L=L, dQ=dq, dK=dk, dV=dv), dict(Y=Yr, L=Lr, dQ=dQ, dK=dK, dV=dV))
 
 
 def test_fp32_forward_then_reverse(ex):
