@@ -1269,6 +1269,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cls = cls_of(qb, kb);
         if (cls == kEmpty) continue;
         const int kc = kb * kBN + 32 * g;  // first key of this group
+        // A bit-row word is loaded before the wait for S and dP, so that the
+        // load is in flight meanwhile.
+        uint32_t bitw = 0xFFFFFFFFu;
+        if (p.mask_kind == kMaskBitmask && cls == kPartial) {
+          const int w = kb * 4 + g;
+          bitw = (i < n && w < p.words_per_row)
+                     ? __ldg(p.bits + static_cast<size_t>(i) * p.words_per_row + w)
+                     : 0u;
+        }
         if (!(ok = mbar_wait(bar(Lay::B_SDP), t & 1, abort_flag))) break;
         tc_fence_after();
         uint32_t allow = 0xFFFFFFFFu;
@@ -1276,13 +1285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           int lo = 0, hi = nk - 1;
           if (p.mask_kind == kMaskCausal || p.mask_kind == kMaskWindow) hi = min(hi, i + off);
           if (p.mask_kind == kMaskWindow) lo = max(lo, i + off - p.window + 1);
-          allow = range_bits(lo - kc, hi - kc);
-          if (p.mask_kind == kMaskBitmask) {
-            const int w = kb * 4 + g;
-            allow &= (i < n && w < p.words_per_row)
-                         ? __ldg(p.bits + static_cast<size_t>(i) * p.words_per_row + w)
-                         : 0u;
-          }
+          allow = range_bits(lo - kc, hi - kc) & bitw;
         }
         const uint32_t tD = tD0 + 128 * (t & 1) + lane_off;
         uint32_t sv[2][16], dpv[2][16];

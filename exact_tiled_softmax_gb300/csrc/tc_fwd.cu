@@ -262,19 +262,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     const int i = w.q0 + threadIdx.x;
     if (i < n) {
       const uint32_t* row = p.bits + static_cast<size_t>(i) * p.words_per_row;
-      for (int kt = w.kt_begin; kt < w.kt_end; ++kt) {
-        bool any = false, all = true;
+      // 32 blocks per table word: the row's bits for them are gathered in
+      // registers (loads unrolled, so several are in flight) and merged with
+      // one shared-memory atomic each.
+      for (int k0 = w.kt_begin & ~31; k0 < w.kt_end; k0 += 32) {
+        uint32_t anyw = 0u, notallw = 0u;
+        const int k1 = min(w.kt_end, k0 + 32);
+#pragma unroll 4
+        for (int kt = max(k0, w.kt_begin); kt < k1; ++kt) {
+          bool any = false, all = true;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int wd = kt * 4 + q;
-          const uint32_t valid = range_bits(0, nk - 1 - 32 * wd);
-          const uint32_t word = wd < p.words_per_row ? __ldg(row + wd) & valid : 0u;
-          any |= word != 0u;
-          all &= word == valid;
+          for (int q = 0; q < 4; ++q) {
+            const int wd = kt * 4 + q;
+            const uint32_t valid = range_bits(0, nk - 1 - 32 * wd);
+            const uint32_t word = wd < p.words_per_row ? __ldg(row + wd) & valid : 0u;
+            any |= word != 0u;
+            all &= word == valid;
+          }
+          anyw |= (any ? 1u : 0u) << (kt & 31);
+          notallw |= (all ? 0u : 1u) << (kt & 31);
         }
-        const int wd = X * (kMaxKT / 32) + (kt >> 5);
-        if (any) atomicOr(&cls_any[wd], 1u << (kt & 31));
-        if (!all) atomicOr(&cls_all[wd], 1u << (kt & 31));
+        const int wd = X * (kMaxKT / 32) + (k0 >> 5);
+        if (anyw) atomicOr(&cls_any[wd], anyw);
+        if (notallw) atomicOr(&cls_all[wd], notallw);
       }
     }
   }
@@ -536,7 +546,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       if (mine.valid) {
         // Key block kt of class c, whose S is in TMEM: P over S's columns, the
         // running maximum and row sum updated.
-        auto block = [&](int kt, int c) {
+        // The bit-row words of row i for key block kt (bitmask kind, PARTIAL
+        // blocks).  Loaded before the wait for S, so that the loads are in
+        // flight while the tensor pipe forms S.
+        auto bit_words = [&](int kt, int c, uint32_t (&bw)[4]) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int wd = kt * 4 + q;
+            bw[q] = 0xFFFFFFFFu;
+            if (p.mask_kind == kMaskBitmask && c == kPartial)
+              bw[q] = (i < n && wd < p.words_per_row)
+                          ? __ldg(p.bits + static_cast<size_t>(i) * p.words_per_row + wd)
+                          : 0u;
+          }
+        };
+        auto block = [&](int kt, int c, const uint32_t (&bw)[4]) {
           uint32_t s[128];
           tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
           tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
@@ -553,14 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             if (p.mask_kind == kMaskWindow) lo = max(lo, ia - p.window + 1);
             uint32_t mw[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              mw[q] = range_bits(lo - (k0 + 32 * q), hi - (k0 + 32 * q));
-              const int wd = kt * 4 + q;
-              if (p.mask_kind == kMaskBitmask)
-                mw[q] &= (i < n && wd < p.words_per_row)
-                             ? __ldg(p.bits + static_cast<size_t>(i) * p.words_per_row + wd)
-                             : 0u;
-            }
+            for (int q = 0; q < 4; ++q)
+              mw[q] = range_bits(lo - (k0 + 32 * q), hi - (k0 + 32 * q)) & bw[q];
 #pragma unroll
             for (int cc = 0; cc < 128; ++cc)
               if (!((mw[cc >> 5] >> (cc & 31)) & 1u)) s[cc] = __float_as_uint(-INFINITY);
@@ -648,11 +666,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           int c = kEmpty;
           int kt = next_block(w.kt_begin, c);
           while (kt < w.kt_end) {
+            uint32_t bw[4];
+            bit_words(kt, c, bw);
             if (!(ok = mbar_wait(bar(Lay::B_S + X), cnt & 1, abort_flag))) break;
             tc_fence_after();
             int c_next = kEmpty;
             const int kt_next = next_block(kt + 1, c_next);
-            block(kt, c);
+            block(kt, c, bw);
             kt = kt_next;
             c = c_next;
           }
@@ -660,9 +680,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           for (int kt = w.kt_begin; kt < w.kt_end; ++kt) {
             const int c = classify(p, mine, X, kt, cls_any, cls_all);
             if (c == kEmpty) continue;
+            uint32_t bw[4];
+            bit_words(kt, c, bw);
             if (!(ok = mbar_wait(bar(Lay::B_S + X), cnt & 1, abort_flag))) break;
             tc_fence_after();
-            block(kt, c);
+            block(kt, c, bw);
           }
         }
       }

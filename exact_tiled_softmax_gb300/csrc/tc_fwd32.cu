@@ -184,18 +184,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = q0 + threadIdx.x;
     if (i < n) {
       const uint32_t* row = p.bits + static_cast<size_t>(i) * p.words_per_row;
-      for (int kt = kt_begin; kt < kt_end; ++kt) {
-        bool any = false, all = true;
+      // 32 blocks per table word, gathered in registers (several loads in
+      // flight) and merged with one shared-memory atomic each.
+      for (int k0 = kt_begin & ~31; k0 < kt_end; k0 += 32) {
+        uint32_t anyw = 0u, notallw = 0u;
+        const int k1 = min(kt_end, k0 + 32);
+#pragma unroll 4
+        for (int kt = max(k0, kt_begin); kt < k1; ++kt) {
+          bool any = false, all = true;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int w = kt * 2 + q;
-          const uint32_t valid = range_bits(0, nk - 1 - 32 * w);
-          const uint32_t word = w < p.words_per_row ? __ldg(row + w) & valid : 0u;
-          any |= word != 0u;
-          all &= word == valid;
+          for (int q = 0; q < 2; ++q) {
+            const int w = kt * 2 + q;
+            const uint32_t valid = range_bits(0, nk - 1 - 32 * w);
+            const uint32_t word = w < p.words_per_row ? __ldg(row + w) & valid : 0u;
+            any |= word != 0u;
+            all &= word == valid;
+          }
+          anyw |= (any ? 1u : 0u) << (kt & 31);
+          notallw |= (all ? 0u : 1u) << (kt & 31);
         }
-        if (any) atomicOr(&cls_any[kt >> 5], 1u << (kt & 31));
-        if (!all) atomicOr(&cls_notall[kt >> 5], 1u << (kt & 31));
+        if (anyw) atomicOr(&cls_any[k0 >> 5], anyw);
+        if (notallw) atomicOr(&cls_notall[k0 >> 5], notallw);
       }
     }
   }
