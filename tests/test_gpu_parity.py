@@ -147,6 +147,26 @@ def test_one_allowed_key_per_row(ex):
     assert np.array_equal(_np(got["Y"])[0, 0], x.V.double().numpy()[0, 0][perm])
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_bitmask_tile_table_across_words(ex, dtype):
+    """n = 4500 keys: the kernels' bitmask tile tables span several 32-block
+    words (128-key blocks: 36; the fp32 forward's 64-key blocks: 71). Key blocks
+    cycle through three kinds: every pair allowed (FULL), a random 30% (PARTIAL)
+    and none but the diagonal (EMPTY for all rows except the block's own 128)."""
+    n = 4500
+    w = workloads.small(1, 1, n, 64, 64, dtype, "bitmask", 0.125, seed=21)
+    x = workloads.make_inputs(w)
+    rng = np.random.default_rng(21)
+    kind = (np.arange(n) // 128) % 3
+    allowed = np.zeros((n, n), dtype=bool)
+    allowed[:, kind == 0] = True
+    part = kind == 1
+    allowed[:, part] = rng.random((n, int(part.sum()))) < 0.3
+    allowed[np.arange(n), np.arange(n)] = True
+    x.bitmask = workloads.pack_bitmask(allowed)
+    compare(dtype, run_gpu(ex, w, x), oracle_all(w, x))
+
+
 def test_empty_allowed_set_reports_and_stays_finite(ex):
     n = 200
     w = workloads.small(1, 1, n, 64, 64, "bf16", "bitmask", 0.125, seed=5)
