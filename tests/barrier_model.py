@@ -280,6 +280,10 @@ def dq_kernel(blocks, ew_warps=3, two_ds=True, NK=3, NV=1):
             k = blocks[ti]
             if k > 0:
                 yield ("wait", "Q", nitem)
+                # delta reads this item's dY from shared memory up to its DPART
+                # arrival: the next item's Q, dY load must not have landed yet
+                # (a second completion of Q ahead shows as a missed parity).
+                yield ("wait", "Q", nitem)
                 yield ("arrive", "DPART")
                 yield ("wait", "DPART", ne)
                 ne += 1

@@ -74,18 +74,18 @@ def test_atomic_kernel_protocol_holds():
     assert _search(bm.atomic_kernel, lambda rnd: rnd.randint(0, 9), 41) == []
 
 
-@pytest.mark.parametrize("factory,drop", [(bm.dq_kernel, "QFREE"), (bm.dq_kernel, "SFREE"),
-                                           (bm.dq_kernel, "DREAD"), (bm.dq_kernel, "DPART"),
-                                           (bm.kv_kernel, "ACCFREE"), (bm.kv_kernel, "P"),
-                                           (bm.fwd_kernel, "OREAD0")])
-def test_model_catches_a_missing_wait(factory, drop):
+@pytest.mark.parametrize("factory,drop,kw", [
+    (bm.dq_kernel, "QFREE", {}), (bm.dq_kernel, "SFREE", {}), (bm.dq_kernel, "DPART", {}),
+    (bm.dq_kernel, "DREAD", {}), (bm.dq_kernel, "EPI", {}),
+    (bm.kv_kernel, "ACCFREE", {}), (bm.kv_kernel, "P", {}), (bm.fwd_kernel, "OREAD0", {})])
+def test_model_catches_a_missing_wait(factory, drop, kw):
     """Planted mistakes in the model: a role that no longer waits on one barrier
     is caught by some schedule, so the checks are not vacuous."""
     if factory is bm.fwd_kernel:
         make = lambda rnd: bm.random_fwd_items(rnd, rnd.randint(3, 8))
     else:
         make = lambda rnd: bm.random_counts(rnd, rnd.randint(3, 8), (0, 1, 2, 3))
-    assert _search(factory, make, 51, n=200, skip_waits={drop})
+    assert _search(factory, make, 51, n=200, skip_waits={drop}, **kw)
 
 
 def test_fp32_reverse_kernels_protocol_holds():
