@@ -158,9 +158,15 @@ __device__ __forceinline__ int classify(const FwdParams& p, const TileRows& t, i
 }
 
 // Item t of the forward -> (row-tile pair x, slice bh, key chunk z).  Items
-// come in groups of kHeadGroup slices; inside a group the pairs run heaviest
-// first under the causal mask (x = 0 is the last pair of rows), so the CTAs at
-// work at one time share the K and V rows of a few slices in L2.
+// come in groups of kHeadGroup slices, so the CTAs at work at one time share
+// the K and V rows of a few slices in L2.  Inside the last group the pairs run
+// heaviest first over its slices (x = 0 is the last pair of rows: the most key
+// blocks under the causal mask), which balances the end of the launch.  Under
+// the causal mask the other groups run slice by slice (heaviest pair first in
+// each), so that the items reading one slice's K and V run close together:
+// measured on B=2 H=32 n=4096, DRAM reads 308 -> 277 MB and the forward 1.3%
+// faster; with the full mask, whose items are all alike, the plain order was
+// faster.
 constexpr int kHeadGroup = 32;
 
 struct FwdItem {
@@ -177,8 +183,15 @@ __device__ __forceinline__ FwdItem make_item(const FwdParams& p, int t) {
   const int base = grp * kHeadGroup;
   const int hg = min(kHeadGroup, p.BH - base);
   const int r = t - grp * per;
-  const int x = r / hg;
-  w.bh = base + (r - x * hg);
+  int x, sl;
+  if (p.mask_kind == kMaskCausal && grp < (p.BH + kHeadGroup - 1) / kHeadGroup - 1) {
+    sl = r / p.n_qblocks;  // slice by slice
+    x = r - sl * p.n_qblocks;
+  } else {
+    x = r / hg;  // heaviest pairs first over the group's slices
+    sl = r - x * hg;
+  }
+  w.bh = base + sl;
   w.q0 = (p.n_qblocks - 1 - x) * 2 * kBM;
 #pragma unroll
   for (int X = 0; X < 2; ++X) {
