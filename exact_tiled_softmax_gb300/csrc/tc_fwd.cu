@@ -61,6 +61,7 @@ struct FwdParams {
   CUtensorMap ty;  // Y as a store target (not used in summary mode)
   unsigned* sched;  // item counter (zero at launch)
   int n, BH, n_qblocks, mask_kind, window, words_per_row;
+  int tile_rows;  // query rows per item: 2 kBM (tiles A and B), or kBM (tile A only)
   int nk, off;  // keys, and the absolute position of query 0 (nk - n)
   int dw, vw;   // columns of Q, K and of V, Y in memory (<= the kernel's D, V)
   const uint32_t* bits;
@@ -192,12 +193,12 @@ __device__ __forceinline__ FwdItem make_item(const FwdParams& p, int t) {
     sl = r - x * hg;
   }
   w.bh = base + sl;
-  w.q0 = (p.n_qblocks - 1 - x) * 2 * kBM;
+  w.q0 = (p.n_qblocks - 1 - x) * p.tile_rows;
 #pragma unroll
   for (int X = 0; X < 2; ++X) {
     w.rows[X].r0 = w.q0 + X * kBM;
     w.rows[X].r1 = min(w.q0 + X * kBM + kBM, p.n) - 1;
-    w.rows[X].valid = w.rows[X].r0 < p.n;
+    w.rows[X].valid = w.rows[X].r0 < p.n && X * kBM < p.tile_rows;
   }
   const int nkt = (p.nk + kBN - 1) / kBN;
   w.kt_begin = 0;
@@ -707,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       if (!(ok = mbar_wait(bar(Lay::B_O + X), nitem & 1, abort_flag))) break;
       tc_fence_after();
       const bool have_o = cnt > cnt0;
-      const bool valid = i < n;
+      const bool valid = mine.valid && i < n;  // tile B of a one-tile item has no rows
       if constexpr (kSum) {
         // Split-KV summary of this key chunk for row i ("Exact tiled softmax
         // attention ...", Forward procedure: the summary of a block of keys).
@@ -883,7 +884,18 @@ cudaError_t launch_tc_fwd_d(const FwdArgs& a, cudaStream_t s, int chunk_kt = 0, 
   p.dw = pr.d;
   p.vw = pr.v;
   p.BH = pr.BH;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // Items are pairs of 128-row tiles; a problem with fewer pairs than SMs runs
+  // one tile per item instead, which puts up to twice the SMs to work (the
+  // second softmax warpgroup of a CTA then idles).
+  p.tile_rows = 2 * kBM;
   p.n_qblocks = (pr.n + 2 * kBM - 1) / (2 * kBM);
+  if (chunk_kt == 0 && p.n_qblocks * pr.BH < sms && pr.n > kBM) {
+    p.tile_rows = kBM;
+    p.n_qblocks = (pr.n + kBM - 1) / kBM;
+  }
   p.mask_kind = pr.mask_kind;
   p.window = pr.window;
   p.words_per_row = pr.words_per_row;
@@ -921,12 +933,7 @@ cudaError_t launch_tc_fwd_d(const FwdArgs& a, cudaStream_t s, int chunk_kt = 0, 
   // the split-KV summaries.
   const int items = p.n_qblocks * pr.BH * p.splits;
   int grid = items;
-  if (chunk_kt == 0 && pr.mask_kind != kMaskBitmask) {
-    int dev = 0, sms = 148;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    grid = items < sms ? items : sms;
-  }
+  if (chunk_kt == 0 && pr.mask_kind != kMaskBitmask) grid = items < sms ? items : sms;
   const int role = chunk_kt > 0 ? kKernSplitPartial : kKernFwd;
   before_launch(role, s);
   kern<<<grid, kThreads, alloc, s>>>(p);
