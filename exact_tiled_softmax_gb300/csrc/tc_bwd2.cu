@@ -613,22 +613,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cb = 32 * g;
         uint32_t allow = 0xFFFFFFFFu;
         if (cls == kPartial) {
+          if (p.mask_kind == kMaskBitmask) {
+            // The warp's 32 keys share one word of every bit row: lane e loads it
+            // for query q0 + cb + e, and the transpose hands lane L (key j) bit L
+            // of each lane's word, i.e. its keys' bits over the 32 queries.
+            const int iq = q0 + cb + lane;
+            const int wd = (k0 >> 5) + wl;  // == j >> 5 for every lane of the warp
+            const uint32_t word = (iq < n && wd < p.words_per_row)
+                                      ? __ldg(p.bits + static_cast<size_t>(iq) * p.words_per_row + wd)
+                                      : 0u;
+            allow = transpose_bits32(word, lane);
+          }
           if (j >= nk) {
             allow = 0u;
           } else if (p.mask_kind == kMaskCausal) {
             allow = range_bits(j - off - q0 - cb, 31);
           } else if (p.mask_kind == kMaskWindow) {
             allow = range_bits(j - off - q0 - cb, j - off + p.window - 1 - q0 - cb);
-          } else if (p.mask_kind == kMaskBitmask) {
-            allow = 0u;
-            const uint32_t* col = p.bits + (j >> 5);
-#pragma unroll 4
-            for (int e = 0; e < 32; ++e) {
-              const int i = q0 + cb + e;
-              if (i < n)
-                allow |= ((__ldg(col + static_cast<size_t>(i) * p.words_per_row) >> (j & 31)) & 1u)
-                         << e;
-            }
           }
         }
         // The mask bits above need no product: they are formed before the wait.
