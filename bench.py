@@ -746,8 +746,11 @@ def run_gpu_decode(args, w):
         step()
     barrier()
     K = args.steps
-    # For nq <= 4 the chunk kernel merges in its last CTA per slice: no merge launch.
-    fused = w.nq <= 4
+    # The library's decode dispatch: bf16, d = v in {64, 128} and nq >= 2 run the
+    # tensor-core chunks and a merge launch; otherwise nq <= 4 runs the register
+    # kernel, which merges in its last CTA per slice (no merge launch).
+    tc = w.dtype == "bf16" and w.d == w.v and w.d in (64, 128) and w.nq > 1
+    fused = not tc and w.nq <= 4
     roles = (ex.KERNEL_SPLIT_PARTIAL,) if fused else (ex.KERNEL_SPLIT_PARTIAL,
                                                      ex.KERNEL_SPLIT_MERGE)
     ev = {r: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -805,8 +808,7 @@ def run_gpu_decode(args, w):
     e = 4 if w.dtype == "f32" else 2
     partial_bytes = w.B * w.H * (w.nq * w.d * e + w.nk * (w.d + w.v) * e)
     achieved = partial_bytes / (kern_ms[ex.KERNEL_SPLIT_PARTIAL] * 1e-3) / 1e9
-    kind = "reg" if w.nq <= 4 else ("tc" if w.dtype == "bf16" and w.d == w.v and w.d in (64, 128)
-                                     else "smem")
+    kind = "tc" if tc else ("reg" if w.nq <= 4 else "smem")
     roofline = {"kernel": f"splitkv_partial_{kind}", "bound": "hbm", "achieved": achieved,
                 "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": f"copy bandwidth, of {peak_kind}",

@@ -376,12 +376,14 @@ int check_qk_shape(const exattn_qk_shape* s) {
 }
 
 // Shapes whose chunks can run on the tensor-core forward in summary mode
-// (bf16, d = v in {64, 128}, more queries than the register kernel takes).
+// (bf16, d = v in {64, 128}, two or more queries).  A single query stays on the
+// register kernel, which streams K and V near the copy bandwidth; from two
+// queries on, the register kernel's per-lane state leaves it too few loads in
+// flight, while the tensor-core chunks stream K and V through TMA whatever nq.
 // The plan depends on the shape alone, so the workspace query and the call
 // agree whatever the kernel path setting.
 bool splitkv_tc_shape(const exattn_qk_shape* s) {
-  return s->dtype == EXATTN_BF16 && s->d == s->v && (s->d == 64 || s->d == 128) &&
-         s->nq > splitkv_reg_max_queries();
+  return s->dtype == EXATTN_BF16 && s->d == s->v && (s->d == 64 || s->d == 128) && s->nq > 1;
 }
 
 // num_splits == 0: enough chunks for about 8 waves of resident CTAs over all

@@ -222,8 +222,9 @@ int exattn_noalloc_device_status(void* cuda_stream);
  * attn_fwd_splitkv cuts the keys into `num_splits` contiguous chunks handled
  * in parallel, writes every chunk's summary (running max, running sum,
  * unnormalised output) per query row to the workspace; the summaries of all
- * chunks are then merged, skipping empty ones, into Y and L (for nq <= 4 by the
- * last CTA of each slice to finish, otherwise by a second kernel).  The
+ * chunks are then merged, skipping empty ones, into Y and L (by the last CTA
+ * of each slice to finish on the register kernel below, otherwise by a second
+ * kernel).  The
  * result is the same attention for every num_splits (up to rounding).
  *
  * Shapes: Q [B][H][nq][d], K [B][H][nk][d], V [B][H][nk][v], Y [B][H][nq][v]
@@ -236,11 +237,11 @@ int exattn_noalloc_device_status(void* cuda_stream);
  * the tensor-core shapes below, so fewer chunks may be used than asked for;
  * 0 picks enough chunks for about 8 waves of resident CTAs over all
  * batch*head slices, at least 256 keys each, from the shape alone, so the
- * workspace query and the call agree).  Kernels: nq <= 4 runs a register-
- * resident chunk kernel that merges in its last CTA per slice; bf16 with
- * d = v in {64, 128}, nq > 4 and a positive scale runs the tensor-core
- * forward in summary mode per chunk, then a merge kernel; other shapes a
- * shared-memory chunk kernel, then the merge kernel.  Rows with an empty
+ * workspace query and the call agree).  Kernels: bf16 with d = v in
+ * {64, 128}, nq >= 2 and a positive scale runs the tensor-core forward in
+ * summary mode per chunk, then a merge kernel; any other shape with nq <= 4
+ * runs a register-resident chunk kernel that merges in its last CTA per
+ * slice; the rest a shared-memory chunk kernel, then the merge kernel.  Rows with an empty
  * allowed set get Y_i = 0, L_i = -inf and the EXATTN_EMPTY_ROW status.
  * Ownership, streams and errors as for attn_fwd.
  * ------------------------------------------------------------------------- */
@@ -345,7 +346,8 @@ enum exattn_kernel {
   EXATTN_KERNEL_BWD_Q = 4,      /* the query-major dQ kernel alone (AUTO path; it also
                                    forms delta_i and L_i log2 e for the dK/dV kernel) */
   EXATTN_KERNEL_SPLIT_PARTIAL = 5, /* per-chunk summaries of attn_fwd_splitkv */
-  EXATTN_KERNEL_SPLIT_MERGE = 6,   /* the merge kernel of attn_fwd_splitkv (nq > 4) */
+  EXATTN_KERNEL_SPLIT_MERGE = 6,   /* the merge kernel of attn_fwd_splitkv (shapes
+                                     whose chunks do not merge themselves) */
   EXATTN_KERNEL_SPLIT32 = 7        /* the tf32 hi / lo split of K and V (fp32 forward) */
 };
 

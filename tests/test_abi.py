@@ -160,6 +160,8 @@ def test_splitkv_workspace_and_split_plan(lib):
     assert chunks(_qk(nq=8, nk=1000), 16) == 8       # 63 -> 128 keys
     assert chunks(_qk(B=8, H=32, nq=8, nk=16384), 0) == 5
     assert chunks(_qk(nq=8, nk=1000, d=80, v=80), 16) == 16   # not a tensor-core shape
+    assert chunks(_qk(nq=2, nk=1000), 16) == 8       # two queries: tensor-core chunks
+    assert chunks(_qk(nq=2, nk=1000, dtype=0), 16) == 16      # fp32: register kernel
     assert size(_qk(nq=65), 1) == 0            # more than 64 queries
     assert size(_qk(d=20, dtype=1), 1) == 0    # bf16 rows need 8-element pieces
     assert size(_qk(d=20, dtype=0), 1) != 0    # fp32: 4-element pieces

@@ -52,7 +52,8 @@ CASES = [
     (1, 2, 64, 300, 64, 64, "f32", "causal", 0),
     (1, 1, 3, 4099, 256, 256, "f32", "none", 0),
     (1, 1, 33, 190, 32, 16, "bf16", "bitmask", 0),
-    # nq <= 4 runs the register-resident kernel; these cover each lane-group
+    # nq <= 4 (nq = 1 only for the tensor-core shapes below) runs the
+    # register-resident kernel; these cover each lane-group
     # layout (8 or 16 lanes per key row, 32 lanes with one or two 16-byte
     # pieces each), rows wider than the pieces in use, and d != v.
     (1, 2, 2, 3000, 80, 96, "f32", "bitmask", 0),
@@ -60,8 +61,10 @@ CASES = [
     (1, 3, 4, 2500, 16, 32, "bf16", "causal", 0),
     (1, 1, 1, 2049, 128, 128, "f32", "causal", 0),
     (1, 2, 3, 1500, 64, 64, "f32", "window", 64),
-    # bf16, d = v in {64, 128}, nq > 4: chunks on the tensor-core forward (summary
+    # bf16, d = v in {64, 128}, nq >= 2: chunks on the tensor-core forward (summary
     # mode, 128-key chunks), then the merge kernel.
+    (1, 2, 2, 4100, 128, 128, "bf16", "causal", 0),
+    (2, 1, 3, 999, 64, 64, "bf16", "window", 200),
     (1, 2, 8, 1000, 128, 128, "bf16", "causal", 0),
     (2, 2, 64, 3000, 64, 64, "bf16", "bitmask", 0),
     (1, 1, 5, 129, 128, 128, "bf16", "none", 0),
@@ -84,6 +87,27 @@ def test_splitkv_matches_oracle_for_every_split_count(ex, case):
         Y, L = ex.fwd_splitkv(q, k, v_, 1 / math.sqrt(d), mask, window, bmt, num_splits=splits)
         torch.cuda.synchronize()
         _check(dtype, Y, L, Yr, Lr)
+
+
+@pytest.mark.parametrize("nq,d,mask", [(2, 128, "causal"), (4, 64, "bitmask"), (3, 128, "none")])
+def test_register_kernel_on_tensor_core_shapes(ex, nq, d, mask):
+    """With the kernel path set to SIMT, bf16 d = v in {64, 128} and nq in 2..4
+    run the register kernel on the tensor-core plan's 128-key chunks."""
+    B, H, nk = 1, 2, 1500
+    Q, K, V, bm = workloads.make_decode_inputs(B, H, nq, nk, d, d, "bf16", mask, seed=40 + nq)
+    Yr, Lr = dense.forward_rect(*(t.double().numpy() for t in (Q, K, V)), 1 / math.sqrt(d),
+                                workloads.MASK_KINDS[mask], 0, bm)
+    dev = torch.device("cuda:0")
+    q, k, v_ = (t.to(dev) for t in (Q, K, V))
+    bmt = None if bm is None else torch.from_numpy(bm.view(np.int32)).to(dev)
+    prev = ex.set_path("simt")
+    try:
+        for splits in (1, 3, 0):
+            Y, L = ex.fwd_splitkv(q, k, v_, 1 / math.sqrt(d), mask, 0, bmt, num_splits=splits)
+            torch.cuda.synchronize()
+            _check("bf16", Y, L, Yr, Lr)
+    finally:
+        ex.set_path(prev)
 
 
 @pytest.mark.parametrize("nq,nk", [(8, 5), (4, 2), (20, 7)])
