@@ -308,9 +308,10 @@ def run_reference(args, w):
 METRIC = "attention TFLOP/s fwd+bwd (fwd alone in fwd_tflops) at 1 GB300; % of dense BF16 peak"
 
 
-def read_traffic(kernel_tag):
-    """DRAM bytes per launch from the committed ncu summary, if it still matches
-    the current kernel source (null otherwise)."""
+def read_traffic(kernel_tag, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken for
+    this workload's launch and still matches the current kernel source (null
+    otherwise)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
@@ -323,7 +324,7 @@ def read_traffic(kernel_tag):
         kv = dict(p.split("=", 1) for p in line.split() if "=" in p)
         entries[kv.get("kernel")] = kv
     e = entries.get(kernel_tag)
-    if e is None:
+    if e is None or e.get("launch") != workload:
         return None
     src = os.path.join(ROOT, "exact_tiled_softmax_gb300", "csrc", e.get("source", ""))
     if not os.path.exists(src):
@@ -356,7 +357,7 @@ def kernel_roofline(args, w, which, achieved, peaks, peak_kind):
         out = {"kernel": tag, "bound": "tensor", "achieved": achieved, "peak": bf16_peak,
                "unit": "TFLOP/s", "frac": achieved / bf16_peak,
                "peak_kind": f"bf16 dense burst, of {peak_kind}",
-               "traffic": None if padded else read_traffic(tag)}
+               "traffic": None if padded else read_traffic(tag, w.name)}
         if padded:
             out["padded_to"] = 64 if w.d <= 64 and w.v <= 64 else 128
         return out
@@ -367,7 +368,7 @@ def kernel_roofline(args, w, which, achieved, peaks, peak_kind):
                 "peak_kind": f"tf32 dense = bf16 burst of {peak_kind} x 1.1/2.25 (nominal ratio)",
                 "tensor_work_frac": 3 * achieved / peak,
                 "note": "3xTF32: the tensor pipe runs three tf32 products per product",
-                "traffic": read_traffic("tc32_fwd")}
+                "traffic": read_traffic("tc32_fwd", w.name)}
     if (w.dtype == "f32" and which == "bwd" and args.path == "auto" and not args.dropout
             and w.d == 64 and w.v == 64):
         peak = bf16_peak * TF32_OVER_BF16
@@ -377,13 +378,13 @@ def kernel_roofline(args, w, which, achieved, peaks, peak_kind):
                 "tensor_work_frac": 21 / 5 * achieved / peak,
                 "note": "3xTF32 reverse: 7 products per tile (S, dP twice; dV, dK, dQ), "
                         "three tf32 products each, against the convention's 5",
-                "traffic": read_traffic("tc32_bwd")}
+                "traffic": read_traffic("tc32_bwd", w.name)}
     mhz = float(peaks.get("sm_max_mhz", 2070.0))
     peak = 152 * 128 * 2 * mhz * 1e6 / 1e12
     return {"kernel": f"simt_{which}", "bound": "alu", "achieved": achieved, "peak": peak,
             "unit": "TFLOP/s", "frac": achieved / peak,
             "peak_kind": f"fp32 FMA: 152 SMs x 128 lanes x 2 flop x {mhz:.0f} MHz",
-            "traffic": read_traffic(f"simt_{which}")}
+            "traffic": read_traffic(f"simt_{which}", w.name)}
 
 
 def host_link(stream, h_in, d_in, h_out, d_out, reps=5):
@@ -812,7 +813,7 @@ def run_gpu_decode(args, w):
     roofline = {"kernel": f"splitkv_partial_{kind}", "bound": "hbm", "achieved": achieved,
                 "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": f"copy bandwidth, of {peak_kind}",
-                "traffic": read_traffic(f"splitkv_partial_{kind}"),
+                "traffic": read_traffic(f"splitkv_partial_{kind}", w.name),
                 "kernel_ms": {"partial": kern_ms[ex.KERNEL_SPLIT_PARTIAL],
                               "merge": "in the chunk kernel" if fused
                               else kern_ms[ex.KERNEL_SPLIT_MERGE]}}

@@ -11,7 +11,7 @@ PEAKS = {"bf16_tflops": 1856.1, "sm_max_mhz": 2070.0}
 
 
 def _w(d, v, dtype="bf16"):
-    return types.SimpleNamespace(d=d, v=v, dtype=dtype)
+    return types.SimpleNamespace(d=d, v=v, dtype=dtype, name=f"attn-d{d}-v{v}-{dtype}")
 
 
 def _args(path="auto", dropout=0.0):
@@ -23,7 +23,7 @@ def no_traffic(monkeypatch):
     """read_traffic stubbed: records the tags asked for, answers 1.0."""
     asked = []
 
-    def fake(tag):
+    def fake(tag, workload):
         asked.append(tag)
         return 1.0
 
@@ -98,8 +98,9 @@ def test_fp32_reverse_of_width_64_is_the_3xtf32_kernel_pair(no_traffic):
         assert bench.kernel_roofline(args, w, "bwd", 1.0, PEAKS, "measured")["kernel"] == "simt_bwd"
 
 
-def test_read_traffic_rejects_a_changed_source(tmp_path, monkeypatch):
-    """An entry counts only while its kernel source hashes to the recorded prefix."""
+def test_read_traffic_rejects_a_changed_source_or_another_launch(tmp_path, monkeypatch):
+    """An entry counts only for the workload launch it was taken on, and only
+    while its kernel source hashes to the recorded prefix."""
     import hashlib
     csrc = tmp_path / "exact_tiled_softmax_gb300" / "csrc"
     csrc.mkdir(parents=True)
@@ -109,9 +110,25 @@ def test_read_traffic_rejects_a_changed_source(tmp_path, monkeypatch):
     sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
     (tmp_path / "profiles" / "ncu_traffic.txt").write_text(
         "# comment\n"
-        f"kernel=tc_fwd source=k.cu source_sha={sha} bytes_per_launch=12345 measured_on=x\n")
+        f"kernel=tc_fwd launch=attn-x source=k.cu source_sha={sha} bytes_per_launch=12345 "
+        "measured_on=x\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.read_traffic("tc_fwd") == 12345.0
-    assert bench.read_traffic("tc_bwd_split") is None
+    assert bench.read_traffic("tc_fwd", "attn-x") == 12345.0
+    assert bench.read_traffic("tc_fwd", "attn-y") is None
+    assert bench.read_traffic("tc_bwd_split", "attn-x") is None
     src.write_bytes(b"__global__ void k() { }\n")
-    assert bench.read_traffic("tc_fwd") is None
+    assert bench.read_traffic("tc_fwd", "attn-x") is None
+
+
+def test_committed_traffic_entries_name_bench_workloads():
+    """Every committed entry names the launch of a workload that bench.py runs."""
+    import workloads
+    names = {workloads.workload(3).name, workloads.decode_workload(1).name,
+             workloads.decode_workload(4).name,
+             workloads.workload(3).name + "-as-f32", workloads.workload(2).name + "-as-f32"}
+    path = bench.os.path.join(bench.ROOT, "profiles", "ncu_traffic.txt")
+    entries = [dict(p.split("=", 1) for p in line.split())
+               for line in open(path) if line.strip() and not line.startswith("#")]
+    assert entries
+    for e in entries:
+        assert e.get("launch") in names, e
