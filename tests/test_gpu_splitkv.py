@@ -65,6 +65,8 @@ CASES = [
     # mode, 128-key chunks), then the merge kernel.
     (1, 2, 2, 4100, 128, 128, "bf16", "causal", 0),
     (2, 1, 3, 999, 64, 64, "bf16", "window", 200),
+    (1, 1, 4, 2100, 64, 64, "bf16", "bitmask", 0),
+    (2, 2, 2, 260, 128, 128, "bf16", "none", 0),
     (1, 2, 8, 1000, 128, 128, "bf16", "causal", 0),
     (2, 2, 64, 3000, 64, 64, "bf16", "bitmask", 0),
     (1, 1, 5, 129, 128, 128, "bf16", "none", 0),
@@ -143,11 +145,11 @@ def test_splitkv_agrees_with_last_rows_of_full_forward(ex, nq):
     assert (L_dec - L_full[:, :, -nq:]).abs().max() <= 1e-4
 
 
-@pytest.mark.parametrize("nq", [1, 16])
+@pytest.mark.parametrize("nq", [1, 4, 16])
 def test_decode_benchmark_size_sampled_heads(ex, nq):
     """bench.py --decode (B=8, H=32, nk=16384, d=v=128, bf16, causal, automatic
-    chunk count): the register kernel for nq = 1, the tensor-core chunks for 16;
-    sampled heads against the oracle."""
+    chunk count): the register kernel for nq = 1, the tensor-core chunks for 4
+    and 16; sampled heads against the oracle."""
     from sampling import head_slices
     w = workloads.decode_workload(nq)
     Q, K, V, _ = workloads.make_decode_inputs(w.B, w.H, w.nq, w.nk, w.d, w.v, w.dtype, w.mask,
