@@ -154,7 +154,7 @@ def test_splitkv_workspace_and_split_plan(lib):
     assert chunks(_qk(B=1, H=1, nk=1000), 0) == 4
     assert chunks(_qk(B=64, H=64, nk=1000), 0) == 2
     assert chunks(_qk(B=128, H=64, nk=1000), 0) == 1
-    # bf16, d = v = 128, nq > 4 (tensor-core chunks): chunks are multiples of 128
+    # bf16, d = v = 128, nq >= 2 (tensor-core chunks): chunks are multiples of 128
     # keys, and auto aims at 8 waves of one CTA per SM (1216 CTAs).
     assert chunks(_qk(nq=8, nk=1000), 4) == 4        # 250 -> 256 keys
     assert chunks(_qk(nq=8, nk=1000), 16) == 8       # 63 -> 128 keys
