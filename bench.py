@@ -711,6 +711,17 @@ def run_reference_decode(args, w):
     print(json.dumps(line), flush=True)
 
 
+def decode_kernels(w):
+    """The split-KV kernels the library runs for a decode workload (kernel path
+    "auto", positive scale): bf16 with d = v in {64, 128} and nq >= 2 takes the
+    tensor-core chunks and a merge launch ("tc"); otherwise nq <= 4 takes the
+    register kernel, which merges in its last CTA per slice ("reg"), and larger nq
+    the shared-memory chunk kernel and a merge launch ("smem")."""
+    if w.dtype == "bf16" and w.d == w.v and w.d in (64, 128) and w.nq > 1:
+        return "tc"
+    return "reg" if w.nq <= 4 else "smem"
+
+
 def run_gpu_decode(args, w):
     import exact_tiled_softmax_gb300 as ex
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -747,11 +758,8 @@ def run_gpu_decode(args, w):
         step()
     barrier()
     K = args.steps
-    # The library's decode dispatch: bf16, d = v in {64, 128} and nq >= 2 run the
-    # tensor-core chunks and a merge launch; otherwise nq <= 4 runs the register
-    # kernel, which merges in its last CTA per slice (no merge launch).
-    tc = w.dtype == "bf16" and w.d == w.v and w.d in (64, 128) and w.nq > 1
-    fused = not tc and w.nq <= 4
+    kind = decode_kernels(w)
+    fused = kind == "reg"  # the register kernel merges in its last CTA per slice
     roles = (ex.KERNEL_SPLIT_PARTIAL,) if fused else (ex.KERNEL_SPLIT_PARTIAL,
                                                      ex.KERNEL_SPLIT_MERGE)
     ev = {r: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -809,7 +817,6 @@ def run_gpu_decode(args, w):
     e = 4 if w.dtype == "f32" else 2
     partial_bytes = w.B * w.H * (w.nq * w.d * e + w.nk * (w.d + w.v) * e)
     achieved = partial_bytes / (kern_ms[ex.KERNEL_SPLIT_PARTIAL] * 1e-3) / 1e9
-    kind = "tc" if tc else ("reg" if w.nq <= 4 else "smem")
     roofline = {"kernel": f"splitkv_partial_{kind}", "bound": "hbm", "achieved": achieved,
                 "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": f"copy bandwidth, of {peak_kind}",

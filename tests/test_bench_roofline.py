@@ -132,3 +132,29 @@ def test_committed_traffic_entries_name_bench_workloads():
     assert entries
     for e in entries:
         assert e.get("launch") in names, e
+
+
+def test_decode_kernel_rule_matches_the_library_plan():
+    """bench.py names the decode kernels from the shape; the library's plan tells
+    the tensor-core chunks apart (whole 128-key chunks, against 32 keys for the
+    other kernels).  With nk = 1000 and 16 chunks asked for, a 128-key plan
+    gives 8 chunks and a 32-key plan 16."""
+    import ctypes
+    import dataclasses
+    import exact_tiled_softmax_gb300 as ex
+    import workloads
+    lib = ex.load_library()
+    base = workloads.decode_workload(1)
+    for dtype in ("bf16", "f32"):
+        for d, v in ((64, 64), (128, 128), (80, 96), (128, 64), (32, 32)):
+            for nq in (1, 2, 3, 4, 5, 16, 64):
+                w = dataclasses.replace(base, B=1, H=1, nq=nq, nk=1000, d=d, v=v, dtype=dtype)
+                shape = ex.QKShape(1, 1, nq, 1000, d, v, 0 if dtype == "f32" else 1)
+                size = lib.exattn_splitkv_workspace_size(ctypes.byref(shape), 16)
+                assert size > 0
+                rows = nq
+                body = size - 256 - 256 - 2 * ((4 * rows * 16 + 255) // 256 * 256)
+                chunks = 8 if body < 16 * rows * 4 * v else 16
+                kind = bench.decode_kernels(w)
+                assert (kind == "tc") == (chunks == 8), (dtype, d, v, nq, kind, chunks)
+                assert kind == "tc" or kind == ("reg" if nq <= 4 else "smem")
