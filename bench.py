@@ -317,7 +317,9 @@ def read_traffic(kernel_tag, workload):
     if not os.path.exists(path):
         return None
     entries = {}
-    for line in open(path):
+    with open(path) as f:
+        lines = f.read().splitlines()
+    for line in lines:
         line = line.strip()
         if not line or line.startswith("#"):
             continue
@@ -329,7 +331,8 @@ def read_traffic(kernel_tag, workload):
     src = os.path.join(ROOT, "exact_tiled_softmax_gb300", "csrc", e.get("source", ""))
     if not os.path.exists(src):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
     if sha != e.get("source_sha"):
         return None
     return float(e["bytes_per_launch"])

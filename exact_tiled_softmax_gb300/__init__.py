@@ -188,6 +188,31 @@ def _check_shapes(q, k, v, y=None, dy=None, L=None, dq=None, dk=None, dv=None, s
             raise ValueError("L must be a contiguous float32 tensor on q's device")
 
 
+_WORD_DTYPES = (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
+
+
+def _check_aux(q, nk, kind, bitmask=None, ws=None, bitmask_device=None):
+    """The bitmask and the workspace, which the library takes as bare pointers:
+    the bitmask must be 32-bit words, contiguous, on ``bitmask_device`` (default:
+    q's device) and, for the bitmask mask kind, hold at least nq * ceil(nk / 32)
+    words (the kernels read that many); the workspace must be contiguous and on
+    q's device.  Raises ValueError before anything reaches the library."""
+    if bitmask is not None:
+        dev = q.device if bitmask_device is None else bitmask_device
+        if (bitmask.dtype not in _WORD_DTYPES or not bitmask.is_contiguous()
+                or bitmask.device != dev):
+            raise ValueError(f"bitmask must be contiguous 32-bit words on {dev}")
+        need = q.shape[2] * ((nk + 31) // 32)
+        if kind == MASK_BITMASK and bitmask.numel() < need:
+            raise ValueError(f"bitmask holds {bitmask.numel()} words, the mask needs {need}")
+    if ws is not None and (ws.device != q.device or not ws.is_contiguous()):
+        raise ValueError("the workspace must be a contiguous tensor on q's device")
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
 def _stream(stream):
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
@@ -217,7 +242,7 @@ def _fwd_qk(lib, q, k, v, scale, kind, window, bitmask, y, L, ws, stream, dropou
         ws = workspace(lib.exattn_fwd_qk_workspace_size(ctypes.byref(shape), kind), q.device)
     st = lib.attn_fwd_qk(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale), kind,
                          int(window), _ptr(bitmask), float(dropout_p), int(seed), _ptr(y),
-                         _ptr(L), _ptr(ws), ws.numel(), _stream(stream))
+                         _ptr(L), _ptr(ws), _nbytes(ws), _stream(stream))
     if st != 0:
         raise ExattnError(st, "attn_fwd_qk")
     return y, L
@@ -234,7 +259,7 @@ def _bwd_qk(lib, q, k, v, y, dy, L, scale, kind, window, bitmask, dq, dk, dv, ws
     st = lib.attn_bwd_qk(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(dy),
                          _ptr(L), float(scale), kind, int(window), _ptr(bitmask),
                          float(dropout_p), int(seed), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
-                         ws.numel(), _stream(stream))
+                         _nbytes(ws), _stream(stream))
     if st != 0:
         raise ExattnError(st, "attn_bwd_qk")
     return dq, dk, dv
@@ -250,6 +275,7 @@ def fwd(q, k, v, scale, mask="none", window=0, bitmask=None, y=None, L=None, ws=
     _check((q, k, v, y), q.dtype, q.device)
     _check_shapes(q, k, v, y=y, L=L)
     kind = _mask_kind(mask)
+    _check_aux(q, k.shape[2], kind, bitmask, ws)
     if k.shape[2] != q.shape[2]:
         return _fwd_qk(lib, q, k, v, scale, kind, window, bitmask, y, L, ws, stream, dropout_p,
                        seed)
@@ -264,10 +290,10 @@ def fwd(q, k, v, scale, mask="none", window=0, bitmask=None, y=None, L=None, ws=
     if dropout_p:
         st = lib.attn_fwd_dropout(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale),
                                   kind, int(window), _ptr(bitmask), float(dropout_p), int(seed),
-                                  _ptr(y), _ptr(L), _ptr(ws), ws.numel(), _stream(stream))
+                                  _ptr(y), _ptr(L), _ptr(ws), _nbytes(ws), _stream(stream))
     else:
         st = lib.attn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale), kind,
-                          int(window), _ptr(bitmask), _ptr(y), _ptr(L), _ptr(ws), ws.numel(),
+                          int(window), _ptr(bitmask), _ptr(y), _ptr(L), _ptr(ws), _nbytes(ws),
                           _stream(stream))
     if st != 0:
         raise ExattnError(st, "attn_fwd_dropout" if dropout_p else "attn_fwd")
@@ -282,6 +308,7 @@ def bwd(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, dq=None, 
     _check((q, k, v, y, dy, dq, dk, dv), q.dtype, q.device)
     _check_shapes(q, k, v, y=y, dy=dy, L=L, dq=dq, dk=dk, dv=dv)
     kind = _mask_kind(mask)
+    _check_aux(q, k.shape[2], kind, bitmask, ws)
     if k.shape[2] != q.shape[2]:
         return _bwd_qk(lib, q, k, v, y, dy, L, scale, kind, window, bitmask, dq, dk, dv, ws,
                        stream, dropout_p, seed)
@@ -296,11 +323,11 @@ def bwd(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, dq=None, 
         st = lib.attn_bwd_dropout(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(y),
                                   _ptr(dy), _ptr(L), float(scale), kind, int(window),
                                   _ptr(bitmask), float(dropout_p), int(seed), _ptr(dq), _ptr(dk),
-                                  _ptr(dv), _ptr(ws), ws.numel(), _stream(stream))
+                                  _ptr(dv), _ptr(ws), _nbytes(ws), _stream(stream))
     else:
         st = lib.attn_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(dy),
                           _ptr(L), float(scale), kind, int(window), _ptr(bitmask), _ptr(dq),
-                          _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream))
+                          _ptr(dk), _ptr(dv), _ptr(ws), _nbytes(ws), _stream(stream))
     if st != 0:
         raise ExattnError(st, "attn_bwd")
     return dq, dk, dv
@@ -319,6 +346,7 @@ def fwd_splitkv(q, k, v, scale, mask="none", window=0, bitmask=None, num_splits=
     B, H, nq, d = q.shape
     shape = QKShape(B, H, nq, k.shape[2], d, v.shape[-1], _DTYPES[q.dtype])
     kind = _mask_kind(mask)
+    _check_aux(q, k.shape[2], kind, bitmask, ws)
     if y is None:
         y = torch.empty((B, H, nq, v.shape[-1]), dtype=q.dtype, device=q.device)
     if L is None:
@@ -328,7 +356,7 @@ def fwd_splitkv(q, k, v, scale, mask="none", window=0, bitmask=None, num_splits=
                        q.device)
     st = lib.attn_fwd_splitkv(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale), kind,
                               int(window), _ptr(bitmask), int(num_splits), _ptr(y), _ptr(L),
-                              _ptr(ws), ws.numel(), _stream(stream))
+                              _ptr(ws), _nbytes(ws), _stream(stream))
     if st != 0:
         raise ExattnError(st, "attn_fwd_splitkv")
     return y, L
@@ -344,6 +372,7 @@ def bwd_noalloc(q, k, v, y, dy, L, scale, mask="none", window=0, bitmask=None, d
     lib = load_library()
     _check((q, k, v, y, dy, dq, dk, dv), q.dtype, q.device)
     _check_shapes(q, k, v, y=y, dy=dy, L=L, dq=dq, dk=dk, dv=dv, same_n=True)
+    _check_aux(q, k.shape[2], _mask_kind(mask), bitmask)
     shape = _shape(q, v)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -379,14 +408,17 @@ def step_host(q, k, v, dy, scale, mask="none", window=0, bitmask=None, out=None,
     synchronise ``stream`` (default: the current stream of ``device``) before
     reading the outputs."""
     lib = load_library()
-    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
     for t in (q, k, v, dy):
         if t.device.type != "cpu" or not t.is_contiguous() or t.dtype != q.dtype:
             raise ValueError("step_host takes contiguous CPU tensors of one dtype")
-    if bitmask is not None and bitmask.device.type != "cpu":
-        raise ValueError("step_host takes the bitmask on the CPU")
     _check_shapes(q, k, v, dy=dy, same_n=True)
     kind = _mask_kind(mask)
+    _check_aux(q, k.shape[2], kind, bitmask, bitmask_device=torch.device("cpu"))
+    if ws is not None and (ws.device != dev or not ws.is_contiguous()):
+        raise ValueError("the workspace must be a contiguous tensor on the step's device")
     shape = _shape(q, v)
     if out is None:
         pin = torch.cuda.is_available()
@@ -396,13 +428,22 @@ def step_host(q, k, v, dy, scale, mask="none", window=0, bitmask=None, out=None,
                torch.empty(k.shape, dtype=q.dtype, pin_memory=pin),
                torch.empty(v.shape, dtype=q.dtype, pin_memory=pin))
     y, L, dq, dk, dv = out
+    rows = tuple(q.shape[:-1])
+    want = {"y": (rows + (v.shape[-1],), q.dtype), "L": (rows, torch.float32),
+            "dq": (tuple(q.shape), q.dtype), "dk": (tuple(k.shape), q.dtype),
+            "dv": (tuple(v.shape), q.dtype)}
+    for name, t in zip(("y", "L", "dq", "dk", "dv"), out):
+        if ((tuple(t.shape), t.dtype) != want[name] or t.device.type != "cpu"
+                or not t.is_contiguous()):
+            raise ValueError(f"out {name} must be a contiguous CPU tensor of shape "
+                             f"{want[name][0]} and dtype {want[name][1]}")
     need = lib.exattn_host_step_workspace_size(ctypes.byref(shape), kind)
     if ws is None:
         ws = workspace(need, dev)
     s = torch.cuda.current_stream(dev) if stream is None else stream
     st = lib.attn_step_host(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(dy), float(scale),
                             kind, int(window), _ptr(bitmask), _ptr(y), _ptr(L), _ptr(dq), _ptr(dk),
-                            _ptr(dv), _ptr(ws), ws.numel(), ctypes.c_void_p(s.cuda_stream))
+                            _ptr(dv), _ptr(ws), _nbytes(ws), ctypes.c_void_p(s.cuda_stream))
     if st != 0:
         raise ExattnError(st, "attn_step_host")
     return y, L, dq, dk, dv

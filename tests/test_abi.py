@@ -21,7 +21,8 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text,
                        flags=re.M)
@@ -223,3 +224,53 @@ def test_binding_rejects_mismatched_shapes_before_any_launch(lib, bad):
         with pytest.raises(ValueError):
             ex.bwd(t["q"], t["k"], t["v"], t["y"], t["dy"], t["L"], 0.1, "causal", dq=t["dq"])
     assert lib.exattn_launch_count() == count
+
+
+def test_binding_rejects_bad_bitmasks_workspaces_and_outputs_before_the_library():
+    """The library takes the bitmask, the workspace and step_host's outputs as
+    bare pointers and sizes it trusts, so the binding checks them first: these
+    calls raise ValueError on CPU tensors without reaching any CUDA call."""
+    import torch
+    import exact_tiled_softmax_gb300 as ex
+    q = torch.zeros(1, 2, 100, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 2, 100, 64, dtype=torch.bfloat16)
+    words = 100 * 4  # rows x ceil(100 / 32)
+    short = torch.zeros(words - 1, dtype=torch.int32)
+    wide = torch.zeros(words, dtype=torch.int64)
+    strided = torch.zeros(2 * words, dtype=torch.int32)[::2]
+    for bm in (short, wide, strided):
+        with pytest.raises(ValueError):
+            ex.fwd(q, k, k, 0.1, "bitmask", 0, bm)
+        with pytest.raises(ValueError):
+            ex.bwd(q, k, k, q, q, torch.zeros(1, 2, 100), 0.1, "bitmask", 0, bm)
+    # decode shape: 3 query rows against 1000 keys read 3 * 32 words
+    qd = torch.zeros(1, 2, 3, 64, dtype=torch.bfloat16)
+    kd = torch.zeros(1, 2, 1000, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ex.fwd_splitkv(qd, kd, kd, 0.1, "bitmask", 0, torch.zeros(3 * 32 - 1, dtype=torch.int32))
+    ex._check_aux(qd, 1000, ex.MASK_BITMASK, torch.zeros(3, 32, dtype=torch.int32))
+    ex._check_aux(q, 100, ex.MASK_BITMASK, torch.zeros(100, 4, dtype=torch.int32))
+    # another kind of mask reads no words: only the form of a given bitmask is checked
+    ex._check_aux(q, 100, ex.MASK_CAUSAL, torch.zeros(1, dtype=torch.int32))
+    with pytest.raises(ValueError):
+        ex._check_aux(q, 100, ex.MASK_CAUSAL, wide)
+    # a workspace on another device than q
+    with pytest.raises(ValueError):
+        ex._check_aux(q, 100, ex.MASK_CAUSAL, None, torch.zeros(1, dtype=torch.uint8,
+                                                                 device="meta"))
+    # step_host: outputs of the wrong shape, dtype or place
+    dev = torch.device("cuda", 0)
+    good = (torch.zeros(1, 2, 100, 64, dtype=torch.bfloat16), torch.zeros(1, 2, 100),
+            torch.zeros(1, 2, 100, 64, dtype=torch.bfloat16),
+            torch.zeros(1, 2, 100, 64, dtype=torch.bfloat16),
+            torch.zeros(1, 2, 100, 64, dtype=torch.bfloat16))
+    for i, bad in ((0, torch.zeros(1, 2, 99, 64, dtype=torch.bfloat16)),
+                   (1, torch.zeros(1, 2, 100, dtype=torch.float64)),
+                   (3, torch.zeros(1, 2, 100, 32, dtype=torch.bfloat16)),
+                   (4, torch.zeros(1, 2, 64, 100, dtype=torch.bfloat16).transpose(2, 3))):
+        out = list(good)
+        out[i] = bad
+        with pytest.raises(ValueError):
+            ex.step_host(q, k, k, q, 0.1, "causal", out=tuple(out), device=dev)
+    with pytest.raises(ValueError):
+        ex.step_host(q, k, k, q, 0.1, "bitmask", 0, short, out=good, device=dev)

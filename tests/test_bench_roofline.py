@@ -127,8 +127,9 @@ def test_committed_traffic_entries_name_bench_workloads():
              workloads.decode_workload(4).name,
              workloads.workload(3).name + "-as-f32", workloads.workload(2).name + "-as-f32"}
     path = bench.os.path.join(bench.ROOT, "profiles", "ncu_traffic.txt")
-    entries = [dict(p.split("=", 1) for p in line.split())
-               for line in open(path) if line.strip() and not line.startswith("#")]
+    with open(path) as f:
+        entries = [dict(p.split("=", 1) for p in line.split())
+                   for line in f if line.strip() and not line.startswith("#")]
     assert entries
     for e in entries:
         assert e.get("launch") in names, e

@@ -21,6 +21,11 @@ from workloads import pack_bitmask
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
+def _load(path):
+    with open(path) as f:
+        return json.load(f)
+
+
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_cases.json")
 KINDS = {"none": masks.NONE, "causal": masks.CAUSAL}
 
@@ -60,7 +65,7 @@ def test_hand_cases_rederived_exactly():
         dQ.append(sum(gam[j] * K[j] for j in range(3)))
         for j in range(3):
             dV[j] += p[j] * G[i]
-    case = json.load(open(GOLDEN))["cases"][2]
+    case = _load(GOLDEN)["cases"][2]
     assert [Fraction(s) for s in case["Y"]] == Y
     assert [Fraction(s) for s in case["dQ"]] == dQ
     assert [Fraction(s) for s in case["dV"]] == dV
@@ -69,7 +74,7 @@ def test_hand_cases_rederived_exactly():
     Vv = [Fraction(1), Fraction(0)]
     Yf = [sum(p[i][j] * Vv[j] for j in range(2)) for i in range(2)]
     gam = [[p[i][j] * (Vv[j] - Yf[i]) for j in range(2)] for i in range(2)]
-    case = json.load(open(GOLDEN))["cases"][0]
+    case = _load(GOLDEN)["cases"][0]
     assert [Fraction(s) for s in case["Y"]] == Yf
     # dK_j = sum_i gamma_ij Q_i with Q = (1, 0)
     assert [Fraction(s) for s in case["dK"]] == [gam[0][0], gam[0][1]]
@@ -80,7 +85,7 @@ def test_hand_cases_rederived_exactly():
 
 def _hand_failures(head_forward, head_backward):
     out = []
-    for case in json.load(open(GOLDEN))["cases"]:
+    for case in _load(GOLDEN)["cases"]:
         arr = {k: np.array([[_expr(x) for x in row] for row in case[k]])
                for k in ("Q", "K", "V", "G")}
         n = arr["Q"].shape[0]
@@ -393,7 +398,7 @@ def test_row_backward_against_torch_autograd_and_hand_cases():
         delta = np.array([x[1] for x in rows])
         assert _rel(dq, tdq) <= 1e-12, kind
         assert _rel(delta, (G * Yt).sum(axis=1)) <= 1e-12, kind
-    for case in json.load(open(GOLDEN))["cases"]:
+    for case in _load(GOLDEN)["cases"]:
         arr = {k: np.array([[_expr(x) for x in row] for row in case[k]])
                for k in ("Q", "K", "V", "G")}
         n = arr["Q"].shape[0]
@@ -569,14 +574,14 @@ def _hex(xs):
 
 
 def test_philox_known_answer_vectors():
-    cases = json.load(open(DROPOUT_GOLDEN))["philox4x32_10"]
+    cases = _load(DROPOUT_GOLDEN)["philox4x32_10"]
     for c in cases:
         got = philox.philox4x32_10(_hex(c["ctr"]), _hex(c["key"]))
         assert np.array_equal(got, _hex(c["out"])), c
 
 
 def test_dropout_mask_layout_golden():
-    c = json.load(open(DROPOUT_GOLDEN))["mask_case"]
+    c = _load(DROPOUT_GOLDEN)["mask_case"]
     u = philox.random_u16(c["bh"], c["row"] + 1, 8, c["seed"])[c["row"]]
     assert np.array_equal(u, _hex(c["u16"]))
     assert philox.threshold(c["q"]) == c["threshold"]
